@@ -1,0 +1,527 @@
+#!/usr/bin/env python3
+"""Benchmark of the small-M NVFP4 W4A4 decode linear on GB300.
+
+Workload (one "step"): one decode step of an 8B-shaped model at M = 1 -- the
+four decode linears (qkv 4096->6144, o 4096->4096, gate_up 4096->24576,
+down 12288->4096) of each of 36 layers with distinct seeded weights, each
+call an on-the-fly activation quantisation followed by the small-M GEMM, all
+replayed as one CUDA graph.  The packed weights (3.9 GB) are far larger than
+L2, so every step streams them from HBM.
+
+Printed: one JSON line (rank 0).  ``value`` is the achieved HBM throughput of
+the whole step over its algorithmic bytes (GB/s, higher is better);
+``detail.per_linear`` has the microseconds per call of each linear shape.
+
+``--impl reference`` times the CPU oracle instead (the only reference that
+exists for this method here), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "NVFP4 W4A4 small-M linear µs/call and HBM GB/s (% of roofline), M=1..8"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("8B-shaped decode linears qkv/o/gate_up/down (K->N 4096->6144, 4096->4096, "
+            "4096->24576, 12288->4096), M=1, act-quantize + GEMM per call, 36 layers of "
+            "distinct weights per step under one CUDA graph")
+
+
+def algorithmic_bytes(m: int, n: int, k: int) -> dict:
+    """Bytes a call must move at minimum: packed weights and scales once,
+    packed activations, both tensor scales, FP32 output; and the activation
+    quantiser's FP32 read plus packed write."""
+    wbytes = n * k // 2 + n * k // 16
+    gemm = wbytes + m * k // 2 + m * k // 16 + 8 + 4 * m * n
+    quant = 4 * m * k + m * k // 2 + m * k // 16 + 4
+    return {"weights": wbytes, "gemm": gemm, "quant": quant}
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+            if hbm:
+                return {"hbm_gbs": float(hbm), "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
+                "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [s.strip() for s in line.split(",")]
+                if len(p) < len(CLOCK_FIELDS):
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, p[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: every rank runs its own copy of the step)
+# ---------------------------------------------------------------------------
+
+def dist_setup(gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class DecodeStack:
+    """36 layers x 4 linears of packed weights resident in HBM, per-call
+    activation buffers, and the graphs that replay them."""
+
+    def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234):
+        self.nv, self.torch = nv, torch
+        self.m = m
+        self.layers = layers
+        self.lins = synthetic.LINEARS_8B
+        dev = torch.device("cuda")
+        gen = torch.Generator(device=dev)
+        self.w = []          # [layer][j] -> (wq, ws, wg)
+        for l in range(layers):
+            row = []
+            for j, lin in enumerate(self.lins):
+                gen.manual_seed(synthetic.weight_seed(seed, l, j))
+                wf = torch.randn((lin.n, lin.k), generator=gen, device=dev, dtype=torch.float32)
+                wf.mul_(synthetic.WEIGHT_STD_8B)
+                row.append(nv.pack_weight(wf))
+                del wf
+            self.w.append(row)
+        torch.cuda.synchronize()
+        # activations: X ~ N(0,1) with 0.5 % x20 outlier channels, per call
+        self.x, self.xg = [], []
+        for l in range(layers):
+            xr, gr = [], []
+            for j, lin in enumerate(self.lins):
+                xa = synthetic.activations(m, lin.k, seed=synthetic.weight_seed(seed + 7, l, j))
+                xd = torch.from_numpy(xa).to(dev)
+                xr.append(xd)
+                gr.append(nv.global_scale(xd))     # static calibration, not timed
+            self.x.append(xr)
+            self.xg.append(gr)
+        self.xq = [(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
+                    torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev)) for lin in self.lins]
+        self.y = [[torch.empty((m, lin.n), dtype=torch.float32, device=dev) for lin in self.lins]
+                  for _ in range(layers)]
+        torch.cuda.synchronize()
+
+    def step(self):
+        nv = self.nv
+        for l in range(self.layers):
+            for j in range(4):
+                xq, xs = self.xq[j]
+                nv.quantize_act(self.x[l][j], self.xg[l][j], out=(xq, xs))
+                wq, ws, wg = self.w[l][j]
+                nv.gemm_smallm(xq, xs, self.xg[l][j], wq, ws, wg, out=self.y[l][j])
+
+    def gemm_only(self, j=None):
+        nv = self.nv
+        for l in range(self.layers):
+            for jj in (range(4) if j is None else (j,)):
+                xq, xs = self.xq[jj]
+                wq, ws, wg = self.w[l][jj]
+                nv.gemm_smallm(xq, xs, self.xg[l][jj], wq, ws, wg, out=self.y[l][jj])
+
+    def capture(self, fn):
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()                       # warm (module load, first-launch costs)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def bytes_per_step(self):
+        tot = {"weights": 0, "gemm": 0, "quant": 0}
+        for lin in self.lins:
+            b = algorithmic_bytes(self.m, lin.n, lin.k)
+            for key in tot:
+                tot[key] += self.layers * b[key]
+        return tot
+
+
+def time_graph(torch, g, reps: int, warm: int = 3) -> float:
+    """Average ms per replay, CUDA events on the replay stream."""
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        g.replay()
+    b.record(st)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def run_ours(args) -> dict:
+    import torch
+
+    import nvfp4_w4a4_decode_gb300 as nv
+    from nvfp4_w4a4_decode_gb300 import build as nvbuild
+
+    rank, world, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    nvbuild.build()
+    nv.library()
+    peaks = load_peaks()
+
+    stack = DecodeStack(nv, torch, m=args.m, layers=args.layers)
+    step_graph = stack.capture(stack.step)
+    launches_per_step = 2 * 4 * stack.layers
+    bytes_step = stack.bytes_per_step()
+    alg_step = bytes_step["gemm"] + bytes_step["quant"]
+
+    # ---- the timed steps: W warm-up replays, then K timed, barrier+sync around
+    for _ in range(args.warmup):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        ev0.record(st)
+        for _ in range(args.steps):
+            step_graph.replay()
+        ev1.record(st)
+        ev1.synchronize()
+        wall = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = ev0.elapsed_time(ev1) / args.steps
+    ms_step_max = reduce_max(ms_step, world)
+    value = world * alg_step / (ms_step_max * 1e-3) / 1e9
+
+    # ---- dominant kernel: the GEMM alone, same calls, same graph discipline
+    gemm_graph = stack.capture(stack.gemm_only)
+    ms_gemm = time_graph(torch, gemm_graph, reps=max(3, args.steps // 2))
+    gemm_launches = 4 * stack.layers
+    gemm_avg_us = ms_gemm * 1e3 / gemm_launches
+    gemm_bytes_per_launch = bytes_step["gemm"] / gemm_launches
+    achieved = gemm_bytes_per_launch / (gemm_avg_us * 1e-6) / 1e9
+
+    per_linear = {}
+    for j, lin in enumerate(stack.lins):
+        g = stack.capture(lambda j=j: stack.gemm_only(j))
+        ms = time_graph(torch, g, reps=max(3, args.steps // 2))
+        us = ms * 1e3 / stack.layers
+        b = algorithmic_bytes(args.m, lin.n, lin.k)["gemm"]
+        gbs = b / (us * 1e-6) / 1e9
+        per_linear[lin.name] = {"n": lin.n, "k": lin.k, "us_per_call": round(us, 3),
+                                "GBps": round(gbs, 1),
+                                "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
+        del g
+
+    # ---- end to end: pinned host X in, host Y out, through the public API
+    e2e = run_e2e(torch, stack, args)
+
+    traffic = profile_traffic("gemm_smallm")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic (seeded Gaussian weights std 0.02, Gaussian activations with "
+                "0.5% x20 outlier channels)",
+        "config": {"workload": WORKLOAD, "m": args.m, "layers": stack.layers,
+                   "weight_bytes_per_step": bytes_step["weights"],
+                   "algorithmic_bytes_per_step": alg_step,
+                   "l2": "inputs larger than L2: 3.9 GB of packed weights per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "graph": "one CUDA graph per step"},
+        "roofline": {"bound": "hbm", "kernel": "nvfp4_gemm_smallm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic,
+                     "bytes_per_launch": round(gemm_bytes_per_launch),
+                     "avg_launch_us": round(gemm_avg_us, 3)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "wall_s_timed": round(wall, 4),
+        "detail": {"per_linear_m1": per_linear,
+                   "step_frac_of_peak": round(value / world / peaks["hbm_gbs"], 4)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    return line if rank == 0 else None
+
+
+def run_e2e(torch, stack, args) -> dict:
+    """Same step, but each step copies its activations from pinned host memory
+    and reads its outputs back to pinned host memory, inside the timed region."""
+    xs_host = [[x.cpu().pin_memory() for x in row] for row in stack.x]
+    ys_host = [[torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in row] for row in stack.y]
+    h2d = sum(x.numel() * 4 for row in xs_host for x in row)
+    d2h = sum(y.numel() * 4 for row in ys_host for y in row)
+    nv = stack.nv
+
+    def one_step():
+        for l in range(stack.layers):
+            for j in range(4):
+                stack.x[l][j].copy_(xs_host[l][j], non_blocking=True)
+                xq, xs = stack.xq[j]
+                nv.quantize_act(stack.x[l][j], stack.xg[l][j], out=(xq, xs))
+                wq, ws, wg = stack.w[l][j]
+                nv.gemm_smallm(xq, xs, stack.xg[l][j], wq, ws, wg, out=stack.y[l][j])
+                ys_host[l][j].copy_(stack.y[l][j], non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    reps = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        one_step()
+    torch.cuda.synchronize()
+    sec = (time.perf_counter() - t0) / reps
+    b = stack.bytes_per_step()
+    v = (b["gemm"] + b["quant"]) / sec / 1e9
+    return {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3),
+            "path": "eager C-ABI calls per linear with pinned host<->device copies"}
+
+
+def profile_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    only if the summary was taken from the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") != kernel_source_hash():
+            return None
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_w4a4_decode_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(rows_per_linear: int, seed: int = 99):
+    """Packed operands for a bounded sample of the workload: all four linears
+    of one layer, ``rows_per_linear`` output rows each (packing not timed)."""
+    import oracle
+    items = []
+    for j, lin in enumerate(synthetic.LINEARS_8B):
+        rows = min(rows_per_linear, lin.n)
+        w = synthetic.weights(rows, lin.k, synthetic.WEIGHT_STD_8B, seed=seed + j)
+        x = synthetic.activations(1, lin.k, seed=seed + 10 + j)
+        wq, ws, gw = oracle.pack_weight(w)
+        gx = oracle.global_scale(x)
+        items.append((x, gx, wq, ws, gw, rows, lin.k))
+    return items
+
+
+def oracle_pass(items):
+    """One pass of the hot path on the CPU: quantise X, GEMM from packed bytes."""
+    import oracle
+    for x, gx, wq, ws, gw, rows, k in items:
+        xq, xs = oracle.quantize(x, gx)
+        oracle.gemm(xq, xs, gx, wq, ws, gw)
+
+
+def sample_bytes(items):
+    tot = 0
+    for x, gx, wq, ws, gw, rows, k in items:
+        tot += algorithmic_bytes(1, rows, k)["gemm"] + algorithmic_bytes(1, rows, k)["quant"]
+    return tot
+
+
+def calibrate_rows(budget_s: float) -> int:
+    probe = oracle_sample(8)
+    t0 = time.perf_counter()
+    oracle_pass(probe)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    return int(max(8, min(24576, 8 * budget_s / dt)))
+
+
+def cpu_baseline(budget_s: float = 12.0) -> dict:
+    rows = calibrate_rows(budget_s)
+    items = oracle_sample(rows)
+    t0 = time.perf_counter()
+    oracle_pass(items)
+    sec = time.perf_counter() - t0
+    v = sample_bytes(items) / sec / 1e9
+    return {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one layer's four 8B-shaped linears at M=1, {rows} output rows each "
+                      f"(quantise X + FP64 GEMM from packed bytes), {sec:.1f} s, single thread",
+            "seconds": round(sec, 2)}
+
+
+def run_reference(args) -> dict | None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    rows = calibrate_rows(budget_s=args.ref_step_seconds)
+    items = oracle_sample(rows)
+    for _ in range(args.warmup):
+        oracle_pass(items)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_pass(items)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    v = sample_bytes(items) / sec / 1e9
+    sample = (f"per step: one layer's four 8B-shaped linears at M=1, {rows} output rows each "
+              f"(quantise X + FP64 GEMM from packed bytes), single thread")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "m": 1, "sample_rows_per_linear": rows},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=synthetic.DECODE_LAYERS_8B)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,124 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) small-M NVFP4 W4A4 decode linear.
+ *
+ * The operation is the linear layer of latency-critical autoregressive decode
+ * described in "ReSET: Accurate Latency-Critical NVFP4 Reasoning via
+ * Step-Aware Temperature Scaling" (abstract; ReSET README, "Core components"
+ * item 2: small-M NVFP4 W4A4 decode kernels for M <= 8):
+ *
+ *     Y[M,N] = X[M,K] . W[N,K]^T,   1 <= M <= 8,
+ *
+ * with W stored in NVFP4 and X quantised to NVFP4 on the fly.  The pages do
+ * not define the bits of NVFP4; this library uses:
+ *   - E2M1 element codes (sign, 2 exponent bits, 1 mantissa bit; magnitudes
+ *     0, 0.5, 1, 1.5, 2, 3, 4, 6), packed two per byte, element 2j in the low
+ *     nibble of byte j;
+ *   - one E4M3 ("FN", max 448) scale byte per 16 consecutive elements of K;
+ *   - one FP32 tensor scale g = amax(|T|) / 2688 (2688 = 6 * 448).
+ * Quantisation of a 16-block with tensor scale g (FP32, each op correctly
+ * rounded): s = bmax / (6 g) (0 when 6 g == 0); sc = E4M3 round-to-nearest-
+ * even of s, saturating at 448; S = dec(sc) * g; q_i = E2M1 round-to-nearest-
+ * even of t_i / S, saturating at 6, sign kept (also for zeros); S == 0 gives
+ * signed zero codes.  Decoded: t_i ~= e2m1(q_i) * dec(sc) * g.
+ *
+ * Layouts (all row-major, no strides, all buffers owned by the caller):
+ *   X    float  [M][K]          W    float  [N][K]
+ *   x_q  uint8  [M][K/2]        w_q  uint8  [N][K/2]
+ *   x_s  uint8  [M][K/16]       w_s  uint8  [N][K/16]
+ *   x_g  float  [1]             w_g  float  [1]
+ *   Y    float  [M][N]
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is DEVICE memory of the current CUDA device.  Nothing is
+ *     allocated, freed or synchronised; work is queued on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and the call returns
+ *     once it is queued.  No state is kept between calls.
+ *   - Argument checks run on the host before anything is launched; a failed
+ *     check returns NVFP4_ERR_INVALID_ARG or NVFP4_ERR_UNSUPPORTED and
+ *     launches nothing.  A launch failure returns NVFP4_ERR_CUDA.
+ *   - K must be a multiple of 16.  X and W must be 16-byte aligned, x_q and
+ *     w_q 8-byte aligned.  Sizes of zero are legal: nothing is computed,
+ *     except that gemm with K == 0 writes zeros to Y.
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment */
+    NVFP4_ERR_UNSUPPORTED = 2, /* M outside 1..8 */
+    NVFP4_ERR_CUDA = 3         /* a CUDA launch or runtime call failed */
+} nvfp4_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvfp4_status_string(int status);
+
+/* Library version, e.g. "nvfp4-gb300 0.1.0 sm_103a". */
+const char* nvfp4_version(void);
+
+/*
+ * Tensor scale: *g = amax(|t[0..count)|) / 2688 in FP32, written on the
+ * device.  This is the NVFP4 per-tensor FP32 scale; the weight path computes
+ * it inside nvfp4_pack_weight, and callers use this entry point to calibrate
+ * the static activation scale x_g.  count == 0 writes 0.
+ *   t      device float[count], 16-byte aligned
+ *   g      device float[1], overwritten
+ * Launches a 4-byte memset and two kernels.
+ */
+int nvfp4_global_scale(const float* t, int64_t count, float* g, void* stream);
+
+/*
+ * Weight packing (offline step before decode; the pages' reset-quantize
+ * step, README "Quantize a model to NVFP4"): quantise W[N][K] with its own
+ * tensor scale.
+ *   w      device float[n][k]
+ *   w_q    device uint8[n][k/2]   out: E2M1 codes
+ *   w_s    device uint8[n][k/16]  out: E4M3 block scales
+ *   w_g    device float[1]        out: tensor scale amax/2688
+ * Launches a memset and three kernels.
+ */
+int nvfp4_pack_weight(const float* w, int64_t n, int64_t k,
+                      uint8_t* w_q, uint8_t* w_s, float* w_g, void* stream);
+
+/*
+ * Activation quantisation, on the fly before each linear (the "A4" half of
+ * W4A4): quantise X[M][K] with the static tensor scale *x_g.
+ *   x      device float[m][k]
+ *   x_g    device float[1]        in: activation tensor scale
+ *   x_q    device uint8[m][k/2]   out
+ *   x_s    device uint8[m][k/16]  out
+ * Any m >= 0 is accepted (the GEMM limits M, not this step).  One kernel.
+ */
+int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g,
+                       uint8_t* x_q, uint8_t* x_s, void* stream);
+
+/*
+ * Small-M W4A4 linear: Y[m][n] = gX * gW * sum_b dec(x_s[m][b]) dec(w_s[n][b])
+ *                                 * sum_{i in b} e2m1(x_q[m][i]) e2m1(w_q[n][i])
+ * accumulated in FP32 (results equal the exact sum up to FP32 rounding).
+ * This is the decode-time projection the ReSET README's "Core components"
+ * item 2 runs for M <= 8 instead of a tensor-core tile that would be at most
+ * 8/128 occupied.
+ *   x_q, x_s, x_g   activation codes, scales, tensor scale (as above)
+ *   w_q, w_s, w_g   weight codes, scales, tensor scale (as above)
+ *   y               device float[m][n], overwritten
+ * m must be 0..8 (NVFP4_ERR_UNSUPPORTED otherwise).  One kernel launch
+ * (a cluster launch on the fast path).  The result does not depend on the
+ * launch order of CTAs: every reduction has a fixed order.
+ */
+int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                      const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
+                      float* y, int64_t m, int64_t n, int64_t k, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,153 @@
+"""Python binding of the GB300 small-M NVFP4 W4A4 decode linear.
+
+A thin ctypes layer over the C ABI in ``include/nvfp4.h`` (library
+``libnvfp4_gb300.so``): it checks tensor devices/dtypes/shapes, allocates
+outputs with torch, passes raw device pointers and the current CUDA stream,
+and raises on a non-zero status.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback -- if the library
+is missing or fails to load, every call raises.
+
+Entry points keep the C names (``nvfp4_quantize_act`` ...) and have short
+aliases (``quantize_act`` ...).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "Nvfp4Error", "library", "nvfp4_global_scale", "nvfp4_pack_weight",
+    "nvfp4_quantize_act", "nvfp4_gemm_smallm", "global_scale", "pack_weight",
+    "quantize_act", "gemm_smallm", "linear", "MAX_M",
+]
+
+MAX_M = 8
+STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED", 3: "NVFP4_ERR_CUDA"}
+
+_lock = threading.Lock()
+_lib = None
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+SIGNATURES = {
+    "nvfp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "nvfp4_version": ([], ctypes.c_char_p),
+    "nvfp4_global_scale": ([_p, _i64, _p, _p], ctypes.c_int),
+    "nvfp4_pack_weight": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
+    "nvfp4_quantize_act": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
+    "nvfp4_gemm_smallm": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p], ctypes.c_int),
+}
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def library(path: str | None = None) -> ctypes.CDLL:
+    """Load ``libnvfp4_gb300.so`` (raises if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is not built; run nvfp4_w4a4_decode_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(name: str, status: int):
+    if status != 0:
+        raise Nvfp4Error(name, status)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def nvfp4_global_scale(t: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Tensor scale amax(|t|)/2688 as a 1-element float32 device tensor."""
+    _dev(t, torch.float32, "t")
+    g = out if out is not None else torch.empty(1, dtype=torch.float32, device=t.device)
+    _check("nvfp4_global_scale",
+           library().nvfp4_global_scale(t.data_ptr(), t.numel(), g.data_ptr(), _stream(t)))
+    return g
+
+
+def nvfp4_pack_weight(w: torch.Tensor):
+    """Quantise W[n, k] (float32) -> (w_q uint8 [n, k/2], w_s uint8 [n, k/16], w_g float32 [1])."""
+    _dev(w, torch.float32, "w")
+    n, k = w.shape
+    wq = torch.empty((n, k // 2), dtype=torch.uint8, device=w.device)
+    ws = torch.empty((n, k // 16), dtype=torch.uint8, device=w.device)
+    wg = torch.empty(1, dtype=torch.float32, device=w.device)
+    _check("nvfp4_pack_weight", library().nvfp4_pack_weight(
+        w.data_ptr(), n, k, wq.data_ptr(), ws.data_ptr(), wg.data_ptr(), _stream(w)))
+    return wq, ws, wg
+
+
+def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None):
+    """Quantise X[m, k] with tensor scale xg -> (x_q [m, k/2], x_s [m, k/16])."""
+    _dev(x, torch.float32, "x")
+    _dev(xg, torch.float32, "xg")
+    m, k = x.shape
+    if out is None:
+        xq = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
+        xs = torch.empty((m, k // 16), dtype=torch.uint8, device=x.device)
+    else:
+        xq, xs = out
+    _check("nvfp4_quantize_act", library().nvfp4_quantize_act(
+        x.data_ptr(), m, k, xg.data_ptr(), xq.data_ptr(), xs.data_ptr(), _stream(x)))
+    return xq, xs
+
+
+def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32."""
+    for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
+        _dev(t, torch.uint8, name)
+    _dev(xg, torch.float32, "xg")
+    _dev(wg, torch.float32, "wg")
+    m, kh = xq.shape
+    n = wq.shape[0]
+    k = kh * 2
+    if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
+        raise ValueError("operand shapes disagree")
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm(
+        xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
+        wg.data_ptr(), y.data_ptr(), m, n, k, _stream(xq)))
+    return y
+
+
+def linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg) -> torch.Tensor:
+    """One W4A4 decode linear: quantise X on the fly, then the small-M GEMM."""
+    xq, xs = nvfp4_quantize_act(x, xg)
+    return nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg)
+
+
+global_scale = nvfp4_global_scale
+pack_weight = nvfp4_pack_weight
+quantize_act = nvfp4_quantize_act
+gemm_smallm = nvfp4_gemm_smallm

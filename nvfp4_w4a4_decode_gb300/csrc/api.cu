@@ -1,0 +1,104 @@
+// api.cu -- the C ABI (include/nvfp4.h): argument checks, then launches on
+// the caller's stream.  No allocation, no synchronisation, no global state.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4.h"
+#include "kernels.cuh"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+int from_cuda(cudaError_t e)
+{
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(int status)
+{
+    switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+    case NVFP4_ERR_UNSUPPORTED: return "NVFP4_ERR_UNSUPPORTED";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+    default: return "NVFP4_ERR_UNKNOWN";
+    }
+}
+
+const char* nvfp4_version(void)
+{
+    return "nvfp4-gb300 0.1.0 sm_103a";
+}
+
+int nvfp4_global_scale(const float* t, int64_t count, float* g, void* stream)
+{
+    if (count < 0 || g == nullptr || (count > 0 && t == nullptr))
+        return NVFP4_ERR_INVALID_ARG;
+    if (count > 0 && !aligned(t, 16))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(nvfp4::launch_global_scale(t, count, g, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_pack_weight(const float* w, int64_t n, int64_t k, uint8_t* w_q, uint8_t* w_s,
+                      float* w_g, void* stream)
+{
+    if (n < 0 || k < 0 || (k % 16) != 0 || w_g == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    const bool empty = (n == 0 || k == 0);
+    if (!empty && (w == nullptr || w_q == nullptr || w_s == nullptr))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!empty && (!aligned(w, 16) || !aligned(w_q, 8)))
+        return NVFP4_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = nvfp4::launch_global_scale(w, empty ? 0 : n * k, w_g, s);
+    if (e != cudaSuccess || empty)
+        return from_cuda(e);
+    return from_cuda(nvfp4::launch_quantize(w, n, k, w_g, w_q, w_s, s));
+}
+
+int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g, uint8_t* x_q,
+                       uint8_t* x_s, void* stream)
+{
+    if (m < 0 || k < 0 || (k % 16) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (m == 0 || k == 0)
+        return NVFP4_OK;
+    if (x == nullptr || x_g == nullptr || x_q == nullptr || x_s == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(x_q, 8) || !aligned(x_g, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(nvfp4::launch_quantize(x, m, k, x_g, x_q, x_s, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                      const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                      int64_t m, int64_t n, int64_t k, void* stream)
+{
+    if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (m > 8)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0)
+        return NVFP4_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (y == nullptr || !aligned(y, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if (k == 0)
+        return from_cuda(cudaMemsetAsync(y, 0, sizeof(float) * (size_t)(m * n), s));
+    if (x_q == nullptr || x_s == nullptr || x_g == nullptr || w_q == nullptr || w_s == nullptr ||
+        w_g == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x_q, 8) || !aligned(w_q, 8) || !aligned(x_g, 4) || !aligned(w_g, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(nvfp4::launch_gemm_generic(x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// formats.cuh -- device-side NVFP4 element codecs for sm_103a.
+//
+// NVFP4 as used by the W4A4 decode linear ("ReSET: Accurate Latency-Critical
+// NVFP4 Reasoning via Step-Aware Temperature Scaling", README "Core
+// components" item 2): E2M1 codes (two per byte, low nibble first), one E4M3
+// scale per 16 elements along K, one FP32 tensor scale.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// E2M1 round-to-nearest-even of v, saturating at 6, sign kept (also for a
+// magnitude that rounds to 0).  Each comparison adds one step of the grid
+// 0, .5, 1, 1.5, 2, 3, 4, 6; the midpoints 0.25, 1.25, 2.5 and 5 round down
+// (to the even code below) and 0.75, 1.75, 3.5 round up (to the even code
+// above), which is where ">" and ">=" alternate.
+__device__ __forceinline__ uint32_t e2m1_rne(float v)
+{
+    const float a = fabsf(v);
+    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f)
+               + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// E4M3 (FN) round-to-nearest-even of s >= 0, saturating at 448 (code 0x7E),
+// through the hardware FP32 -> FP8 conversion with .satfinite.
+__device__ __forceinline__ uint32_t e4m3_rne_satfinite(float s)
+{
+    return (uint32_t)__nv_cvt_float_to_fp8(s, __NV_SATFINITE, __NV_E4M3);
+}
+
+// E4M3 byte -> FP32 (exact).
+__device__ __forceinline__ float e4m3_to_float(uint32_t code)
+{
+    __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// Two E2M1 codes in the low byte of `byte2` (element 2j low nibble, 2j+1 high
+// nibble) -> f16x2 {lo: element 2j, hi: element 2j+1}, exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte2)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+        : "=r"(r) : "r"(byte2));
+    return r;
+}
+
+// Byte j (0..3) of a 32-bit word.
+template <int J>
+__device__ __forceinline__ uint32_t byte_of(uint32_t w)
+{
+    return (w >> (8 * J)) & 0xFFu;
+}
+
+// Eight E2M1 codes (one 32-bit word, element 0 in the low nibble) -> four
+// f16x2 registers holding elements {0,1}, {2,3}, {4,5}, {6,7}.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&h)[4])
+{
+    h[0] = e2m1x2_to_f16x2(byte_of<0>(w));
+    h[1] = e2m1x2_to_f16x2(byte_of<1>(w));
+    h[2] = e2m1x2_to_f16x2(byte_of<2>(w));
+    h[3] = e2m1x2_to_f16x2(byte_of<3>(w));
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Sum of the two halves of an f16x2, in FP32 (exact: each half converts
+// exactly and the sum of two halves fits FP32).
+__device__ __forceinline__ float f16x2_sum(uint32_t h)
+{
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    float2 f = __half22float2(v);
+    return f.x + f.y;
+}
+
+// Read-only, no-L1-allocate 128-bit load for the weight stream (each weight
+// byte is used once).
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_u2(const void* p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+}  // namespace nvfp4

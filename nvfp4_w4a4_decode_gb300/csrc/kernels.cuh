@@ -1,0 +1,20 @@
+// kernels.cuh -- host-side launchers shared between the translation units of
+// the library (the C ABI in api.cu calls these).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStream_t stream);
+
+cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float* g,
+                            uint8_t* q, uint8_t* s, cudaStream_t stream);
+
+// Any shape with k % 16 == 0 and 8-byte aligned code rows.
+cudaError_t launch_gemm_generic(const uint8_t* xq, const uint8_t* xs, const float* xg,
+                                const uint8_t* wq, const uint8_t* ws, const float* wg,
+                                float* y, int m, int64_t n, int64_t k, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -1,0 +1,123 @@
+// quantize.cu -- NVFP4 quantisation kernels: tensor amax, tensor scale, and
+// the per-16-block E4M3 scale + E2M1 round-to-nearest-even encoder used for
+// both the offline weight packing and the on-the-fly activation quantisation
+// of the W4A4 decode linear ("ReSET: Accurate Latency-Critical NVFP4
+// Reasoning via Step-Aware Temperature Scaling", README "Core components"
+// item 2 and "Quantize a model to NVFP4").
+//
+// Every quantised byte has exactly one correct value; the FP32 steps below
+// use explicitly rounded intrinsics (__fmul_rn, __fdiv_rn) so no contraction
+// or approximate division can change a code.
+#include "formats.cuh"
+#include "kernels.cuh"
+
+namespace nvfp4 {
+
+// amax(|t|) as FP32 bits, folded into *out with an unsigned atomic max (the
+// bit pattern of a non-negative float orders like its value).  *out must
+// start at 0.
+__global__ void __launch_bounds__(256) amax_kernel(const float* __restrict__ t, int64_t count,
+                                                   uint32_t* __restrict__ out)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float a = 0.0f;
+    const int64_t nvec = count / 4;
+    const float4* t4 = reinterpret_cast<const float4*>(t);
+    for (int64_t i = tid; i < nvec; i += stride) {
+        float4 v = __ldg(t4 + i);
+        a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    for (int64_t i = nvec * 4 + tid; i < count; i += stride)
+        a = fmaxf(a, fabsf(__ldg(t + i)));
+    uint32_t bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a));
+    if ((threadIdx.x & 31) == 0 && bits != 0)
+        atomicMax(out, bits);
+}
+
+// *g = amax / 2688 in place (2688 = 6 * 448, the largest E2M1 magnitude times
+// the largest E4M3 scale).
+__global__ void finalize_scale_kernel(float* g)
+{
+    const float amax = __uint_as_float(*reinterpret_cast<uint32_t*>(g));
+    *g = __fdiv_rn(amax, 2688.0f);
+}
+
+// One thread per 16-element block: block amax, E4M3 block scale relative to
+// the tensor scale, then the 16 E2M1 codes.  Blocks are numbered row-major,
+// so consecutive threads read consecutive 64-byte blocks of t and write
+// consecutive 8-byte code groups and scale bytes.
+__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ t, int64_t nblocks,
+                                                       const float* __restrict__ g_ptr,
+                                                       uint8_t* __restrict__ q,
+                                                       uint8_t* __restrict__ s)
+{
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks)
+        return;
+    const float g = __ldg(g_ptr);
+    const float six_g = __fmul_rn(6.0f, g);
+
+    const float4* src = reinterpret_cast<const float4*>(t) + b * 4;
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float4 f = __ldg(src + i);
+        v[4 * i + 0] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    float bmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        bmax = fmaxf(bmax, fabsf(v[i]));
+
+    uint32_t sc = 0;
+    if (six_g > 0.0f)
+        sc = e4m3_rne_satfinite(__fdiv_rn(bmax, six_g));
+    const float S = __fmul_rn(e4m3_to_float(sc), g);
+
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t code = (S == 0.0f) ? ((__float_as_uint(v[i]) >> 28) & 8u)
+                                    : e2m1_rne(__fdiv_rn(v[i], S));
+        packed[i / 8] |= code << (4 * (i % 8));
+    }
+    reinterpret_cast<uint2*>(q)[b] = make_uint2(packed[0], packed[1]);
+    s[b] = (uint8_t)sc;
+}
+
+cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStream_t stream)
+{
+    cudaError_t err = cudaMemsetAsync(g, 0, sizeof(float), stream);
+    if (err != cudaSuccess)
+        return err;
+    if (count > 0) {
+        int64_t blocks = (count / 4 + 255) / 256;
+        if (blocks < 1)
+            blocks = 1;
+        if (blocks > 4 * 152 * 8)
+            blocks = 4 * 152 * 8;
+        amax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(t, count, reinterpret_cast<uint32_t*>(g));
+        err = cudaGetLastError();
+        if (err != cudaSuccess)
+            return err;
+    }
+    finalize_scale_kernel<<<1, 1, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float* g,
+                            uint8_t* q, uint8_t* s, cudaStream_t stream)
+{
+    const int64_t nblocks = rows * (k / 16);
+    if (nblocks == 0)
+        return cudaSuccess;
+    const int64_t grid = (nblocks + 255) / 256;
+    quantize_kernel<<<(unsigned)grid, 256, 0, stream>>>(t, nblocks, g, q, s);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,89 @@
+"""The C ABI library loads and exports every entry point include/*.h
+declares; argument checks answer on the host before any launch.  CPU only:
+the calls below never reach a kernel (they fail validation or are empty)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import nvfp4_w4a4_decode_gb300 as nv
+from nvfp4_w4a4_decode_gb300 import build as nvbuild
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(nvfp4_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nvbuild.build()
+    return nv.library()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("nvfp4_pack_weight", "nvfp4_quantize_act", "nvfp4_gemm_smallm",
+                 "nvfp4_global_scale", "nvfp4_status_string", "nvfp4_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(nv.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in nv.STATUS.items():
+        assert lib.nvfp4_status_string(code).decode() == name
+    assert lib.nvfp4_status_string(99).decode() == "NVFP4_ERR_UNKNOWN"
+    assert b"sm_103a" in lib.nvfp4_version()
+
+
+FAKE = 1 << 20  # a non-null, 256-byte aligned value never dereferenced
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    g = lib.nvfp4_gemm_smallm
+    ok_args = [FAKE] * 7
+    assert g(*ok_args, 9, 16, 32, None) == 2        # M > 8: unsupported
+    assert g(*ok_args, 1, 16, 24, None) == 1        # K not a multiple of 16
+    assert g(*ok_args, -1, 16, 32, None) == 1
+    assert g(*ok_args, 1, -16, 32, None) == 1
+    bad = list(ok_args)
+    bad[3] = None                                   # null weight codes
+    assert g(*bad, 1, 16, 32, None) == 1
+    bad = list(ok_args)
+    bad[0] = FAKE + 4                               # misaligned activation codes
+    assert g(*bad, 1, 16, 32, None) == 1
+    assert g(*ok_args, 0, 16, 32, None) == 0        # empty batch: nothing to do
+    assert g(*ok_args, 2, 0, 32, None) == 0         # empty output
+
+
+def test_quantize_and_pack_reject_bad_arguments(lib):
+    q = lib.nvfp4_quantize_act
+    assert q(FAKE, 1, 20, FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE + 8, 1, 32, FAKE, FAKE, FAKE, None) == 1    # X not 16-byte aligned
+    assert q(None, 1, 32, FAKE, FAKE, FAKE, None) == 1
+    assert q(FAKE, 0, 32, FAKE, FAKE, FAKE, None) == 0        # empty
+    p = lib.nvfp4_pack_weight
+    assert p(FAKE, 4, 40, FAKE, FAKE, FAKE, None) == 1
+    assert p(FAKE, 4, 32, FAKE, FAKE, None, None) == 1
+    s = lib.nvfp4_global_scale
+    assert s(FAKE, -1, FAKE, None) == 1
+    assert s(FAKE, 4, None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(nv, "_lib", None)
+    with pytest.raises(ImportError):
+        nv.library(str(tmp_path / "missing.so"))

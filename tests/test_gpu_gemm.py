@@ -1,0 +1,178 @@
+"""GPU parity of the small-M W4A4 GEMM against the oracle's FP64 result.
+
+Operands are quantised by each side independently (the quantisers are
+bit-exact, tested separately), then Y from the C ABI is compared with the
+oracle's FP64 Y computed from the oracle's own bytes.  Tolerance: GEMM_TOL on
+max |y - ref| / max(|ref|, row rms).  Marked gpu."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from helpers import GEMM_TOL, gemm_error, sampled_error
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_w4a4_decode_gb300 as nvmod
+    from nvfp4_w4a4_decode_gb300 import build as nvbuild
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    nvbuild.build()
+    oracle.build()
+    nvmod.library()
+    return nvmod
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def run_both(nv, x, w):
+    """(y_gpu, y_oracle, oracle operands) for one linear."""
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg)
+    return host(y), ref
+
+
+SMALL = [(1, 256, 512), (1, 1, 16), (2, 3, 32), (3, 17, 48), (5, 33, 272), (8, 64, 256),
+         (4, 100, 4112), (7, 129, 1024), (8, 1000, 4096), (6, 31, 12288 + 16)]
+
+
+@pytest.mark.parametrize("m,n,k", SMALL)
+def test_gemm_small_shapes(nv, m, n, k):
+    x = synthetic.activations(m, k, seed=m * 1000 + k)
+    w = synthetic.weights(n, k, 0.02, seed=n * 1000 + k)
+    y, ref = run_both(nv, x, w)
+    assert gemm_error(y, ref) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("m", range(1, 9))
+def test_gemm_every_m_tiles_and_tail(nv, m):
+    """Several row tiles plus a ragged row tail, K spanning several tiles."""
+    n, k = 16 * 37 + 5, 4096 + 256
+    x = synthetic.activations(m, k, seed=m)
+    w = synthetic.weights(n, k, 0.02, seed=77)
+    y, ref = run_both(nv, x, w)
+    assert gemm_error(y, ref) <= GEMM_TOL
+
+
+def test_gemm_decades_of_scales(nv):
+    """Block scales over many decades (subnormal to saturated E4M3)."""
+    m, n, k = 4, 96, 2048
+    x = synthetic.log_uniform_blocks(m, k, seed=3)
+    w = synthetic.log_uniform_blocks(n, k, seed=4)
+    y, ref = run_both(nv, x, w)
+    assert gemm_error(y, ref) <= GEMM_TOL
+
+
+def test_gemm_zero_operands(nv):
+    m, n, k = 3, 40, 512
+    x = np.zeros((m, k), np.float32)
+    w = synthetic.weights(n, k, 0.02, seed=5)
+    y, ref = run_both(nv, x, w)
+    assert not ref.any() and not y.any()
+    x = synthetic.activations(m, k, seed=6)
+    w[:] = 0
+    y, ref = run_both(nv, x, w)
+    assert not y.any()
+
+
+def test_gemm_k_zero_writes_zeros(nv):
+    y = torch.full((2, 5), 7.0, device="cuda")
+    e8 = torch.empty((2, 0), dtype=torch.uint8, device="cuda")
+    w8 = torch.empty((5, 0), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, device="cuda")
+    nv.gemm_smallm(e8, e8, g, w8, w8, g, out=y)
+    assert not host(y).any()
+
+
+def test_gemm_empty_m_leaves_output(nv):
+    y = torch.full((0, 5), 7.0, device="cuda")
+    xq = torch.empty((0, 16), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((0, 2), dtype=torch.uint8, device="cuda")
+    wq = torch.zeros((5, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros((5, 2), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, device="cuda")
+    nv.gemm_smallm(xq, xs, g, wq, ws, g, out=y)
+
+
+def test_gemm_m9_unsupported(nv):
+    xq = torch.zeros((9, 16), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((9, 2), dtype=torch.uint8, device="cuda")
+    wq = torch.zeros((4, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros((4, 2), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, device="cuda")
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.gemm_smallm(xq, xs, g, wq, ws, g)
+    assert e.value.status == 2
+
+
+def test_gemm_deterministic_and_no_overrun(nv):
+    m, n, k = 8, 24576 // 8, 4096
+    x = synthetic.activations(m, k, seed=8)
+    w = synthetic.weights(n, k, 0.02, seed=9)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    canary = torch.full((m * n + 1024,), 123.0, device="cuda")
+    y1 = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=canary[: m * n].view(m, n))
+    a = host(y1).copy()
+    y2 = nv.gemm_smallm(xq, xs, xg, wq, ws, wg)
+    np.testing.assert_array_equal(a, host(y2))
+    assert np.all(host(canary[m * n:]) == 123.0)
+
+
+def full_size_case(nv, m, n, k, std, seed, samples=64):
+    """Full-size linear: whole GPU path; the oracle evaluates ``samples``
+    output rows n (all m) from its own quantisation of those rows."""
+    w = synthetic.weights(n, k, std, seed=seed)
+    x = synthetic.activations(m, k, seed=seed + 1)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    y = host(nv.gemm_smallm(xq, xs, xg, wq, ws, wg))
+    del wq, ws
+    gx = oracle.global_scale(x)
+    gw = oracle.global_scale(w)
+    oxq, oxs = oracle.quantize(x, gx)
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, samples - 2)]))
+    owq, ows = oracle.quantize(w[rows], gw)
+    ref = oracle.gemm(oxq, oxs, gx, owq, ows, gw)        # [m, len(rows)]
+    # the row rms of the full output is estimated from the GPU-independent
+    # sampled reference
+    row_rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+    err = sampled_error(y[:, rows], ref, row_rms)
+    torch.cuda.empty_cache()
+    return err
+
+
+@pytest.mark.parametrize("m", synthetic.M_SWEEP_8B)
+@pytest.mark.parametrize("lin", synthetic.LINEARS_8B, ids=lambda l: l.name)
+def test_gemm_full_size_8b(nv, lin, m):
+    err = full_size_case(nv, m, lin.n, lin.k, synthetic.WEIGHT_STD_8B, seed=lin.n + lin.k)
+    assert err <= GEMM_TOL
+
+
+@pytest.mark.parametrize("m", synthetic.M_SWEEP_32B)
+@pytest.mark.parametrize("lin", synthetic.LINEARS_32B, ids=lambda l: l.name)
+def test_gemm_full_size_32b(nv, lin, m):
+    err = full_size_case(nv, m, lin.n, lin.k, synthetic.WEIGHT_STD_32B, seed=lin.n + 3 * lin.k)
+    assert err <= GEMM_TOL

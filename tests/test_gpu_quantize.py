@@ -1,0 +1,152 @@
+"""GPU parity of the quantisation kernels: tensor scale, activation
+quantisation and weight packing are bit-exact with the oracle (every byte has
+one correct value).  Marked gpu; the CUDA side runs through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_w4a4_decode_gb300 as nvmod
+    from nvfp4_w4a4_decode_gb300 import build as nvbuild
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    nvbuild.build()
+    oracle.build()
+    nvmod.library()
+    return nvmod
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("count", [0, 1, 3, 4, 17, 4096, 1 << 20, (1 << 20) + 5])
+def test_global_scale_bit_exact(nv, count):
+    t = synthetic.activations(1, max(count, 1), seed=count)[0, :count].copy()
+    g = host(nv.global_scale(dev(t)))[0]
+    assert np.float32(g) == oracle.global_scale(t)
+
+
+@pytest.mark.parametrize("m", [1, 3, 8])
+@pytest.mark.parametrize("k", [16, 48, 512, 4096, 12288, 25600])
+@pytest.mark.parametrize("dist", ["outliers", "decades"])
+def test_quantize_act_bit_exact(nv, m, k, dist):
+    if dist == "outliers":
+        x = synthetic.activations(m, k, seed=100 + k + m)
+    else:
+        x = synthetic.log_uniform_blocks(m, k, seed=200 + k + m)
+    gx = oracle.global_scale(x)
+    oq, os_ = oracle.quantize(x, gx)
+    xq, xs = nv.quantize_act(dev(x), dev(np.array([gx], np.float32)))
+    np.testing.assert_array_equal(host(xq), oq)
+    np.testing.assert_array_equal(host(xs), os_)
+
+
+def test_quantize_static_scale_saturates(nv):
+    """A static activation scale that is too small saturates block scales at
+    448 and codes at 6, identically on both sides."""
+    x = synthetic.activations(2, 256, seed=7)
+    gx = np.float32(oracle.global_scale(x) / 50)
+    oq, os_ = oracle.quantize(x, gx)
+    assert (os_ == 0x7E).any()
+    xq, xs = nv.quantize_act(dev(x), dev(np.array([gx], np.float32)))
+    np.testing.assert_array_equal(host(xq), oq)
+    np.testing.assert_array_equal(host(xs), os_)
+
+
+def test_quantize_every_e4m3_tie_and_e2m1_tie(nv):
+    """Block maxima at every E4M3 midpoint (and one FP32 ulp either side), and
+    elements at every E2M1 midpoint with S == 1, against the oracle."""
+    g = np.float32(0.25)                      # 6 g = 1.5
+    codes = np.arange(0, 0x7E)
+    vals = np.array([oracle.e4m3_value(c) for c in range(0, 0x7F)])
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    targets = np.concatenate([mids, np.nextafter(mids, np.float32(0)),
+                              np.nextafter(mids, np.float32(1e9)), vals.astype(np.float32)])
+    bmax = (targets.astype(np.float64) * 1.5).astype(np.float32)
+    # bmax / 1.5 must reproduce the target in FP32 for the tie to be exact;
+    # keep the rows where it does (most of them) and test all rows anyway.
+    rows = bmax.size
+    x = np.zeros((rows, 16), np.float32)
+    x[:, 0] = bmax
+    x[:, 1] = -bmax / 3
+    x[:, 2:] = np.linspace(-1, 1, 14, dtype=np.float32) * bmax[:, None] / 7
+    oq, os_ = oracle.quantize(x, g)
+    xq, xs = nv.quantize_act(dev(x), dev(np.array([g], np.float32)))
+    np.testing.assert_array_equal(host(xs), os_)
+    np.testing.assert_array_equal(host(xq), oq)
+    assert len(set(os_.ravel())) > 100 and codes.size == 0x7E
+    # E2M1 ties: bmax 6 and g 0.25 give s = 4 exactly and S = 1.
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    x = np.zeros((2, 16), np.float32)
+    x[0, 0] = 6.0
+    x[0, 1:8] = ties
+    x[0, 8:15] = -ties
+    x[1, 0] = -6.0
+    x[1, 1:8] = np.nextafter(ties, np.float32(0))
+    x[1, 8:15] = np.nextafter(ties, np.float32(9))
+    oq, os_ = oracle.quantize(x, g)
+    xq, xs = nv.quantize_act(dev(x), dev(np.array([g], np.float32)))
+    np.testing.assert_array_equal(host(xs), os_)
+    np.testing.assert_array_equal(host(xq), oq)
+
+
+def test_quantize_zeros_and_signed_zeros(nv):
+    x = np.zeros((3, 64), np.float32)
+    x[1, 5] = -0.0
+    x[2, :16] = 1.0
+    x[2, 16:32] = -0.0
+    x[2, 33] = -1e-30          # rounds to a zero code, keeps its sign
+    for gx in (np.float32(0.0), oracle.global_scale(x)):
+        oq, os_ = oracle.quantize(x, gx)
+        xq, xs = nv.quantize_act(dev(x), dev(np.array([gx], np.float32)))
+        np.testing.assert_array_equal(host(xq), oq)
+        np.testing.assert_array_equal(host(xs), os_)
+
+
+@pytest.mark.parametrize("n,k", [(1, 16), (256, 512), (1000, 48), (300, 4096)])
+def test_pack_weight_bit_exact(nv, n, k):
+    w = synthetic.weights(n, k, 0.02, seed=n + k)
+    oq, os_, og = oracle.pack_weight(w)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    assert np.float32(host(wg)[0]) == og
+    np.testing.assert_array_equal(host(wq), oq)
+    np.testing.assert_array_equal(host(ws), os_)
+
+
+@pytest.mark.parametrize("shape", [(l.n, l.k, "8B") for l in synthetic.LINEARS_8B]
+                         + [(l.n, l.k, "32B") for l in synthetic.LINEARS_32B])
+def test_pack_weight_full_size_sampled_rows(nv, shape):
+    """Full-size layers: the tensor scale over the whole tensor, and the codes
+    and scales of 48 sampled rows (first, last, random)."""
+    n, k, fam = shape
+    std = synthetic.WEIGHT_STD_8B if fam == "8B" else synthetic.WEIGHT_STD_32B
+    w = synthetic.weights(n, k, std, seed=n * 7 + k)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    og = oracle.global_scale(w)
+    assert np.float32(host(wg)[0]) == og
+    rng = np.random.default_rng(n + k)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 46)]))
+    oq, os_ = oracle.quantize(w[rows], og)
+    idx = torch.from_numpy(rows).cuda()
+    np.testing.assert_array_equal(host(wq.index_select(0, idx)), oq)
+    np.testing.assert_array_equal(host(ws.index_select(0, idx)), os_)
+    del wq, ws
+    torch.cuda.empty_cache()
+
+
+def test_pack_weight_empty(nv):
+    w = torch.empty((0, 32), dtype=torch.float32, device="cuda")
+    wq, ws, wg = nv.pack_weight(w)
+    assert wq.shape == (0, 16) and host(wg)[0] == 0.0
