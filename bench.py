@@ -167,9 +167,10 @@ class DecodeStack:
     """36 layers x 4 linears of packed weights resident in HBM, per-call
     activation buffers, and the graphs that replay them."""
 
-    def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234):
+    def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True):
         self.nv, self.torch = nv, torch
         self.m = m
+        self.pdl = pdl
         self.layers = layers
         self.lins = synthetic.LINEARS_8B
         dev = torch.device("cuda")
@@ -207,9 +208,9 @@ class DecodeStack:
         for l in range(self.layers):
             for j in range(4):
                 xq, xs = self.xq[j]
-                nv.quantize_act(self.x[l][j], self.xg[l][j], out=(xq, xs))
+                nv.quantize_act(self.x[l][j], self.xg[l][j], out=(xq, xs), pdl=self.pdl)
                 wq, ws, wg = self.w[l][j]
-                nv.gemm_smallm(xq, xs, self.xg[l][j], wq, ws, wg, out=self.y[l][j])
+                nv.gemm_smallm(xq, xs, self.xg[l][j], wq, ws, wg, out=self.y[l][j], pdl=self.pdl)
 
     def gemm_only(self, j=None):
         nv = self.nv
@@ -217,7 +218,8 @@ class DecodeStack:
             for jj in (range(4) if j is None else (j,)):
                 xq, xs = self.xq[jj]
                 wq, ws, wg = self.w[l][jj]
-                nv.gemm_smallm(xq, xs, self.xg[l][jj], wq, ws, wg, out=self.y[l][jj])
+                nv.gemm_smallm(xq, xs, self.xg[l][jj], wq, ws, wg, out=self.y[l][jj],
+                               pdl=self.pdl)
 
     def capture(self, fn):
         torch = self.torch
@@ -272,8 +274,14 @@ def run_ours(args) -> dict:
     nv.library()
     peaks = load_peaks()
 
-    stack = DecodeStack(nv, torch, m=args.m, layers=args.layers)
+    stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl)
     step_graph = stack.capture(stack.step)
+    if args.profile_step:
+        # only the step graph, replayed: a clean launch list for the profiler
+        for _ in range(args.warmup + args.steps):
+            step_graph.replay()
+        torch.cuda.synchronize()
+        return None
     launches_per_step = 2 * 4 * stack.layers
     bytes_step = stack.bytes_per_step()
     alg_step = bytes_step["gemm"] + bytes_step["quant"]
@@ -317,6 +325,7 @@ def run_ours(args) -> dict:
         b = algorithmic_bytes(args.m, lin.n, lin.k)["gemm"]
         gbs = b / (us * 1e-6) / 1e9
         per_linear[lin.name] = {"n": lin.n, "k": lin.k, "us_per_call": round(us, 3),
+                                "kernel": nv.KERNEL_NAMES.get(nv.gemm_select(args.m, lin.n, lin.k)),
                                 "GBps": round(gbs, 1),
                                 "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
         del g
@@ -336,7 +345,8 @@ def run_ours(args) -> dict:
                    "algorithmic_bytes_per_step": alg_step,
                    "l2": "inputs larger than L2: 3.9 GB of packed weights per step",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "graph": "one CUDA graph per step"},
+                   "graph": "one CUDA graph per step",
+                   "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "kernel": "nvfp4_gemm_smallm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
@@ -515,6 +525,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="replay only the step graph (warmup + steps times) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -117,6 +117,50 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
                       const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
                       float* y, int64_t m, int64_t n, int64_t k, void* stream);
 
+/*
+ * Options of the _ex entry points: a kernel choice in the low byte, OR-ed
+ * with flags.
+ *
+ * NVFP4_KERNEL_AUTO     the library's choice for the shape (what the plain
+ *                       entry points use).
+ * NVFP4_KERNEL_GENERIC  the shape-general CUDA-core kernel (any K % 16 == 0).
+ * NVFP4_KERNEL_GEMV     the persistent CUDA-core weight-streaming kernel:
+ *                       M <= 2, K a multiple of 1024 (of 2048 above 16384)
+ *                       and at most 32768, x_q/w_q 16-byte and x_s/w_s
+ *                       4-byte aligned; NVFP4_ERR_UNSUPPORTED otherwise.
+ * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
+ *                       while the previous kernel on the stream is still
+ *                       running and waits for it before it touches anything
+ *                       that kernel could have written -- EXCEPT that the GEMM
+ *                       streams w_q/w_s before waiting.  Set it only when the
+ *                       work queued just before the call does not write the
+ *                       weights (true in decode, where weights are constant).
+ */
+#define NVFP4_KERNEL_AUTO 0u
+#define NVFP4_KERNEL_GENERIC 1u
+#define NVFP4_KERNEL_GEMV 2u
+#define NVFP4_KERNEL_MASK 0xFFu
+#define NVFP4_FLAG_PDL 0x100u
+
+/* nvfp4_quantize_act with options (only NVFP4_FLAG_PDL is meaningful). */
+int nvfp4_quantize_act_ex(const float* x, int64_t m, int64_t k, const float* x_g,
+                          uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream);
+
+/* nvfp4_gemm_smallm with a kernel choice and flags (see above).  Same
+ * arguments, same result up to FP32 rounding order. */
+int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
+                         float* y, int64_t m, int64_t n, int64_t k,
+                         uint32_t options, void* stream);
+
+/*
+ * Which kernel a GEMM of shape (m, n, k) with suitably aligned operands runs
+ * under `options` (one of NVFP4_KERNEL_*), or minus a status code when the
+ * shape is invalid or the requested kernel cannot take it.  Host only; the
+ * counterpart of the README's "nvfp4r.status()" inspection.
+ */
+int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,7 +42,15 @@ SIGNATURES = {
     "nvfp4_pack_weight": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
     "nvfp4_quantize_act": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
     "nvfp4_gemm_smallm": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p], ctypes.c_int),
+    "nvfp4_quantize_act_ex": ([_p, _i64, _i64, _p, _p, _p, ctypes.c_uint32, _p], ctypes.c_int),
+    "nvfp4_gemm_smallm_ex": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_uint32, _p],
+                             ctypes.c_int),
+    "nvfp4_gemm_select": ([_i64, _i64, _i64, ctypes.c_uint32], ctypes.c_int),
 }
+
+KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV = 0, 1, 2
+KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv"}
+FLAG_PDL = 0x100
 
 
 class Nvfp4Error(RuntimeError):
@@ -108,7 +116,7 @@ def nvfp4_pack_weight(w: torch.Tensor):
     return wq, ws, wg
 
 
-def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None):
+def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None, pdl: bool = False):
     """Quantise X[m, k] with tensor scale xg -> (x_q [m, k/2], x_s [m, k/16])."""
     _dev(x, torch.float32, "x")
     _dev(xg, torch.float32, "xg")
@@ -118,13 +126,19 @@ def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None):
         xs = torch.empty((m, k // 16), dtype=torch.uint8, device=x.device)
     else:
         xq, xs = out
-    _check("nvfp4_quantize_act", library().nvfp4_quantize_act(
-        x.data_ptr(), m, k, xg.data_ptr(), xq.data_ptr(), xs.data_ptr(), _stream(x)))
+    _check("nvfp4_quantize_act", library().nvfp4_quantize_act_ex(
+        x.data_ptr(), m, k, xg.data_ptr(), xq.data_ptr(), xs.data_ptr(),
+        FLAG_PDL if pdl else 0, _stream(x)))
     return xq, xs
 
 
-def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None) -> torch.Tensor:
-    """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32."""
+def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
+                      kernel: int = KERNEL_AUTO, pdl: bool = False) -> torch.Tensor:
+    """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32.
+
+    ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV); ``pdl`` lets
+    the launch overlap the previous kernel (weights must not be written by
+    it)."""
     for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
         _dev(t, torch.uint8, name)
     _dev(xg, torch.float32, "xg")
@@ -135,10 +149,16 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None) -
     if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
         raise ValueError("operand shapes disagree")
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
-    _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm(
+    opts = int(kernel) | (FLAG_PDL if pdl else 0)
+    _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm_ex(
         xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
-        wg.data_ptr(), y.data_ptr(), m, n, k, _stream(xq)))
+        wg.data_ptr(), y.data_ptr(), m, n, k, opts, _stream(xq)))
     return y
+
+
+def nvfp4_gemm_select(m: int, n: int, k: int, kernel: int = KERNEL_AUTO) -> int:
+    """Kernel id the library runs for this shape (negative status if none)."""
+    return library().nvfp4_gemm_select(m, n, k, kernel)
 
 
 def linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg) -> torch.Tensor:
@@ -151,3 +171,4 @@ global_scale = nvfp4_global_scale
 pack_weight = nvfp4_pack_weight
 quantize_act = nvfp4_quantize_act
 gemm_smallm = nvfp4_gemm_smallm
+gemm_select = nvfp4_gemm_select

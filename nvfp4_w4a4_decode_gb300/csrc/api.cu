@@ -64,10 +64,10 @@ int nvfp4_pack_weight(const float* w, int64_t n, int64_t k, uint8_t* w_q, uint8_
     return from_cuda(nvfp4::launch_quantize(w, n, k, w_g, w_q, w_s, s));
 }
 
-int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g, uint8_t* x_q,
-                       uint8_t* x_s, void* stream)
+int nvfp4_quantize_act_ex(const float* x, int64_t m, int64_t k, const float* x_g, uint8_t* x_q,
+                          uint8_t* x_s, uint32_t options, void* stream)
 {
-    if (m < 0 || k < 0 || (k % 16) != 0)
+    if (m < 0 || k < 0 || (k % 16) != 0 || (options & ~(uint32_t)NVFP4_FLAG_PDL) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if (m == 0 || k == 0)
         return NVFP4_OK;
@@ -75,14 +75,50 @@ int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g, u
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(x_q, 8) || !aligned(x_g, 4))
         return NVFP4_ERR_INVALID_ARG;
-    return from_cuda(nvfp4::launch_quantize(x, m, k, x_g, x_q, x_s, static_cast<cudaStream_t>(stream)));
+    return from_cuda(nvfp4::launch_quantize(x, m, k, x_g, x_q, x_s, static_cast<cudaStream_t>(stream),
+                                            (options & NVFP4_FLAG_PDL) != 0));
 }
 
-int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
-                      const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
-                      int64_t m, int64_t n, int64_t k, void* stream)
+int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g, uint8_t* x_q,
+                       uint8_t* x_s, void* stream)
+{
+    return nvfp4_quantize_act_ex(x, m, k, x_g, x_q, x_s, 0u, stream);
+}
+
+namespace {
+
+// Kernel for a GEMM of this shape and operand alignment (negative status on
+// a request that cannot be met).
+int select_kernel(int64_t m, int64_t k, uint32_t options, bool ptrs_ok_fast)
+{
+    const uint32_t req = options & NVFP4_KERNEL_MASK;
+    const bool gemv_ok = nvfp4::gemv_supported(m, k) && ptrs_ok_fast;
+    switch (req) {
+    case NVFP4_KERNEL_AUTO: return gemv_ok ? (int)NVFP4_KERNEL_GEMV : (int)NVFP4_KERNEL_GENERIC;
+    case NVFP4_KERNEL_GENERIC: return (int)NVFP4_KERNEL_GENERIC;
+    case NVFP4_KERNEL_GEMV: return gemv_ok ? (int)NVFP4_KERNEL_GEMV : -(int)NVFP4_ERR_UNSUPPORTED;
+    default: return -(int)NVFP4_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options)
+{
+    if (m < 1 || n < 1 || k < 16 || (k % 16) != 0)
+        return -NVFP4_ERR_INVALID_ARG;
+    if (m > 8)
+        return -NVFP4_ERR_UNSUPPORTED;
+    return select_kernel(m, k, options, true);
+}
+
+int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                         int64_t m, int64_t n, int64_t k, uint32_t options, void* stream)
 {
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL)) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if (m > 8)
         return NVFP4_ERR_UNSUPPORTED;
@@ -98,7 +134,26 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x_q, 8) || !aligned(w_q, 8) || !aligned(x_g, 4) || !aligned(w_g, 4))
         return NVFP4_ERR_INVALID_ARG;
-    return from_cuda(nvfp4::launch_gemm_generic(x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k, s));
+    const bool fast_ptrs = aligned(x_q, 16) && aligned(w_q, 16) && aligned(x_s, 4) &&
+                           aligned(w_s, 4);
+    const int kern = select_kernel(m, k, options, fast_ptrs);
+    if (kern < 0)
+        return -kern;
+    const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
+    const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k, s};
+    switch (kern) {
+    case NVFP4_KERNEL_GEMV:
+        return from_cuda(nvfp4::launch_gemm_gemv(a, pdl));
+    default:
+        return from_cuda(nvfp4::launch_gemm_generic(a));
+    }
+}
+
+int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                      const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                      int64_t m, int64_t n, int64_t k, void* stream)
+{
+    return nvfp4_gemm_smallm_ex(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, 0u, stream);
 }
 
 }  // extern "C"

@@ -72,28 +72,25 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(
 }
 
 template <int M>
-static cudaError_t launch_generic_m(const uint8_t* xq, const uint8_t* xs, const float* xg,
-                                    const uint8_t* wq, const uint8_t* ws, const float* wg,
-                                    float* y, int64_t n, int64_t k, cudaStream_t stream)
+static cudaError_t launch_generic_m(const GemmArgs& a)
 {
-    const int64_t grid = (n + 7) / 8;
-    gemm_generic_kernel<M><<<(unsigned)grid, 256, 0, stream>>>(xq, xs, xg, wq, ws, wg, y, n, k);
+    const int64_t grid = (a.n + 7) / 8;
+    gemm_generic_kernel<M><<<(unsigned)grid, 256, 0, a.stream>>>(a.xq, a.xs, a.xg, a.wq, a.ws,
+                                                                 a.wg, a.y, a.n, a.k);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_generic(const uint8_t* xq, const uint8_t* xs, const float* xg,
-                                const uint8_t* wq, const uint8_t* ws, const float* wg,
-                                float* y, int m, int64_t n, int64_t k, cudaStream_t stream)
+cudaError_t launch_gemm_generic(const GemmArgs& a)
 {
-    switch (m) {
-    case 1: return launch_generic_m<1>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 2: return launch_generic_m<2>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 3: return launch_generic_m<3>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 4: return launch_generic_m<4>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 5: return launch_generic_m<5>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 6: return launch_generic_m<6>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 7: return launch_generic_m<7>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
-    case 8: return launch_generic_m<8>(xq, xs, xg, wq, ws, wg, y, n, k, stream);
+    switch (a.m) {
+    case 1: return launch_generic_m<1>(a);
+    case 2: return launch_generic_m<2>(a);
+    case 3: return launch_generic_m<3>(a);
+    case 4: return launch_generic_m<4>(a);
+    case 5: return launch_generic_m<5>(a);
+    case 6: return launch_generic_m<6>(a);
+    case 7: return launch_generic_m<7>(a);
+    case 8: return launch_generic_m<8>(a);
     default: return cudaErrorInvalidValue;
     }
 }

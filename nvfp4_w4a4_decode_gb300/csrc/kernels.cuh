@@ -7,14 +7,31 @@
 
 namespace nvfp4 {
 
+struct GemmArgs {
+    const uint8_t* xq;
+    const uint8_t* xs;
+    const float* xg;
+    const uint8_t* wq;
+    const uint8_t* ws;
+    const float* wg;
+    float* y;
+    int m;
+    int64_t n;
+    int64_t k;
+    cudaStream_t stream;
+};
+
 cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStream_t stream);
 
 cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float* g,
-                            uint8_t* q, uint8_t* s, cudaStream_t stream);
+                            uint8_t* q, uint8_t* s, cudaStream_t stream, bool pdl = false);
 
 // Any shape with k % 16 == 0 and 8-byte aligned code rows.
-cudaError_t launch_gemm_generic(const uint8_t* xq, const uint8_t* xs, const float* xg,
-                                const uint8_t* wq, const uint8_t* ws, const float* wg,
-                                float* y, int m, int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_gemm_generic(const GemmArgs& a);
+
+// Persistent CUDA-core weight-streaming kernel: m in {1, 2}, k a multiple of
+// 1024 up to 32768; x_q/w_q 16-byte and x_s/w_s 4-byte aligned.
+bool gemv_supported(int64_t m, int64_t k);
+cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl);
 
 }  // namespace nvfp4

@@ -43,50 +43,57 @@ __global__ void finalize_scale_kernel(float* g)
     *g = __fdiv_rn(amax, 2688.0f);
 }
 
-// One thread per 16-element block: block amax, E4M3 block scale relative to
-// the tensor scale, then the 16 E2M1 codes.  Blocks are numbered row-major,
-// so consecutive threads read consecutive 64-byte blocks of t and write
-// consecutive 8-byte code groups and scale bytes.
+// Four threads per 16-element block (each holds 4 consecutive elements):
+// block amax by a quad shuffle, the E4M3 block scale relative to the tensor
+// scale, then each thread's 4 E2M1 codes; the quad gathers its 16 codes into
+// two 32-bit words.  Blocks are numbered row-major, so a warp reads 512
+// contiguous bytes of t and writes 64 contiguous code bytes.  With
+// programmatic dependent launch the kernel lets the next kernel (the GEMM)
+// launch at once, then waits for the producer of t.
+template <bool PDL>
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ t, int64_t nblocks,
                                                        const float* __restrict__ g_ptr,
                                                        uint8_t* __restrict__ q,
                                                        uint8_t* __restrict__ s)
 {
-    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= nblocks)
-        return;
+    if constexpr (PDL) {
+        asm volatile("griddepcontrol.launch_dependents;");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t b = tid >> 2;
+    const int sub = (int)(tid & 3);
+    const bool valid = b < nblocks;
+
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid)
+        v = __ldg(reinterpret_cast<const float4*>(t) + tid);
+    float bmax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 2));
+
     const float g = __ldg(g_ptr);
     const float six_g = __fmul_rn(6.0f, g);
-
-    const float4* src = reinterpret_cast<const float4*>(t) + b * 4;
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float4 f = __ldg(src + i);
-        v[4 * i + 0] = f.x;
-        v[4 * i + 1] = f.y;
-        v[4 * i + 2] = f.z;
-        v[4 * i + 3] = f.w;
-    }
-    float bmax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        bmax = fmaxf(bmax, fabsf(v[i]));
-
     uint32_t sc = 0;
     if (six_g > 0.0f)
         sc = e4m3_rne_satfinite(__fdiv_rn(bmax, six_g));
     const float S = __fmul_rn(e4m3_to_float(sc), g);
 
-    uint32_t packed[2] = {0u, 0u};
+    const float e[4] = {v.x, v.y, v.z, v.w};
+    uint32_t codes = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        uint32_t code = (S == 0.0f) ? ((__float_as_uint(v[i]) >> 28) & 8u)
-                                    : e2m1_rne(__fdiv_rn(v[i], S));
-        packed[i / 8] |= code << (4 * (i % 8));
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c = (S == 0.0f) ? ((__float_as_uint(e[i]) >> 28) & 8u)
+                                       : e2m1_rne(__fdiv_rn(e[i], S));
+        codes |= c << (4 * i);
     }
-    reinterpret_cast<uint2*>(q)[b] = make_uint2(packed[0], packed[1]);
-    s[b] = (uint8_t)sc;
+    // lanes sub = 0,1 own codes 0..7 of the block (one word), sub = 2,3 codes 8..15
+    uint32_t mine = codes << (16 * (sub & 1));
+    const uint32_t word = mine | __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+    if (valid && (sub & 1) == 0)
+        reinterpret_cast<uint32_t*>(q)[2 * b + (sub >> 1)] = word;
+    if (valid && sub == 0)
+        s[b] = (uint8_t)sc;
 }
 
 cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStream_t stream)
@@ -110,14 +117,26 @@ cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStr
 }
 
 cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float* g,
-                            uint8_t* q, uint8_t* s, cudaStream_t stream)
+                            uint8_t* q, uint8_t* s, cudaStream_t stream, bool pdl)
 {
     const int64_t nblocks = rows * (k / 16);
     if (nblocks == 0)
         return cudaSuccess;
-    const int64_t grid = (nblocks + 255) / 256;
-    quantize_kernel<<<(unsigned)grid, 256, 0, stream>>>(t, nblocks, g, q, s);
-    return cudaGetLastError();
+    const int64_t grid = (4 * nblocks + 255) / 256;
+    if (!pdl) {
+        quantize_kernel<false><<<(unsigned)grid, 256, 0, stream>>>(t, nblocks, g, q, s);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<true>, t, nblocks, g, q, s);
 }
 
 }  // namespace nvfp4

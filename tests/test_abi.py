@@ -87,3 +87,25 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nv, "_lib", None)
     with pytest.raises(ImportError):
         nv.library(str(tmp_path / "missing.so"))
+
+
+def test_gemm_select_host_only(lib):
+    """Kernel selection is host logic: which kernel each shape gets."""
+    AUTO, GENERIC, GEMV = nv.KERNEL_AUTO, nv.KERNEL_GENERIC, nv.KERNEL_GEMV
+    for k in (2048, 4096, 5120, 6144, 8192, 12288, 25600, 10240):
+        assert nv.gemm_select(1, 100, k) == GEMV, k
+        assert nv.gemm_select(2, 100, k, GEMV) == GEMV, k
+    for m, k in ((1, 512), (1, 16), (2, 4112), (1, 9 * 4096 + 2048), (8, 4096)):
+        assert nv.gemm_select(m, 100, k) == GENERIC, (m, k)
+    assert nv.gemm_select(3, 10, 4096, GEMV) == -2
+    assert nv.gemm_select(1, 10, 512, GEMV) == -2
+    assert nv.gemm_select(9, 10, 4096) == -2
+    assert nv.gemm_select(1, 10, 24) == -1
+    assert nv.gemm_select(1, 10, 4096, 77) == -2
+
+
+def test_ex_options_validated(lib):
+    ok = [FAKE] * 7
+    assert lib.nvfp4_gemm_smallm_ex(*ok, 1, 16, 32, 0x200, None) == 1     # unknown flag
+    assert lib.nvfp4_gemm_smallm_ex(*ok, 3, 16, 4096, 2, None) == 2       # GEMV with M = 3
+    assert lib.nvfp4_quantize_act_ex(FAKE, 1, 32, FAKE, FAKE, FAKE, 1, None) == 1

@@ -176,3 +176,89 @@ def test_gemm_full_size_8b(nv, lin, m):
 def test_gemm_full_size_32b(nv, lin, m):
     err = full_size_case(nv, m, lin.n, lin.k, synthetic.WEIGHT_STD_32B, seed=lin.n + 3 * lin.k)
     assert err <= GEMM_TOL
+
+
+# ---- each kernel through the C ABI --------------------------------------------
+
+# K values cover one and two chunks per thread, 1..4 rows per group, CTAs
+# ending in a partial warp (K = 17408, 25600), and row counts that leave the
+# last group and the last CTA partial.
+GEMV_SHAPES = [(1, 16 * 9 + 3, 2048), (2, 40, 4096), (1, 1, 5120), (2, 333, 6144),
+               (1, 70, 8192), (2, 64, 12288), (1, 20, 25600), (2, 5, 10240), (1, 17, 16384),
+               (1, 1000, 1024), (2, 77, 3072), (1, 9, 17408), (2, 3, 32768), (2, 2000, 4096)]
+
+
+@pytest.mark.parametrize("m,n,k", GEMV_SHAPES)
+@pytest.mark.parametrize("pdl", [False, True])
+def test_gemv_kernel(nv, m, n, k, pdl):
+    assert nv.gemm_select(m, n, k, nv.KERNEL_GEMV) == nv.KERNEL_GEMV
+    x = synthetic.activations(m, k, seed=k + m)
+    w = synthetic.weights(n, k, 0.02, seed=n + k)
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg, pdl=pdl)
+    y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_GEMV, pdl=pdl)
+    assert gemm_error(host(y), ref) <= GEMM_TOL
+    yg = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_GENERIC)
+    assert gemm_error(host(yg), ref) <= GEMM_TOL
+
+
+def test_gemv_rejects_unsupported(nv):
+    xq = torch.zeros((3, 2048), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((3, 256), dtype=torch.uint8, device="cuda")
+    wq = torch.zeros((4, 2048), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros((4, 256), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, device="cuda")
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.gemm_smallm(xq, xs, g, wq, ws, g, kernel=nv.KERNEL_GEMV)   # M = 3
+    assert e.value.status == 2
+    small = [torch.zeros(shape, dtype=torch.uint8, device="cuda")
+             for shape in ((1, 8), (1, 1), (4, 8), (4, 1))]
+    with pytest.raises(nv.Nvfp4Error):
+        nv.gemm_smallm(small[0], small[1], g, small[2], small[3], g,
+                       kernel=nv.KERNEL_GEMV)                          # K = 16
+
+
+def test_pdl_chain_in_graph(nv):
+    """quantize -> GEMM pairs with programmatic dependent launch, captured in
+    a CUDA graph and replayed, equal the plain launches bit for bit."""
+    lin = synthetic.LINEARS_8B
+    xs_, ws_, refs = [], [], []
+    for j, l in enumerate(lin):
+        x = dev(synthetic.activations(1, l.k, seed=50 + j))
+        w = nv.pack_weight(dev(synthetic.weights(l.n, l.k, 0.02, seed=60 + j)))
+        xs_.append((x, nv.global_scale(x)))
+        ws_.append(w)
+    outs = [torch.empty((1, l.n), device="cuda") for l in lin]
+    plain = []
+    for j in range(4):
+        xq, xsc = nv.quantize_act(*xs_[j])
+        plain.append(nv.gemm_smallm(xq, xsc, xs_[j][1], *ws_[j]))
+    bufs = [(torch.empty((1, l.k // 2), dtype=torch.uint8, device="cuda"),
+             torch.empty((1, l.k // 16), dtype=torch.uint8, device="cuda")) for l in lin]
+
+    def step():
+        for j in range(4):
+            nv.quantize_act(*xs_[j], out=bufs[j], pdl=True)
+            nv.gemm_smallm(*bufs[j], xs_[j][1], *ws_[j], out=outs[j], pdl=True)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for j in range(4):
+        np.testing.assert_array_equal(host(outs[j]), host(plain[j]))
