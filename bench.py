@@ -260,6 +260,86 @@ def time_graph(torch, g, reps: int, warm: int = 3) -> float:
     return a.elapsed_time(b) / reps
 
 
+def make_weights(nv, torch, lin, std, copies, seed):
+    gen = torch.Generator(device="cuda")
+    out = []
+    for c in range(copies):
+        gen.manual_seed(seed + c)
+        wf = torch.randn((lin.n, lin.k), generator=gen, device="cuda", dtype=torch.float32)
+        wf.mul_(std)
+        out.append(nv.pack_weight(wf))
+        del wf
+    return out
+
+
+def time_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
+    """µs per call of one linear shape at this M: a graph of len(weights) GEMMs
+    over distinct weight copies (larger than L2 together), replayed."""
+    xa = synthetic.activations(m, lin.k, seed=seed)
+    xd = torch.from_numpy(xa).cuda()
+    xg = nv.global_scale(xd)
+    xq, xs = nv.quantize_act(xd, xg)
+    y = torch.empty((m, lin.n), device="cuda")
+
+    def calls():
+        for wq, ws, wg in weights:
+            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel, pdl=pdl)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    ms = time_graph(torch, g, reps=reps)
+    us = ms * 1e3 / len(weights)
+    b = algorithmic_bytes(m, lin.n, lin.k)["gemm"]
+    return {"us_per_call": round(us, 3), "GBps": round(b / (us * 1e-6) / 1e9, 1)}
+
+
+def sweep(nv, torch, stack, peaks, args) -> dict:
+    """µs/call and GB/s of every linear shape for every M of the sweep, with
+    the library's kernel choice and with each kernel that takes the shape."""
+    kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "generic": nv.KERNEL_GENERIC}
+    out = {"8B": {}, "32B": {}}
+    reps = 5
+    w8 = {j: [stack.w[l][j] for l in range(stack.layers)] for j in range(4)}
+    for m in synthetic.M_SWEEP_8B:
+        row = {}
+        for j, lin in enumerate(synthetic.LINEARS_8B):
+            auto = nv.gemm_select(m, lin.n, lin.k)
+            ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
+            for name, kid in kernels.items():
+                if name == "generic" and not args.sweep_generic:
+                    continue
+                if nv.gemm_select(m, lin.n, lin.k, kid) != kid:
+                    continue
+                ent[name] = time_linear(nv, torch, w8[j], lin, m, kid, stack.pdl, reps)
+            ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
+            row[lin.name] = ent
+        out["8B"][f"M={m}"] = row
+    for j, lin in enumerate(synthetic.LINEARS_32B):
+        per_copy = lin.n * lin.k * 9 // 16
+        copies = max(3, -(-400_000_000 // per_copy))
+        ws = make_weights(nv, torch, lin, synthetic.WEIGHT_STD_32B, copies, seed=4000 + 100 * j)
+        for m in synthetic.M_SWEEP_32B:
+            auto = nv.gemm_select(m, lin.n, lin.k)
+            ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
+            for name, kid in kernels.items():
+                if name == "generic" and not args.sweep_generic:
+                    continue
+                if nv.gemm_select(m, lin.n, lin.k, kid) != kid:
+                    continue
+                ent[name] = time_linear(nv, torch, ws, lin, m, kid, stack.pdl, reps)
+            ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
+            out["32B"].setdefault(f"M={m}", {})[lin.name] = ent
+        del ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args) -> dict:
     import torch
 
@@ -332,6 +412,7 @@ def run_ours(args) -> dict:
 
     # ---- end to end: pinned host X in, host Y out, through the public API
     e2e = run_e2e(torch, stack, args)
+    sweep_detail = None if args.no_sweep else sweep(nv, torch, stack, peaks, args)
 
     traffic = profile_traffic("gemm_smallm")
     line = {
@@ -359,7 +440,8 @@ def run_ours(args) -> dict:
         "e2e": e2e,
         "wall_s_timed": round(wall, 4),
         "detail": {"per_linear_m1": per_linear,
-                   "step_frac_of_peak": round(value / world / peaks["hbm_gbs"], 4)},
+                   "step_frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
+                   "sweep": sweep_detail},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
@@ -527,6 +609,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-shape M sweep (8B M=1,2,4,8; 32B M=1,4)")
+    ap.add_argument("--sweep-generic", action="store_true",
+                    help="also time the shape-general kernel in the sweep")
     ap.add_argument("--profile-step", action="store_true",
                     help="replay only the step graph (warmup + steps times) and exit")
     args = ap.parse_args()

@@ -125,9 +125,12 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       entry points use).
  * NVFP4_KERNEL_GENERIC  the shape-general CUDA-core kernel (any K % 16 == 0).
  * NVFP4_KERNEL_GEMV     the persistent CUDA-core weight-streaming kernel:
- *                       M <= 2, K a multiple of 1024 (of 2048 above 16384)
- *                       and at most 32768, x_q/w_q 16-byte and x_s/w_s
- *                       4-byte aligned; NVFP4_ERR_UNSUPPORTED otherwise.
+ *                       M <= 2, K a multiple of 1024 and at most 32768.
+ * NVFP4_KERNEL_MMA      the tensor-core kernel (mma.sync f16, swap-AB, FP32
+ *                       accumulation): M <= 8, K a multiple of 256 that the
+ *                       kernel can cut into at most 8 cluster ranks.
+ *   The GEMV and MMA kernels need x_q/w_q 32-byte and x_s/w_s 4-byte aligned;
+ *   a request they cannot take returns NVFP4_ERR_UNSUPPORTED.
  * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
  *                       while the previous kernel on the stream is still
  *                       running and waits for it before it touches anything
@@ -139,6 +142,7 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_KERNEL_AUTO 0u
 #define NVFP4_KERNEL_GENERIC 1u
 #define NVFP4_KERNEL_GEMV 2u
+#define NVFP4_KERNEL_MMA 3u
 #define NVFP4_KERNEL_MASK 0xFFu
 #define NVFP4_FLAG_PDL 0x100u
 

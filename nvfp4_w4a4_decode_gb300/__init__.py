@@ -48,8 +48,8 @@ SIGNATURES = {
     "nvfp4_gemm_select": ([_i64, _i64, _i64, ctypes.c_uint32], ctypes.c_int),
 }
 
-KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV = 0, 1, 2
-KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv"}
+KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA = 0, 1, 2, 3
+KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma"}
 FLAG_PDL = 0x100
 
 
@@ -136,7 +136,7 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
                       kernel: int = KERNEL_AUTO, pdl: bool = False) -> torch.Tensor:
     """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32.
 
-    ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV); ``pdl`` lets
+    ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA); ``pdl`` lets
     the launch overlap the previous kernel (weights must not be written by
     it)."""
     for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):

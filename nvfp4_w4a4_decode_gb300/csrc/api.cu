@@ -93,10 +93,15 @@ int select_kernel(int64_t m, int64_t k, uint32_t options, bool ptrs_ok_fast)
 {
     const uint32_t req = options & NVFP4_KERNEL_MASK;
     const bool gemv_ok = nvfp4::gemv_supported(m, k) && ptrs_ok_fast;
+    const bool mma_ok = nvfp4::mma_supported(m, k) && ptrs_ok_fast;
     switch (req) {
-    case NVFP4_KERNEL_AUTO: return gemv_ok ? (int)NVFP4_KERNEL_GEMV : (int)NVFP4_KERNEL_GENERIC;
+    case NVFP4_KERNEL_AUTO:
+        if (gemv_ok)
+            return (int)NVFP4_KERNEL_GEMV;
+        return mma_ok ? (int)NVFP4_KERNEL_MMA : (int)NVFP4_KERNEL_GENERIC;
     case NVFP4_KERNEL_GENERIC: return (int)NVFP4_KERNEL_GENERIC;
     case NVFP4_KERNEL_GEMV: return gemv_ok ? (int)NVFP4_KERNEL_GEMV : -(int)NVFP4_ERR_UNSUPPORTED;
+    case NVFP4_KERNEL_MMA: return mma_ok ? (int)NVFP4_KERNEL_MMA : -(int)NVFP4_ERR_UNSUPPORTED;
     default: return -(int)NVFP4_ERR_UNSUPPORTED;
     }
 }
@@ -134,7 +139,7 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x_q, 8) || !aligned(w_q, 8) || !aligned(x_g, 4) || !aligned(w_g, 4))
         return NVFP4_ERR_INVALID_ARG;
-    const bool fast_ptrs = aligned(x_q, 16) && aligned(w_q, 16) && aligned(x_s, 4) &&
+    const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
                            aligned(w_s, 4);
     const int kern = select_kernel(m, k, options, fast_ptrs);
     if (kern < 0)
@@ -144,6 +149,8 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
     switch (kern) {
     case NVFP4_KERNEL_GEMV:
         return from_cuda(nvfp4::launch_gemm_gemv(a, pdl));
+    case NVFP4_KERNEL_MMA:
+        return from_cuda(nvfp4::launch_gemm_mma(a, pdl));
     default:
         return from_cuda(nvfp4::launch_gemm_generic(a));
     }

@@ -34,4 +34,10 @@ cudaError_t launch_gemm_generic(const GemmArgs& a);
 bool gemv_supported(int64_t m, int64_t k);
 cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl);
 
+// Tensor-core (mma.sync f16, swap-AB) kernel: m in 1..8, k a multiple of 256
+// that splits into at most 8 cluster ranks of 4..16 warps x 1, 2 or 4
+// 256-element ranges; x_q/w_q 32-byte and x_s/w_s 4-byte aligned.
+bool mma_supported(int64_t m, int64_t k);
+cudaError_t launch_gemm_mma(const GemmArgs& a, bool pdl);
+
 }  // namespace nvfp4

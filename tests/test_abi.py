@@ -95,13 +95,21 @@ def test_gemm_select_host_only(lib):
     for k in (2048, 4096, 5120, 6144, 8192, 12288, 25600, 10240):
         assert nv.gemm_select(1, 100, k) == GEMV, k
         assert nv.gemm_select(2, 100, k, GEMV) == GEMV, k
-    for m, k in ((1, 512), (1, 16), (2, 4112), (1, 9 * 4096 + 2048), (8, 4096)):
+    for m, k in ((1, 384), (1, 16), (2, 4112), (8, 4112), (3, 48)):
         assert nv.gemm_select(m, 100, k) == GENERIC, (m, k)
     assert nv.gemm_select(3, 10, 4096, GEMV) == -2
     assert nv.gemm_select(1, 10, 512, GEMV) == -2
     assert nv.gemm_select(9, 10, 4096) == -2
     assert nv.gemm_select(1, 10, 24) == -1
     assert nv.gemm_select(1, 10, 4096, 77) == -2
+    MMA = nv.KERNEL_MMA
+    for m in range(1, 9):
+        for k in (1024, 2048, 4096, 5120, 8192, 12288, 25600):
+            assert nv.gemm_select(m, 100, k, MMA) == MMA, (m, k)
+        assert nv.gemm_select(m, 100, 4096) == (GEMV if m <= 2 else MMA)
+    assert nv.gemm_select(1, 10, 384, MMA) == -2          # too few 128-ranges
+    assert nv.gemm_select(4, 10, 256 * 37, MMA) == -2     # 74 ranges: no split fits
+    assert nv.gemm_select(4, 10, 256 * 37) == GENERIC
 
 
 def test_ex_options_validated(lib):

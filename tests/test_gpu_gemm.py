@@ -262,3 +262,47 @@ def test_pdl_chain_in_graph(nv):
     torch.cuda.synchronize()
     for j in range(4):
         np.testing.assert_array_equal(host(outs[j]), host(plain[j]))
+
+
+# Tensor-core kernel: every M, K values that take 1..5 cluster ranks and
+# 1, 2 or 4 ranges per warp, row counts below one tile, odd tile counts and a
+# ragged last tile.
+MMA_SHAPES = [(1024, 37), (2048, 5), (4096, 16 * 37 + 5), (5120, 300), (8192, 33),
+              (12288, 64), (25600, 21), (6144, 17 * 16)]
+
+
+@pytest.mark.parametrize("k,n", MMA_SHAPES)
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 8])
+def test_mma_kernel(nv, m, n, k):
+    assert nv.gemm_select(m, n, k, nv.KERNEL_MMA) == nv.KERNEL_MMA
+    x = synthetic.activations(m, k, seed=k + 7 * m)
+    w = synthetic.weights(n, k, 0.02, seed=n + 3 * k)
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_MMA)
+    assert gemm_error(host(y), ref) <= GEMM_TOL
+    y2 = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_MMA, pdl=True)
+    np.testing.assert_array_equal(host(y2), host(y))
+
+
+def test_mma_decades_of_scales(nv):
+    """Extreme block scales stay exact in the folded FP16 operands."""
+    m, n, k = 8, 96, 4096
+    x = synthetic.log_uniform_blocks(m, k, seed=13)
+    w = synthetic.log_uniform_blocks(n, k, seed=14)
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_MMA)
+    assert gemm_error(host(y), ref) <= GEMM_TOL
