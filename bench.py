@@ -302,7 +302,8 @@ def time_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
 def sweep(nv, torch, stack, peaks, args) -> dict:
     """µs/call and GB/s of every linear shape for every M of the sweep, with
     the library's kernel choice and with each kernel that takes the shape."""
-    kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "generic": nv.KERNEL_GENERIC}
+    kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA,
+               "generic": nv.KERNEL_GENERIC}
     out = {"8B": {}, "32B": {}}
     reps = 5
     w8 = {j: [stack.w[l][j] for l in range(stack.layers)] for j in range(4)}

@@ -129,8 +129,18 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  * NVFP4_KERNEL_MMA      the tensor-core kernel (mma.sync f16, swap-AB, FP32
  *                       accumulation): M <= 8, K a multiple of 256 that the
  *                       kernel can cut into at most 8 cluster ranks.
- *   The GEMV and MMA kernels need x_q/w_q 32-byte and x_s/w_s 4-byte aligned;
- *   a request they cannot take returns NVFP4_ERR_UNSUPPORTED.
+ * NVFP4_KERNEL_TMA      the tensor-core kernel fed by bulk asynchronous copies
+ *                       (cp.async.bulk + mbarrier ring in shared memory):
+ *                       M <= 8, K a multiple of 256 (per cluster rank), N
+ *                       below 2^30.
+ *   The GEMV and MMA kernels need x_q/w_q 32-byte and x_s/w_s 4-byte
+ *   aligned, the TMA kernel all four 32-byte aligned; a request a kernel
+ *   cannot take returns NVFP4_ERR_UNSUPPORTED.
+ * NVFP4_FLAG_TEST_WAIT_TIMEOUT  test hook of the TMA kernel: the first stage
+ *                       waits for 16 bytes that never come, so its bounded
+ *                       wait runs out (after a few microseconds) and the
+ *                       kernel records NVFP4_DEVICE_WAIT_TIMEOUT; Y is left
+ *                       unspecified.  For testing the timeout path only.
  * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
  *                       while the previous kernel on the stream is still
  *                       running and waits for it before it touches anything
@@ -143,8 +153,13 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_KERNEL_GENERIC 1u
 #define NVFP4_KERNEL_GEMV 2u
 #define NVFP4_KERNEL_MMA 3u
+#define NVFP4_KERNEL_TMA 4u
 #define NVFP4_KERNEL_MASK 0xFFu
 #define NVFP4_FLAG_PDL 0x100u
+#define NVFP4_FLAG_TEST_WAIT_TIMEOUT 0x10000u
+
+/* Bits of the device status word (nvfp4_device_status). */
+#define NVFP4_DEVICE_WAIT_TIMEOUT 1u
 
 /* nvfp4_quantize_act with options (only NVFP4_FLAG_PDL is meaningful). */
 int nvfp4_quantize_act_ex(const float* x, int64_t m, int64_t k, const float* x_g,
@@ -164,6 +179,15 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
  * counterpart of the README's "nvfp4r.status()" inspection.
  */
 int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options);
+
+/*
+ * Device status word of the library on the current device: the OR of the
+ * NVFP4_DEVICE_* bits recorded by kernels since it was last cleared (a wait
+ * that ran out of its budget sets NVFP4_DEVICE_WAIT_TIMEOUT; the results of
+ * that launch are unspecified).  Synchronises `stream`; with clear != 0 the
+ * word is reset to 0 afterwards.  *flags is written on the host.
+ */
+int nvfp4_device_status(void* stream, uint32_t* flags, int clear);
 
 #ifdef __cplusplus
 }

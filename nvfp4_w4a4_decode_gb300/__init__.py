@@ -46,11 +46,15 @@ SIGNATURES = {
     "nvfp4_gemm_smallm_ex": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_uint32, _p],
                              ctypes.c_int),
     "nvfp4_gemm_select": ([_i64, _i64, _i64, ctypes.c_uint32], ctypes.c_int),
+    "nvfp4_device_status": ([_p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int], ctypes.c_int),
 }
 
-KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA = 0, 1, 2, 3
-KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma"}
+KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA = 0, 1, 2, 3, 4
+KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma",
+                KERNEL_TMA: "tma"}
 FLAG_PDL = 0x100
+FLAG_TEST_WAIT_TIMEOUT = 0x10000
+DEVICE_WAIT_TIMEOUT = 1
 
 
 class Nvfp4Error(RuntimeError):
@@ -133,7 +137,8 @@ def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None, pdl: bool = 
 
 
 def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
-                      kernel: int = KERNEL_AUTO, pdl: bool = False) -> torch.Tensor:
+                      kernel: int = KERNEL_AUTO, pdl: bool = False,
+                      test_wait_timeout: bool = False) -> torch.Tensor:
     """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32.
 
     ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA); ``pdl`` lets
@@ -149,7 +154,7 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
     if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
         raise ValueError("operand shapes disagree")
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
-    opts = int(kernel) | (FLAG_PDL if pdl else 0)
+    opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0)
     _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm_ex(
         xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
         wg.data_ptr(), y.data_ptr(), m, n, k, opts, _stream(xq)))
@@ -159,6 +164,14 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
 def nvfp4_gemm_select(m: int, n: int, k: int, kernel: int = KERNEL_AUTO) -> int:
     """Kernel id the library runs for this shape (negative status if none)."""
     return library().nvfp4_gemm_select(m, n, k, kernel)
+
+
+def nvfp4_device_status(clear: bool = True, stream=None) -> int:
+    """Device status bits recorded by the kernels (synchronises the stream)."""
+    v = ctypes.c_uint32(0)
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _check("nvfp4_device_status", library().nvfp4_device_status(st, ctypes.byref(v), int(clear)))
+    return int(v.value)
 
 
 def linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg) -> torch.Tensor:
@@ -172,3 +185,4 @@ pack_weight = nvfp4_pack_weight
 quantize_act = nvfp4_quantize_act
 gemm_smallm = nvfp4_gemm_smallm
 gemm_select = nvfp4_gemm_select
+device_status = nvfp4_device_status

@@ -89,19 +89,27 @@ namespace {
 
 // Kernel for a GEMM of this shape and operand alignment (negative status on
 // a request that cannot be met).
-int select_kernel(int64_t m, int64_t k, uint32_t options, bool ptrs_ok_fast)
+int select_kernel(int64_t m, int64_t n, int64_t k, uint32_t options, bool ptrs_ok_fast,
+                  bool ptrs_ok_tma)
 {
     const uint32_t req = options & NVFP4_KERNEL_MASK;
     const bool gemv_ok = nvfp4::gemv_supported(m, k) && ptrs_ok_fast;
     const bool mma_ok = nvfp4::mma_supported(m, k) && ptrs_ok_fast;
+    const bool tma_ok = nvfp4::tma_supported(m, n, k) && ptrs_ok_tma;
     switch (req) {
     case NVFP4_KERNEL_AUTO:
+        // measured on GB300 over the 8B / 32B decode shapes: the CUDA-core
+        // stream wins at M <= 2, the TMA-fed tensor-core kernel at larger M
+        // when K fits one CTA, the register-streaming one otherwise
         if (gemv_ok)
             return (int)NVFP4_KERNEL_GEMV;
+        if (tma_ok && nvfp4::tma_single_cta_k(m, k))
+            return (int)NVFP4_KERNEL_TMA;
         return mma_ok ? (int)NVFP4_KERNEL_MMA : (int)NVFP4_KERNEL_GENERIC;
     case NVFP4_KERNEL_GENERIC: return (int)NVFP4_KERNEL_GENERIC;
     case NVFP4_KERNEL_GEMV: return gemv_ok ? (int)NVFP4_KERNEL_GEMV : -(int)NVFP4_ERR_UNSUPPORTED;
     case NVFP4_KERNEL_MMA: return mma_ok ? (int)NVFP4_KERNEL_MMA : -(int)NVFP4_ERR_UNSUPPORTED;
+    case NVFP4_KERNEL_TMA: return tma_ok ? (int)NVFP4_KERNEL_TMA : -(int)NVFP4_ERR_UNSUPPORTED;
     default: return -(int)NVFP4_ERR_UNSUPPORTED;
     }
 }
@@ -114,7 +122,7 @@ int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options)
         return -NVFP4_ERR_INVALID_ARG;
     if (m > 8)
         return -NVFP4_ERR_UNSUPPORTED;
-    return select_kernel(m, k, options, true);
+    return select_kernel(m, n, k, options, true, true);
 }
 
 int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
@@ -123,7 +131,10 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
 {
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
         return NVFP4_ERR_INVALID_ARG;
-    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL)) != 0)
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL |
+                               NVFP4_FLAG_TEST_WAIT_TIMEOUT)) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if ((options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) && (options & NVFP4_KERNEL_MASK) != NVFP4_KERNEL_TMA)
         return NVFP4_ERR_INVALID_ARG;
     if (m > 8)
         return NVFP4_ERR_UNSUPPORTED;
@@ -141,7 +152,8 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
         return NVFP4_ERR_INVALID_ARG;
     const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
                            aligned(w_s, 4);
-    const int kern = select_kernel(m, k, options, fast_ptrs);
+    const bool tma_ptrs = fast_ptrs && aligned(x_s, 32) && aligned(w_s, 32);
+    const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs);
     if (kern < 0)
         return -kern;
     const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
@@ -151,9 +163,23 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
         return from_cuda(nvfp4::launch_gemm_gemv(a, pdl));
     case NVFP4_KERNEL_MMA:
         return from_cuda(nvfp4::launch_gemm_mma(a, pdl));
+    case NVFP4_KERNEL_TMA:
+        return from_cuda(nvfp4::launch_gemm_tma(a, pdl, (options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) != 0));
     default:
         return from_cuda(nvfp4::launch_gemm_generic(a));
     }
+}
+
+int nvfp4_device_status(void* stream, uint32_t* flags, int clear)
+{
+    if (flags == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    unsigned v = 0u;
+    const cudaError_t e = nvfp4::read_device_status(static_cast<cudaStream_t>(stream), &v, clear != 0);
+    if (e != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    *flags = v;
+    return NVFP4_OK;
 }
 
 int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,

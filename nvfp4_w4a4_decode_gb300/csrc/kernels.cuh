@@ -40,4 +40,13 @@ cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl);
 bool mma_supported(int64_t m, int64_t k);
 cudaError_t launch_gemm_mma(const GemmArgs& a, bool pdl);
 
+// Tensor-core kernel fed by cp.async.bulk into a shared-memory ring: m in
+// 1..8, k a multiple of 256 per cluster rank, n < 2^30; all operand pointers
+// 32-byte aligned.  test_timeout arms the bounded-wait test hook.
+bool tma_supported(int64_t m, int64_t n, int64_t k);
+// true when the TMA kernel keeps the whole K in one CTA (no cluster split)
+bool tma_single_cta_k(int64_t m, int64_t k);
+cudaError_t launch_gemm_tma(const GemmArgs& a, bool pdl, bool test_timeout);
+cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
+
 }  // namespace nvfp4

@@ -106,7 +106,8 @@ def test_gemm_select_host_only(lib):
     for m in range(1, 9):
         for k in (1024, 2048, 4096, 5120, 8192, 12288, 25600):
             assert nv.gemm_select(m, 100, k, MMA) == MMA, (m, k)
-        assert nv.gemm_select(m, 100, 4096) == (GEMV if m <= 2 else MMA)
+        assert nv.gemm_select(m, 100, 4096) == (GEMV if m <= 2 else nv.KERNEL_TMA)
+        assert nv.gemm_select(m, 100, 12288) in ((GEMV,) if m <= 2 else (MMA, nv.KERNEL_TMA))
     assert nv.gemm_select(1, 10, 384, MMA) == -2          # too few 128-ranges
     assert nv.gemm_select(4, 10, 256 * 37, MMA) == -2     # 74 ranges: no split fits
     assert nv.gemm_select(4, 10, 256 * 37) == GENERIC

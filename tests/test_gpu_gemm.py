@@ -306,3 +306,60 @@ def test_mma_decades_of_scales(nv):
     xq, xs = nv.quantize_act(xd, xg)
     y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_MMA)
     assert gemm_error(host(y), ref) <= GEMM_TOL
+
+
+# TMA-fed tensor-core kernel: every M, one to five cluster ranks, 2..4 ring
+# stages, fewer rows than a tile, a ragged last tile, more tiles than ring
+# stages per CTA.
+TMA_SHAPES = [(512, 37), (1024, 5), (2048, 16 * 70 + 5), (4096, 16 * 37 + 5), (5120, 300),
+              (6144, 17 * 16), (8192, 33), (12288, 64), (25600, 21), (4096, 40000)]
+
+
+@pytest.mark.parametrize("k,n", TMA_SHAPES)
+@pytest.mark.parametrize("m", [1, 2, 4, 8])
+def test_tma_kernel(nv, m, n, k):
+    assert nv.gemm_select(m, n, k, nv.KERNEL_TMA) == nv.KERNEL_TMA
+    x = synthetic.activations(m, k, seed=k + 11 * m)
+    w = synthetic.weights(n, k, 0.02, seed=n + 5 * k)
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    y = host(nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_TMA))
+    if n <= 4096:
+        ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+        assert gemm_error(y, ref) <= GEMM_TOL
+    else:  # many tiles: check a sample of rows (first, last, random)
+        rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(n).integers(0, n, 62)]))
+        ref = oracle.gemm(xq_o, xs_o, gx, wq_o[rows], ws_o[rows], gw)
+        rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+        assert sampled_error(y[:, rows], ref, rms) <= GEMM_TOL
+    y2 = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_TMA, pdl=True)
+    np.testing.assert_array_equal(host(y2), y)
+    assert nv.device_status() == 0
+
+
+def test_tma_bounded_wait_times_out_and_recovers(nv):
+    """The test hook makes the first stage wait for bytes that never come:
+    the bounded wait runs out, the kernel records the timeout and returns,
+    and the context stays usable for a normal launch afterwards."""
+    m, n, k = 1, 32, 4096
+    x = synthetic.activations(m, k, seed=1)
+    w = synthetic.weights(n, k, 0.02, seed=2)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    assert nv.device_status() == 0
+    nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_TMA, test_wait_timeout=True)
+    assert nv.device_status(clear=True) & nv.DEVICE_WAIT_TIMEOUT
+    assert nv.device_status() == 0
+    y = host(nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_TMA))
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    assert gemm_error(y, oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)) <= GEMM_TOL
+    assert nv.device_status() == 0
