@@ -149,14 +149,21 @@ def barrier(world: int):
         dist.barrier()
 
 
-def reduce_max(v: float, world: int) -> float:
+def reduce_max(v: float, world: int, device: str = "cuda") -> float:
+    """Max of v over the ranks (the slowest rank's time sets the job's)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, ms_step_max: float, world: int) -> float:
+    """Whole-job GB/s: every rank moves its own bytes per step (replicas, weak
+    scaling); the step time is the maximum over ranks."""
+    return world * bytes_per_rank_step / (ms_step_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -167,10 +174,12 @@ class DecodeStack:
     """36 layers x 4 linears of packed weights resident in HBM, per-call
     activation buffers, and the graphs that replay them."""
 
-    def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True):
+    def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
+                 fused: bool = True):
         self.nv, self.torch = nv, torch
         self.m = m
         self.pdl = pdl
+        self.fused = fused
         self.layers = layers
         self.lins = synthetic.LINEARS_8B
         dev = torch.device("cuda")
@@ -186,31 +195,45 @@ class DecodeStack:
                 del wf
             self.w.append(row)
         torch.cuda.synchronize()
-        # activations: X ~ N(0,1) with 0.5 % x20 outlier channels, per call
-        self.x, self.xg = [], []
+        # activations: X ~ N(0,1) with 0.5 % x20 outlier channels, per call;
+        # all calls' X (and Y) are views of one flat buffer, so a step's inputs
+        # and outputs move between host and device in one copy each
+        xsz = sum(m * lin.k for lin in self.lins) * layers
+        ysz = sum(m * lin.n for lin in self.lins) * layers
+        self.x_flat = torch.empty(xsz, dtype=torch.float32, device=dev)
+        self.y_flat = torch.empty(ysz, dtype=torch.float32, device=dev)
+        self.x, self.xg, self.y = [], [], []
+        xo = yo = 0
         for l in range(layers):
-            xr, gr = [], []
+            xr, gr, yr = [], [], []
             for j, lin in enumerate(self.lins):
                 xa = synthetic.activations(m, lin.k, seed=synthetic.weight_seed(seed + 7, l, j))
-                xd = torch.from_numpy(xa).to(dev)
+                xd = self.x_flat[xo:xo + m * lin.k].view(m, lin.k)
+                xd.copy_(torch.from_numpy(xa))
+                xo += m * lin.k
                 xr.append(xd)
                 gr.append(nv.global_scale(xd))     # static calibration, not timed
+                yr.append(self.y_flat[yo:yo + m * lin.n].view(m, lin.n))
+                yo += m * lin.n
             self.x.append(xr)
             self.xg.append(gr)
+            self.y.append(yr)
         self.xq = [(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
                     torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev)) for lin in self.lins]
-        self.y = [[torch.empty((m, lin.n), dtype=torch.float32, device=dev) for lin in self.lins]
-                  for _ in range(layers)]
         torch.cuda.synchronize()
 
     def step(self):
         nv = self.nv
         for l in range(self.layers):
             for j in range(4):
-                xq, xs = self.xq[j]
-                nv.quantize_act(self.x[l][j], self.xg[l][j], out=(xq, xs), pdl=self.pdl)
                 wq, ws, wg = self.w[l][j]
-                nv.gemm_smallm(xq, xs, self.xg[l][j], wq, ws, wg, out=self.y[l][j], pdl=self.pdl)
+                nv.linear(self.x[l][j], self.xg[l][j], wq, ws, wg, out=self.y[l][j],
+                          x_out=self.xq[j], pdl=self.pdl, fused=self.fused)
+
+    def quantize_all(self):
+        """Fill the per-shape activation buffers (before GEMM-only timing)."""
+        for j in range(4):
+            self.nv.quantize_act(self.x[-1][j], self.xg[-1][j], out=self.xq[j])
 
     def gemm_only(self, j=None):
         nv = self.nv
@@ -355,7 +378,8 @@ def run_ours(args) -> dict:
     nv.library()
     peaks = load_peaks()
 
-    stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl)
+    stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
+                        fused=args.fused)
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -363,7 +387,9 @@ def run_ours(args) -> dict:
             step_graph.replay()
         torch.cuda.synchronize()
         return None
-    launches_per_step = 2 * 4 * stack.layers
+    launches_per_step = sum(1 if (stack.fused and nv.gemm_select(args.m, lin.n, lin.k)
+                                  == nv.KERNEL_GEMV) else 2
+                            for lin in stack.lins) * stack.layers
     bytes_step = stack.bytes_per_step()
     alg_step = bytes_step["gemm"] + bytes_step["quant"]
 
@@ -388,9 +414,10 @@ def run_ours(args) -> dict:
     barrier(world)
     ms_step = ev0.elapsed_time(ev1) / args.steps
     ms_step_max = reduce_max(ms_step, world)
-    value = world * alg_step / (ms_step_max * 1e-3) / 1e9
+    value = job_throughput(alg_step, ms_step_max, world)
 
     # ---- dominant kernel: the GEMM alone, same calls, same graph discipline
+    stack.quantize_all()
     gemm_graph = stack.capture(stack.gemm_only)
     ms_gemm = time_graph(torch, gemm_graph, reps=max(3, args.steps // 2))
     gemm_launches = 4 * stack.layers
@@ -412,7 +439,7 @@ def run_ours(args) -> dict:
         del g
 
     # ---- end to end: pinned host X in, host Y out, through the public API
-    e2e = run_e2e(torch, stack, args)
+    e2e = run_e2e(torch, stack, step_graph, args)
     sweep_detail = None if args.no_sweep else sweep(nv, torch, stack, peaks, args)
 
     traffic = profile_traffic("gemm_smallm")
@@ -428,7 +455,8 @@ def run_ours(args) -> dict:
                    "l2": "inputs larger than L2: 3.9 GB of packed weights per step",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "graph": "one CUDA graph per step",
-                   "pdl": not args.no_pdl},
+                   "pdl": not args.no_pdl,
+                   "fused_quantize": args.fused},
         "roofline": {"bound": "hbm", "kernel": "nvfp4_gemm_smallm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
@@ -449,29 +477,25 @@ def run_ours(args) -> dict:
     return line if rank == 0 else None
 
 
-def run_e2e(torch, stack, args) -> dict:
-    """Same step, but each step copies its activations from pinned host memory
-    and reads its outputs back to pinned host memory, inside the timed region."""
-    xs_host = [[x.cpu().pin_memory() for x in row] for row in stack.x]
-    ys_host = [[torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in row] for row in stack.y]
-    h2d = sum(x.numel() * 4 for row in xs_host for x in row)
-    d2h = sum(y.numel() * 4 for row in ys_host for y in row)
-    nv = stack.nv
+def run_e2e(torch, stack, step_graph, args) -> dict:
+    """End to end through the public API: every step copies all of its
+    activations from pinned host memory to the device, replays the step (the
+    same graph of C-ABI calls) and reads all of its outputs back to pinned host
+    memory -- both copies inside the timed region."""
+    x_host = stack.x_flat.cpu().pin_memory()
+    y_host = torch.empty(stack.y_flat.shape, dtype=torch.float32).pin_memory()
+    h2d = x_host.numel() * 4
+    d2h = y_host.numel() * 4
 
     def one_step():
-        for l in range(stack.layers):
-            for j in range(4):
-                stack.x[l][j].copy_(xs_host[l][j], non_blocking=True)
-                xq, xs = stack.xq[j]
-                nv.quantize_act(stack.x[l][j], stack.xg[l][j], out=(xq, xs))
-                wq, ws, wg = stack.w[l][j]
-                nv.gemm_smallm(xq, xs, stack.xg[l][j], wq, ws, wg, out=stack.y[l][j])
-                ys_host[l][j].copy_(stack.y[l][j], non_blocking=True)
+        stack.x_flat.copy_(x_host, non_blocking=True)
+        step_graph.replay()
+        y_host.copy_(stack.y_flat, non_blocking=True)
 
-    for _ in range(max(2, args.warmup)):
+    for _ in range(max(3, args.warmup)):
         one_step()
     torch.cuda.synchronize()
-    reps = max(3, args.steps // 2)
+    reps = max(10, args.steps // 3)
     t0 = time.perf_counter()
     for _ in range(reps):
         one_step()
@@ -481,7 +505,8 @@ def run_e2e(torch, stack, args) -> dict:
     v = (b["gemm"] + b["quant"]) / sec / 1e9
     return {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3),
-            "path": "eager C-ABI calls per linear with pinned host<->device copies"}
+            "path": "per step: pinned H2D of all activations, the step's CUDA graph of "
+                    "nvfp4_linear calls, D2H of all outputs; wall clock"}
 
 
 def profile_traffic(kernel: str):
@@ -608,6 +633,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="one kernel per linear (quantisation in the GEMM prologue) instead of "
+                         "quantiser + GEMM")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--no-sweep", action="store_true",

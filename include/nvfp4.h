@@ -156,6 +156,7 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_KERNEL_TMA 4u
 #define NVFP4_KERNEL_MASK 0xFFu
 #define NVFP4_FLAG_PDL 0x100u
+#define NVFP4_FLAG_FUSED_QUANTIZE 0x200u
 #define NVFP4_FLAG_TEST_WAIT_TIMEOUT 0x10000u
 
 /* Bits of the device status word (nvfp4_device_status). */
@@ -179,6 +180,27 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
  * counterpart of the README's "nvfp4r.status()" inspection.
  */
 int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options);
+
+/*
+ * One W4A4 decode linear: quantise X[m][k] with the static tensor scale *x_g
+ * (exactly as nvfp4_quantize_act: the codes and scales are written to x_q and
+ * x_s) and compute Y[m][n] = X . W^T from them (as nvfp4_gemm_smallm_ex with
+ * `options`): two launches.  With NVFP4_FLAG_FUSED_QUANTIZE, and when the
+ * chosen kernel is the CUDA-core stream (M <= 2, K a multiple of 1024), it is
+ * ONE kernel instead: each CTA quantises X cooperatively in its prologue (same
+ * bytes as the stand-alone quantiser; CTA 0 stores them).  One launch is
+ * cheaper for a lone call; inside a CUDA graph with NVFP4_FLAG_PDL the two
+ * launches measured faster (the separate quantiser overlaps the previous GEMM,
+ * the fused prologue does not), hence the default.  With NVFP4_FLAG_PDL the
+ * kernel(s) start streaming weights before the previous kernel on the stream
+ * has finished (the weights must not be written by it).
+ *   x        device float[m][k], 16-byte aligned
+ *   x_q, x_s device outputs as in nvfp4_quantize_act (required)
+ *   others   as in nvfp4_gemm_smallm
+ */
+int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                 const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                 uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream);
 
 /*
  * Device status word of the library on the current device: the OR of the

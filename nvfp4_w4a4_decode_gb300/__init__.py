@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "Nvfp4Error", "library", "nvfp4_global_scale", "nvfp4_pack_weight",
     "nvfp4_quantize_act", "nvfp4_gemm_smallm", "global_scale", "pack_weight",
-    "quantize_act", "gemm_smallm", "linear", "MAX_M",
+    "quantize_act", "gemm_smallm", "nvfp4_linear", "linear", "MAX_M",
 ]
 
 MAX_M = 8
@@ -47,12 +47,15 @@ SIGNATURES = {
                              ctypes.c_int),
     "nvfp4_gemm_select": ([_i64, _i64, _i64, ctypes.c_uint32], ctypes.c_int),
     "nvfp4_device_status": ([_p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int], ctypes.c_int),
+    "nvfp4_linear": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p],
+                     ctypes.c_int),
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA = 0, 1, 2, 3, 4
 KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma",
                 KERNEL_TMA: "tma"}
 FLAG_PDL = 0x100
+FLAG_FUSED_QUANTIZE = 0x200
 FLAG_TEST_WAIT_TIMEOUT = 0x10000
 DEVICE_WAIT_TIMEOUT = 1
 
@@ -174,10 +177,35 @@ def nvfp4_device_status(clear: bool = True, stream=None) -> int:
     return int(v.value)
 
 
-def linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg) -> torch.Tensor:
-    """One W4A4 decode linear: quantise X on the fly, then the small-M GEMM."""
-    xq, xs = nvfp4_quantize_act(x, xg)
-    return nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg)
+def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=None,
+                 kernel: int = KERNEL_AUTO, pdl: bool = False,
+                 fused: bool = False) -> torch.Tensor:
+    """One W4A4 decode linear: quantise X[m, k] on the fly and multiply by the
+    packed W[n, k].  ``fused`` asks for one kernel (where the CUDA-core stream
+    takes the shape); ``x_out`` = (x_q, x_s) receive the quantised activations."""
+    _dev(x, torch.float32, "x")
+    for t, name in ((wq, "wq"), (ws, "ws")):
+        _dev(t, torch.uint8, name)
+    _dev(xg, torch.float32, "xg")
+    _dev(wg, torch.float32, "wg")
+    m, k = x.shape
+    n = wq.shape[0]
+    if wq.shape[1] * 2 != k or ws.shape != (n, k // 16):
+        raise ValueError("operand shapes disagree")
+    if x_out is None:
+        xq = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
+        xs = torch.empty((m, k // 16), dtype=torch.uint8, device=x.device)
+    else:
+        xq, xs = x_out
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
+    opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_FUSED_QUANTIZE if fused else 0)
+    _check("nvfp4_linear", library().nvfp4_linear(
+        x.data_ptr(), m, n, k, xg.data_ptr(), wq.data_ptr(), ws.data_ptr(), wg.data_ptr(),
+        y.data_ptr(), xq.data_ptr(), xs.data_ptr(), opts, _stream(x)))
+    return y
+
+
+linear = nvfp4_linear
 
 
 global_scale = nvfp4_global_scale

@@ -170,6 +170,45 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
     }
 }
 
+int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                 const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                 uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream)
+{
+    if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_FUSED_QUANTIZE)) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (m > 8)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0)
+        return NVFP4_OK;
+    const bool fuse = (options & NVFP4_FLAG_FUSED_QUANTIZE) != 0;
+    options &= ~(uint32_t)NVFP4_FLAG_FUSED_QUANTIZE;
+    if (k > 0 && (x == nullptr || x_q == nullptr || x_s == nullptr || !aligned(x, 16) ||
+                  !aligned(x_q, 8)))
+        return NVFP4_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
+    if (fuse && k > 0 && w_q != nullptr && w_s != nullptr && w_g != nullptr && x_g != nullptr &&
+        y != nullptr && aligned(y, 4) && aligned(x_g, 4) && aligned(w_g, 4)) {
+        const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
+                               aligned(w_s, 4);
+        const bool tma_ptrs = fast_ptrs && aligned(x_s, 32) && aligned(w_s, 32);
+        const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs);
+        if (kern < 0)
+            return -kern;
+        if (kern == (int)NVFP4_KERNEL_GEMV) {
+            const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k, s};
+            const nvfp4::FusedAct fa = {x, x_q, x_s};
+            return from_cuda(nvfp4::launch_gemm_gemv(a, pdl, &fa));
+        }
+    }
+    const int st = nvfp4_quantize_act_ex(x, m, k, x_g, x_q, x_s, pdl ? NVFP4_FLAG_PDL : 0u, stream);
+    if (st != NVFP4_OK)
+        return st;
+    return nvfp4_gemm_smallm_ex(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, stream);
+}
+
 int nvfp4_device_status(void* stream, uint32_t* flags, int clear)
 {
     if (flags == nullptr)

@@ -91,4 +91,83 @@ __device__ __forceinline__ uint2 ld_stream_u2(const void* p)
     return v;
 }
 
+// ---- the quantisation recipe, shared by every kernel that quantises ----------
+// (one implementation, so the stand-alone quantiser and the GEMM prologues
+// produce the same bytes)
+
+// Block scale: sc = E4M3 RNE (bmax / (6 g)) saturating, 0 when 6 g == 0;
+// returns sc and sets S = dec(sc) * g (FP32, each op correctly rounded).
+__device__ __forceinline__ uint32_t block_scale(float bmax, float g, float& S)
+{
+    const float six_g = __fmul_rn(6.0f, g);
+    uint32_t sc = 0;
+    if (six_g > 0.0f)
+        sc = e4m3_rne_satfinite(__fdiv_rn(bmax, six_g));
+    S = __fmul_rn(e4m3_to_float(sc), g);
+    return sc;
+}
+
+// E2M1 code of t in a block with scale S: RNE of t / S (IEEE division), or the
+// signed zero when S == 0.
+__device__ __forceinline__ uint32_t element_code(float t, float S)
+{
+    return (S == 0.0f) ? ((__float_as_uint(t) >> 28) & 8u) : e2m1_rne(__fdiv_rn(t, S));
+}
+
+// The 16 elements of a block share S, so the quotients t / S can use one
+// reciprocal: r = RN(1/S) (__frcp_rn), q0 = RN(t r), rem = t - S q0 (exact
+// with one FMA), q = RN(q0 + rem r).  This is Markstein's FMA correction (P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with a correctly rounded
+// reciprocal and no intermediate overflow or underflow, q equals the
+// correctly rounded quotient, so the codes equal those of element_code().
+// The guard keeps S and t inside that domain and falls back to the IEEE
+// division outside it; tests compare both forms at every code threshold.
+struct BlockDivisor {
+    float S, r;
+    bool fast;
+};
+
+__device__ __forceinline__ BlockDivisor make_divisor(float S)
+{
+    BlockDivisor d;
+    d.S = S;
+    d.r = __frcp_rn(S);
+    d.fast = S >= 0x1p-100f && S <= 0x1p+100f;
+    return d;
+}
+
+__device__ __forceinline__ uint32_t element_code_div(float t, const BlockDivisor& d)
+{
+    if (d.S == 0.0f)
+        return (__float_as_uint(t) >> 28) & 8u;
+    if (!d.fast || !(fabsf(t) <= 0x1p+100f))
+        return e2m1_rne(__fdiv_rn(t, d.S));
+    const float q0 = __fmul_rn(t, d.r);
+    const float rem = __fmaf_rn(-d.S, q0, t);
+    return e2m1_rne(__fmaf_rn(rem, d.r, q0));
+}
+
+// Quantise one 16-element block held by one thread: scale code returned,
+// codes packed two per byte (element 2j low nibble) into two words.
+__device__ __forceinline__ uint32_t quantize_block16(const float* v, float g, uint32_t& w0,
+                                                     uint32_t& w1)
+{
+    float bmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        bmax = fmaxf(bmax, fabsf(v[i]));
+    float S;
+    const uint32_t sc = block_scale(bmax, g, S);
+    const BlockDivisor d = make_divisor(S);
+    w0 = 0u;
+    w1 = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w0 |= element_code_div(v[i], d) << (4 * i);
+        w1 |= element_code_div(v[8 + i], d) << (4 * i);
+    }
+    return sc;
+}
+
 }  // namespace nvfp4

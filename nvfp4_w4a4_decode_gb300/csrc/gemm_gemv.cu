@@ -29,6 +29,11 @@
 //
 // With programmatic dependent launch the weight prefetch is issued before
 // waiting on the previous kernel; X and Y are touched only after the wait.
+//
+// Fused form (nvfp4_linear): the prologue quantises the FP32 activations
+// itself -- the CTA's threads share the 16-blocks, run the same recipe code as
+// the stand-alone quantiser (so the codes are the same bytes) into shared
+// memory, and read their chunks from there; CTA 0 also stores the codes.
 #include "formats.cuh"
 #include "kernels.cuh"
 
@@ -37,8 +42,11 @@ namespace nvfp4 {
 namespace {
 
 struct GemvParams {
-    const uint8_t* xq;
+    const uint8_t* xq;     // quantised activations (unfused) ...
     const uint8_t* xs;
+    const float* x;        // ... or FP32 activations, quantised in the prologue (fused)
+    uint8_t* xq_out;       // fused: where CTA 0 stores the activation codes
+    uint8_t* xs_out;       //        and block scales (both may be null)
     const float* xg;
     const uint8_t* wq;
     const uint8_t* ws;
@@ -76,11 +84,12 @@ __device__ __forceinline__ float rs_step(float a, float b, int bit, bool upper)
     return keep + __shfl_xor_sync(0xFFFFFFFFu, send, bit);
 }
 
-template <int M, int STAGES, int MAXT, bool PDL>
-__global__ void __launch_bounds__(MAXT) gemv_kernel(const GemvParams prm)
+template <int M, int STAGES, int MAXT, int MINB, bool PDL, bool FUSED>
+__global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
 {
     static_assert(STAGES == 8 || STAGES == 4, "reduce-scatter is written for 8 or 4 stages");
-    extern __shared__ float red[];  // [2][P][STAGES][M][G/32] warp sums
+    extern __shared__ __align__(16) float red[];  // [2][P][STAGES][M][G/32] warp sums,
+                                                  // then (fused) X codes and scales
     if constexpr (PDL)
         asm volatile("griddepcontrol.launch_dependents;");
 
@@ -119,17 +128,55 @@ __global__ void __launch_bounds__(MAXT) gemv_kernel(const GemvParams prm)
     // 2. activations, after the producer of X has finished
     if constexpr (PDL)
         asm volatile("griddepcontrol.wait;" ::: "memory");
+    // fused form: the CTA quantises X once, cooperatively (one 16-block per
+    // task, tasks spread over all threads), into shared memory after the
+    // reduction buffers; CTA 0 also stores the codes and scales
+    const int nb = (int)kb;
+    unsigned char* xcodes = reinterpret_cast<unsigned char*>(red + 2 * (size_t)P * STAGES * M * WPR);
+    unsigned char* xscales = xcodes + (size_t)M * kh;
+    if constexpr (FUSED) {
+        const float g = __ldg(prm.xg);
+        for (int u = t; u < M * nb; u += blockDim.x) {
+            const int m = u / nb, b = u - m * nb;
+            float e[16];
+            const float4* src = reinterpret_cast<const float4*>(prm.x + m * prm.k + 16 * b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 f = __ldg(src + i);
+                e[4 * i + 0] = f.x;
+                e[4 * i + 1] = f.y;
+                e[4 * i + 2] = f.z;
+                e[4 * i + 3] = f.w;
+            }
+            uint32_t c0, c1;
+            const uint32_t sc = quantize_block16(e, g, c0, c1);
+            *reinterpret_cast<uint2*>(xcodes + (size_t)m * kh + 8 * b) = make_uint2(c0, c1);
+            xscales[(size_t)m * nb + b] = (unsigned char)sc;
+            if (blockIdx.x == 0 && prm.xq_out != nullptr) {
+                *reinterpret_cast<uint2*>(prm.xq_out + m * kh + 8 * b) = make_uint2(c0, c1);
+                prm.xs_out[m * kb + b] = (uint8_t)sc;
+            }
+        }
+        __syncthreads();
+    }
     uint32_t xh[M][16];
     float sx[M][2];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(prm.xq + m * kh + 16 * c));
+        uint4 v;
+        uint32_t sc2;
+        if constexpr (FUSED) {
+            v = *reinterpret_cast<const uint4*>(xcodes + (size_t)m * kh + 16 * c);
+            sc2 = *reinterpret_cast<const unsigned short*>(xscales + (size_t)m * nb + 2 * c);
+        } else {
+            v = __ldg(reinterpret_cast<const uint4*>(prm.xq + m * kh + 16 * c));
+            sc2 = __ldg(reinterpret_cast<const unsigned short*>(prm.xs + m * kb + 2 * c));
+        }
         e2m1x8_to_f16(v.x, *reinterpret_cast<uint32_t(*)[4]>(&xh[m][0]));
         e2m1x8_to_f16(v.y, *reinterpret_cast<uint32_t(*)[4]>(&xh[m][4]));
         e2m1x8_to_f16(v.z, *reinterpret_cast<uint32_t(*)[4]>(&xh[m][8]));
         e2m1x8_to_f16(v.w, *reinterpret_cast<uint32_t(*)[4]>(&xh[m][12]));
-        const float2 f = e4m3x2_to_float2(
-            __ldg(reinterpret_cast<const unsigned short*>(prm.xs + m * kb + 2 * c)));
+        const float2 f = e4m3x2_to_float2(sc2);
         sx[m][0] = f.x;
         sx[m][1] = f.y;
     }
@@ -249,12 +296,21 @@ int sm_count_gemv()
     return sms;
 }
 
-template <int M, int STAGES, int MAXT, bool PDL>
-cudaError_t launch_typed(const GemmArgs& a, const Shape& sh)
+template <int M, int STAGES, int MAXT, int MINB, bool PDL, bool FUSED>
+cudaError_t launch_typed(const GemmArgs& a, const Shape& sh, const FusedAct* fa)
 {
     const int T = sh.G * sh.P;
-    const size_t smem = sizeof(float) * 2 * (size_t)sh.P * STAGES * M * (sh.G / 32);
-    auto kern = gemv_kernel<M, STAGES, MAXT, PDL>;
+    size_t smem = sizeof(float) * 2 * (size_t)sh.P * STAGES * M * (sh.G / 32);
+    smem = (smem + 15) / 16 * 16;
+    if (FUSED)
+        smem += (size_t)M * (a.k / 2 + a.k / 16);
+    auto kern = gemv_kernel<M, STAGES, MAXT, MINB, PDL, FUSED>;
+    if (smem > 48 * 1024) {
+        cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)smem);
+        if (e0 != cudaSuccess)
+            return e0;
+    }
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, smem);
     if (e != cudaSuccess)
@@ -268,7 +324,9 @@ cudaError_t launch_typed(const GemmArgs& a, const Shape& sh)
     if (grid > groups)
         grid = groups;
 
-    GemvParams prm = {a.xq, a.xs, a.xg, a.wq, a.ws, a.wg, a.y, a.n, a.k, sh.G, sh.P};
+    GemvParams prm = {a.xq, a.xs,
+                      fa ? fa->x : nullptr, fa ? fa->xq_out : nullptr, fa ? fa->xs_out : nullptr,
+                      a.xg, a.wq, a.ws, a.wg, a.y, a.n, a.k, sh.G, sh.P};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3((unsigned)T, 1, 1);
@@ -282,13 +340,20 @@ cudaError_t launch_typed(const GemmArgs& a, const Shape& sh)
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
-template <int M>
-cudaError_t launch_m(const GemmArgs& a, const Shape& sh, bool pdl)
+template <int M, bool FUSED>
+cudaError_t launch_m(const GemmArgs& a, const Shape& sh, bool pdl, const FusedAct* fa)
 {
-    // up to 512 threads: 8 stages in flight; larger CTAs: 4 (register budget)
-    if (sh.G * sh.P <= 512)
-        return pdl ? launch_typed<M, 8, 512, true>(a, sh) : launch_typed<M, 8, 512, false>(a, sh);
-    return pdl ? launch_typed<M, 4, 1024, true>(a, sh) : launch_typed<M, 4, 1024, false>(a, sh);
+    // up to 512 threads: 8 stages in flight (two 256-thread CTAs per SM);
+    // larger CTAs: 4 stages, one per SM (register budget)
+    const int T = sh.G * sh.P;
+    if (T <= 256)
+        return pdl ? launch_typed<M, 8, 256, 2, true, FUSED>(a, sh, fa)
+                   : launch_typed<M, 8, 256, 2, false, FUSED>(a, sh, fa);
+    if (T <= 512)
+        return pdl ? launch_typed<M, 8, 512, 1, true, FUSED>(a, sh, fa)
+                   : launch_typed<M, 8, 512, 1, false, FUSED>(a, sh, fa);
+    return pdl ? launch_typed<M, 4, 1024, 1, true, FUSED>(a, sh, fa)
+               : launch_typed<M, 4, 1024, 1, false, FUSED>(a, sh, fa);
 }
 
 }  // namespace
@@ -299,14 +364,21 @@ bool gemv_supported(int64_t m, int64_t k)
     return m >= 1 && m <= 2 && pick_shape(k, &sh);
 }
 
-cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl)
+cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl, const FusedAct* fa)
 {
     Shape sh;
     if (!pick_shape(a.k, &sh))
         return cudaErrorInvalidValue;
+    if (fa != nullptr) {
+        switch (a.m) {
+        case 1: return launch_m<1, true>(a, sh, pdl, fa);
+        case 2: return launch_m<2, true>(a, sh, pdl, fa);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (a.m) {
-    case 1: return launch_m<1>(a, sh, pdl);
-    case 2: return launch_m<2>(a, sh, pdl);
+    case 1: return launch_m<1, false>(a, sh, pdl, nullptr);
+    case 2: return launch_m<2, false>(a, sh, pdl, nullptr);
     default: return cudaErrorInvalidValue;
     }
 }

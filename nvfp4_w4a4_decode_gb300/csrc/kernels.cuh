@@ -29,10 +29,19 @@ cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float
 // Any shape with k % 16 == 0 and 8-byte aligned code rows.
 cudaError_t launch_gemm_generic(const GemmArgs& a);
 
+// FP32 activations for a GEMM that quantises them in its prologue, and where
+// the quantised codes and scales go (both may be null).
+struct FusedAct {
+    const float* x;
+    uint8_t* xq_out;
+    uint8_t* xs_out;
+};
+
 // Persistent CUDA-core weight-streaming kernel: m in {1, 2}, k a multiple of
-// 1024 up to 32768; x_q/w_q 16-byte and x_s/w_s 4-byte aligned.
+// 1024 up to 32768; x_q/w_q 16-byte and x_s/w_s 4-byte aligned.  With `fa`
+// the activations are quantised in the prologue (x 16-byte aligned).
 bool gemv_supported(int64_t m, int64_t k);
-cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl);
+cudaError_t launch_gemm_gemv(const GemmArgs& a, bool pdl, const FusedAct* fa = nullptr);
 
 // Tensor-core (mma.sync f16, swap-AB) kernel: m in 1..8, k a multiple of 256
 // that splits into at most 8 cluster ranks of 4..16 warps x 1, 2 or 4

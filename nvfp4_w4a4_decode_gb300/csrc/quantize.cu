@@ -72,21 +72,15 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
     bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
     bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 2));
 
-    const float g = __ldg(g_ptr);
-    const float six_g = __fmul_rn(6.0f, g);
-    uint32_t sc = 0;
-    if (six_g > 0.0f)
-        sc = e4m3_rne_satfinite(__fdiv_rn(bmax, six_g));
-    const float S = __fmul_rn(e4m3_to_float(sc), g);
+    float S;
+    const uint32_t sc = block_scale(bmax, __ldg(g_ptr), S);
 
     const float e[4] = {v.x, v.y, v.z, v.w};
+    const BlockDivisor d = make_divisor(S);
     uint32_t codes = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t c = (S == 0.0f) ? ((__float_as_uint(e[i]) >> 28) & 8u)
-                                       : e2m1_rne(__fdiv_rn(e[i], S));
-        codes |= c << (4 * i);
-    }
+    for (int i = 0; i < 4; ++i)
+        codes |= element_code_div(e[i], d) << (4 * i);
     // lanes sub = 0,1 own codes 0..7 of the block (one word), sub = 2,3 codes 8..15
     uint32_t mine = codes << (16 * (sub & 1));
     const uint32_t word = mine | __shfl_xor_sync(0xFFFFFFFFu, mine, 1);

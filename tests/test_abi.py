@@ -118,3 +118,14 @@ def test_ex_options_validated(lib):
     assert lib.nvfp4_gemm_smallm_ex(*ok, 1, 16, 32, 0x200, None) == 1     # unknown flag
     assert lib.nvfp4_gemm_smallm_ex(*ok, 3, 16, 4096, 2, None) == 2       # GEMV with M = 3
     assert lib.nvfp4_quantize_act_ex(FAKE, 1, 32, FAKE, FAKE, FAKE, 1, None) == 1
+
+
+def test_linear_rejects_bad_arguments(lib):
+    f = lib.nvfp4_linear
+    # x, m, n, k, x_g, w_q, w_s, w_g, y, x_q, x_s, options, stream
+    assert f(FAKE, 9, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 2
+    assert f(FAKE, 1, 16, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 1
+    assert f(FAKE + 4, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 1
+    assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, None) == 1
+    assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0x400, None) == 1
+    assert f(FAKE, 0, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 0

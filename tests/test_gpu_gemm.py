@@ -363,3 +363,69 @@ def test_tma_bounded_wait_times_out_and_recovers(nv):
     wq_o, ws_o, gw = oracle.pack_weight(w)
     assert gemm_error(y, oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)) <= GEMM_TOL
     assert nv.device_status() == 0
+
+
+# ---- fused quantise + GEMM (nvfp4_linear) --------------------------------------
+
+LINEAR_SHAPES = [(1, 256, 1024), (2, 1000, 4096), (1, 16 * 37 + 5, 4096), (2, 77, 12288),
+                 (1, 20, 25600), (1, 64, 8192), (4, 96, 4096), (8, 50, 4096), (3, 40, 512)]
+
+
+@pytest.mark.parametrize("m,n,k", LINEAR_SHAPES)
+@pytest.mark.parametrize("pdl", [False, True])
+@pytest.mark.parametrize("fused", [False, True])
+def test_linear_matches_two_step_and_oracle(nv, m, n, k, pdl, fused):
+    """The fused kernel writes the same activation bytes as the quantiser and
+    the same Y as quantise + GEMM; both within tolerance of the oracle."""
+    x = synthetic.activations(m, k, seed=3 * k + m)
+    w = synthetic.weights(n, k, 0.02, seed=5 * n + k)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq = torch.full((m, k // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    xs = torch.full((m, k // 16), 0xAB, dtype=torch.uint8, device="cuda")
+    y = nv.linear(xd, xg, wq, ws, wg, x_out=(xq, xs), pdl=pdl, fused=fused)
+    xq2, xs2 = nv.quantize_act(xd, xg)
+    y2 = nv.gemm_smallm(xq2, xs2, xg, wq, ws, wg)
+    np.testing.assert_array_equal(host(xq), host(xq2))
+    np.testing.assert_array_equal(host(xs), host(xs2))
+    np.testing.assert_array_equal(host(y), host(y2))
+    gx = oracle.global_scale(x)
+    oxq, oxs = oracle.quantize(x, gx)
+    owq, ows, ogw = oracle.pack_weight(w)
+    np.testing.assert_array_equal(host(xq), oxq)
+    assert gemm_error(host(y), oracle.gemm(oxq, oxs, gx, owq, ows, ogw)) <= GEMM_TOL
+
+
+def test_linear_pdl_graph_step(nv):
+    """A captured decode-style chain of fused linears equals eager launches."""
+    lin = synthetic.LINEARS_8B
+    ins, ws_, outs, bufs = [], [], [], []
+    for j, l in enumerate(lin):
+        x = dev(synthetic.activations(1, l.k, seed=70 + j))
+        ins.append((x, nv.global_scale(x)))
+        ws_.append(nv.pack_weight(dev(synthetic.weights(l.n, l.k, 0.02, seed=80 + j))))
+        outs.append(torch.empty((1, l.n), device="cuda"))
+        bufs.append((torch.empty((1, l.k // 2), dtype=torch.uint8, device="cuda"),
+                     torch.empty((1, l.k // 16), dtype=torch.uint8, device="cuda")))
+    eager = [host(nv.linear(ins[j][0], ins[j][1], *ws_[j])).copy() for j in range(4)]
+
+    def step():
+        for j in range(4):
+            nv.linear(ins[j][0], ins[j][1], *ws_[j], out=outs[j], x_out=bufs[j], pdl=True,
+                      fused=(j % 2 == 0))
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    for j in range(4):
+        np.testing.assert_array_equal(host(outs[j]), eager[j])

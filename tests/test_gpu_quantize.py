@@ -150,3 +150,38 @@ def test_pack_weight_empty(nv):
     w = torch.empty((0, 32), dtype=torch.float32, device="cuda")
     wq, ws, wg = nv.pack_weight(w)
     assert wq.shape == (0, 16) and host(wg)[0] == 0.0
+
+
+def test_quantize_codes_at_every_threshold_for_many_scales(nv):
+    """The quantisers divide by one reciprocal per block with an FMA
+    correction; elements placed on, and a few ulps around, every E2M1
+    decision threshold for many block scales give the oracle's codes (which
+    come from IEEE division)."""
+    rng = np.random.default_rng(42)
+    thresholds = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    rows = []
+    for _ in range(400):
+        S = np.float32(np.exp2(rng.uniform(-30, 30)))
+        g = np.float32(S / 448.0)          # block scale code saturates near 448
+        base = np.float32(6.0) * S         # block max: code 7, scale exact-ish
+        vals = [base]
+        for th in thresholds:
+            c = np.float32(th) * S
+            vals.append(c)
+            for k in (1, 2, 3):
+                vals.append(np.nextafter(c, np.float32(0), dtype=np.float32) if k == 1 else
+                            np.float32(c) * np.float32(1 - k * 2.0 ** -23))
+                vals.append(np.nextafter(c, np.float32(1e30), dtype=np.float32) if k == 1 else
+                            np.float32(c) * np.float32(1 + k * 2.0 ** -23))
+        vals = np.array(vals, np.float32)
+        vals = np.concatenate([vals, -vals])
+        pad = (-len(vals)) % 16
+        vals = np.concatenate([vals, np.zeros(pad, np.float32)])
+        blk = vals.reshape(-1, 16)
+        blk[:, 0] = base                    # every block keeps the same max
+        rows.append((blk.reshape(1, -1), g))
+    for x, g in rows:
+        oq, os_ = oracle.quantize(x, g)
+        xq, xs = nv.quantize_act(dev(x), dev(np.array([g], np.float32)))
+        np.testing.assert_array_equal(host(xs), os_)
+        np.testing.assert_array_equal(host(xq), oq)
