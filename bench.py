@@ -592,6 +592,45 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
             "seconds": round(sec, 2)}
 
 
+def run_single(args) -> None:
+    """One linear shape, repeated: the case the kernel-level ncu captures run.
+    Seeded N(0, 0.02^2) weights packed on the device, one seeded activation
+    batch quantised once, then the GEMM with the chosen kernel `reps` times and
+    20 more under CUDA events (printed: µs per call, GB/s)."""
+    import torch
+
+    import nvfp4_w4a4_decode_gb300 as nv
+    from nvfp4_w4a4_decode_gb300 import build as nvbuild
+    m, n, k = args.single
+    kernel = {"auto": nv.KERNEL_AUTO, "generic": nv.KERNEL_GENERIC, "gemv": nv.KERNEL_GEMV,
+              "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA}[args.kernel]
+    nvbuild.build()
+    nv.library()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    w = torch.randn((n, k), generator=gen, device="cuda") * synthetic.WEIGHT_STD_8B
+    wq, ws, wg = nv.pack_weight(w)
+    del w
+    x = torch.from_numpy(synthetic.activations(m, k, seed=1)).cuda()
+    xg = nv.global_scale(x)
+    xq, xs = nv.quantize_act(x, xg)
+    torch.cuda.synchronize()
+    for _ in range(args.reps):
+        y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=kernel)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(20):
+        y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=kernel)
+    b.record()
+    b.synchronize()
+    us = a.elapsed_time(b) * 1e3 / 20
+    byt = algorithmic_bytes(m, n, k)["gemm"]
+    print(json.dumps({"single": [m, n, k], "kernel": args.kernel, "us_per_call": round(us, 3),
+                      "GBps": round(byt / (us * 1e-6) / 1e9, 1), "y00": float(y[0, 0])}))
+
+
 def run_reference(args) -> dict | None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -642,11 +681,18 @@ def main():
                     help="skip the per-shape M sweep (8B M=1,2,4,8; 32B M=1,4)")
     ap.add_argument("--sweep-generic", action="store_true",
                     help="also time the shape-general kernel in the sweep")
+    ap.add_argument("--single", type=int, nargs=3, metavar=("M", "N", "K"),
+                    help="time one linear shape (for kernel-level profiling) and exit")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "generic", "gemv", "mma", "tma"])
+    ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--profile-step", action="store_true",
                     help="replay only the step graph (warmup + steps times) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.single:
+        run_single(args)
+        return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
