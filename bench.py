@@ -595,8 +595,9 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
 def run_single(args) -> None:
     """One linear shape, repeated: the case the kernel-level ncu captures run.
     Seeded N(0, 0.02^2) weights packed on the device, one seeded activation
-    batch quantised once, then the GEMM with the chosen kernel `reps` times and
-    20 more under CUDA events (printed: µs per call, GB/s)."""
+    batch quantised once, then the GEMM with the chosen kernel `reps` times, then
+    a CUDA graph of 20 calls timed with CUDA events (printed: µs per call, GB/s;
+    the same weights every call, so shapes below L2 read from L2)."""
     import torch
 
     import nvfp4_w4a4_decode_gb300 as nv
@@ -615,14 +616,22 @@ def run_single(args) -> None:
     xg = nv.global_scale(x)
     xq, xs = nv.quantize_act(x, xg)
     torch.cuda.synchronize()
+    y = torch.empty((m, n), device="cuda")
     for _ in range(args.reps):
-        y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=kernel)
+        nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(20):
+            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel)
+    g.replay()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(20):
-        y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=kernel)
+    g.replay()
     b.record()
     b.synchronize()
     us = a.elapsed_time(b) * 1e3 / 20

@@ -36,6 +36,7 @@
 // memory, and read their chunks from there; CTA 0 also stores the codes.
 #include "formats.cuh"
 #include "kernels.cuh"
+#include "launch_cache.cuh"
 
 namespace nvfp4 {
 
@@ -284,18 +285,6 @@ bool pick_shape(int64_t k, Shape* out)
     return true;
 }
 
-int sm_count_gemv()
-{
-    static thread_local int dev_cached = -1, sms = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev != dev_cached) {
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        dev_cached = dev;
-    }
-    return sms;
-}
-
 template <int M, int STAGES, int MAXT, int MINB, bool PDL, bool FUSED>
 cudaError_t launch_typed(const GemmArgs& a, const Shape& sh, const FusedAct* fa)
 {
@@ -305,14 +294,14 @@ cudaError_t launch_typed(const GemmArgs& a, const Shape& sh, const FusedAct* fa)
     if (FUSED)
         smem += (size_t)M * (a.k / 2 + a.k / 16);
     auto kern = gemv_kernel<M, STAGES, MAXT, MINB, PDL, FUSED>;
+    const int dev = current_device();
     if (smem > 48 * 1024) {
-        cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)smem);
+        cudaError_t e0 = ensure_smem_limit(kern, smem, dev);
         if (e0 != cudaSuccess)
             return e0;
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, smem);
+    cudaError_t e = cached_occupancy(kern, T, smem, 0, dev, &per_sm);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)
@@ -320,7 +309,7 @@ cudaError_t launch_typed(const GemmArgs& a, const Shape& sh, const FusedAct* fa)
     if (per_sm > 2)
         per_sm = 2;
     const int64_t groups = (a.n + sh.P - 1) / sh.P;
-    int64_t grid = (int64_t)sm_count_gemv() * per_sm;
+    int64_t grid = (int64_t)device_sm_count(dev) * per_sm;
     if (grid > groups)
         grid = groups;
 

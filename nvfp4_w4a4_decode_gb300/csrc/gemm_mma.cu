@@ -20,6 +20,8 @@
 // A tile is 16 weight rows.  CTAs of one thread-block cluster (one per
 // K-slice) walk the same tiles -- tile c, c + C, ... for cluster c -- two
 // tiles per step, and reduce through distributed shared memory in rank order.
+// Without a K split the warps reduce each tile without a CTA barrier: every
+// warp stores its partial, the last one to arrive sums them in warp order.
 // Per (tile, range) a lane loads rows g and g+8 (g = lane / 4), bytes
 // [16 t, 16 t + 16) of the range (t = lane % 4), plus the 2 matching scale
 // bytes; the next two items are in flight while one is decoded.  Registers
@@ -30,12 +32,15 @@
 
 #include "formats.cuh"
 #include "kernels.cuh"
+#include "launch_cache.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace nvfp4 {
 
 namespace {
+
+constexpr int kSlots = 4;  // tile slots of the barrier-free reduction (a multiple of 2)
 
 struct MmaParams {
     const uint8_t* xq;
@@ -139,6 +144,9 @@ __global__ void __launch_bounds__(512, 2) mma_kernel(const MmaParams prm)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ float part[2][2][128];  // this CTA's K-slice sums per tile pair (cluster exchange)
+    __shared__ unsigned s_count[kSlots];  // warps that have stored their partial of a tile slot
+    if (threadIdx.x < kSlots)
+        s_count[threadIdx.x] = 0u;
 
     if constexpr (PDL)
         asm volatile("griddepcontrol.launch_dependents;");
@@ -218,6 +226,57 @@ __global__ void __launch_bounds__(512, 2) mma_kernel(const MmaParams prm)
 
     const bool has_b = g < M;
     const int bstride = 4 * M;
+    if (nsplit == 1) {
+        // Whole K in this CTA: no CTA-wide barrier per tile.  Each warp stores
+        // its partial tile in one of kSlots slots and counts itself in; the
+        // last warp to arrive adds the NW partials in warp order and writes Y.
+        // Slots are reused only after the barrier every kSlots tiles, so no
+        // warp can overwrite a slot that is still being summed.
+        for (int base = 0; base < niters; base += 2) {
+#pragma unroll
+            for (int tp = 0; tp < 2; ++tp) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const int e = (base + tp) * R + i;
+                    const int slot = (tp * R + i) & 1;
+                    Item cur = ring[slot];
+                    issue(ring[slot], e + 2);
+                    const uint4* bsrc = xfrag + (size_t)(warp + NW * i) * 4 * bstride + lane;
+                    mma_item(acc, cur, bsrc, bstride, has_b);
+                }
+                const int it = base + tp;
+                const int ts = it % kSlots;
+                reinterpret_cast<float4*>(red + ((size_t)ts * NW + warp) * 128)[lane] =
+                    make_float4(acc[0], acc[1], acc[2], acc[3]);
+                __threadfence_block();
+                unsigned arrived = 0;
+                if (lane == 0)
+                    arrived = atomicAdd(&s_count[ts], 1u);
+                arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+                if (arrived == (unsigned)NW - 1) {
+                    __threadfence_block();
+                    for (int v = lane; v < 128; v += 32) {
+                        const int lv = v >> 2, j = v & 3;
+                        const int row = (lv >> 2) + 8 * (j >> 1), col = 2 * (lv & 3) + (j & 1);
+                        const int r = rowA0 - g + it * tile_rows + row;
+                        if (col >= M || it >= niters || r >= nrows)
+                            continue;
+                        const float* src = red + (size_t)ts * NW * 128 + v;
+                        float sum = 0.0f;
+                        for (int w = 0; w < NW; ++w)
+                            sum += src[(size_t)w * 128];
+                        prm.y[(int64_t)col * n + r] = sum * gxw;
+                    }
+                    if (lane == 0)
+                        s_count[ts] = 0u;
+                }
+            }
+            if ((base + 2) % kSlots == 0)
+                __syncthreads();
+        }
+        return;
+    }
     int buf = 0;
     for (int base = 0; base < niters; base += 2) {
 #pragma unroll
@@ -312,56 +371,29 @@ bool plan_mma(int64_t m, int64_t k, MmaPlan* out)
     return false;
 }
 
-struct DevSms {
-    int dev = -1, sms = 0;
-};
-
-int sm_count()
-{
-    static thread_local DevSms c;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev != c.dev) {
-        cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
-        c.dev = dev;
-    }
-    return c.sms;
-}
-
 template <int R, bool PDL>
 cudaError_t launch_plan(const GemmArgs& a, const MmaPlan& p)
 {
     const int threads = 32 * p.NW;
     const int ks = (int)(a.k / p.nsplit);
-    const size_t smem = (size_t)(ks / 128) * 4 * 4 * a.m * 16 + sizeof(float) * 2 * 2 * p.NW * 128;
+    const size_t smem = (size_t)(ks / 128) * 4 * 4 * a.m * 16 + sizeof(float) * kSlots * p.NW * 128;
     auto kern = mma_kernel<R, PDL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const int dev = current_device();
+    cudaError_t e = ensure_smem_limit(kern, smem, dev);
     if (e != cudaSuccess)
         return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    e = cached_occupancy(kern, threads, smem, 0, dev, &per_sm);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
     const int64_t ntiles = (a.n + 15) / 16;
-    int64_t clusters = ((int64_t)sm_count() * per_sm) / p.nsplit;
+    int64_t clusters = ((int64_t)device_sm_count(dev) * per_sm) / p.nsplit;
     if (p.nsplit > 1) {
-        cudaLaunchConfig_t q = {};
-        q.gridDim = dim3((unsigned)p.nsplit, 1, 1);
-        q.blockDim = dim3((unsigned)threads, 1, 1);
-        q.dynamicSmemBytes = smem;
-        cudaLaunchAttribute ca;
-        ca.id = cudaLaunchAttributeClusterDimension;
-        ca.val.clusterDim.x = (unsigned)p.nsplit;
-        ca.val.clusterDim.y = 1;
-        ca.val.clusterDim.z = 1;
-        q.attrs = &ca;
-        q.numAttrs = 1;
         int maxc = 0;
-        if (cudaOccupancyMaxActiveClusters(&maxc, kern, &q) == cudaSuccess && maxc > 0 &&
-            maxc < clusters)
+        if (cached_occupancy(kern, threads, smem, p.nsplit, dev, &maxc) == cudaSuccess &&
+            maxc > 0 && maxc < clusters)
             clusters = maxc;
     }
     if (clusters > ntiles)

@@ -30,6 +30,7 @@
 #include "../../include/nvfp4.h"
 #include "formats.cuh"
 #include "kernels.cuh"
+#include "launch_cache.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -396,35 +397,18 @@ bool plan_tma(int64_t m, int64_t k, TmaPlan* out)
     return false;
 }
 
-int sm_count_tma()
-{
-    static thread_local int dev_cached = -1, sms = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev != dev_cached) {
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        dev_cached = dev;
-    }
-    return sms;
-}
-
 template <int R, bool PDL>
 cudaError_t launch_tma_t(const GemmArgs& a, const TmaPlan& p, long long budget, int skew)
 {
     const int threads = 32 * (p.NC + 1);
     const Layout L = make_layout(p.ks, a.m, p.NC, p.S, p.nsplit == 1);
     auto kern = tma_kernel<R, PDL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L.total);
+    const int dev = current_device();
+    cudaError_t e = ensure_smem_limit(kern, L.total, dev);
     if (e != cudaSuccess)
         return e;
-    if (p.nsplit > 1) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess)
-            return e;
-    }
     const int ntiles = (int)((a.n + 15) / 16);
-    int clusters = sm_count_tma() / p.nsplit;
+    int clusters = device_sm_count(dev) / p.nsplit;
     cudaLaunchAttribute attr[2];
     int na = 0;
     if (p.nsplit > 1) {
@@ -433,15 +417,9 @@ cudaError_t launch_tma_t(const GemmArgs& a, const TmaPlan& p, long long budget, 
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
-        cudaLaunchConfig_t q = {};
-        q.gridDim = dim3((unsigned)p.nsplit, 1, 1);
-        q.blockDim = dim3((unsigned)threads, 1, 1);
-        q.dynamicSmemBytes = L.total;
-        q.attrs = attr;
-        q.numAttrs = 1;
         int maxc = 0;
-        if (cudaOccupancyMaxActiveClusters(&maxc, kern, &q) == cudaSuccess && maxc > 0 &&
-            maxc < clusters)
+        if (cached_occupancy(kern, threads, L.total, p.nsplit, dev, &maxc) == cudaSuccess &&
+            maxc > 0 && maxc < clusters)
             clusters = maxc;
     }
     if (clusters > ntiles)
