@@ -162,6 +162,17 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 /* Bits of the device status word (nvfp4_device_status). */
 #define NVFP4_DEVICE_WAIT_TIMEOUT 1u
 
+/*
+ * Activation quantisation with a dynamic tensor scale (the other reading of
+ * "quantised on the fly": the scale comes from this X, not from calibration):
+ * *x_g = amax(|X|) / 2688 is computed and written first (as
+ * nvfp4_global_scale), then X is quantised with it (as nvfp4_quantize_act).
+ *   x_g   device float[1], OUTPUT here
+ * Launches a memset and three kernels.
+ */
+int nvfp4_quantize_act_dynamic(const float* x, int64_t m, int64_t k, float* x_g,
+                               uint8_t* x_q, uint8_t* x_s, void* stream);
+
 /* nvfp4_quantize_act with options (only NVFP4_FLAG_PDL is meaningful). */
 int nvfp4_quantize_act_ex(const float* x, int64_t m, int64_t k, const float* x_g,
                           uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream);

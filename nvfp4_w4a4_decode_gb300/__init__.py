@@ -49,6 +49,7 @@ SIGNATURES = {
     "nvfp4_device_status": ([_p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int], ctypes.c_int),
     "nvfp4_linear": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p],
                      ctypes.c_int),
+    "nvfp4_quantize_act_dynamic": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA = 0, 1, 2, 3, 4
@@ -139,6 +140,22 @@ def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None, pdl: bool = 
     return xq, xs
 
 
+def nvfp4_quantize_act_dynamic(x: torch.Tensor, out=None):
+    """Quantise X[m, k] with its own tensor scale amax(|X|)/2688 ->
+    (x_q [m, k/2], x_s [m, k/16], x_g [1])."""
+    _dev(x, torch.float32, "x")
+    m, k = x.shape
+    if out is None:
+        xq = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
+        xs = torch.empty((m, k // 16), dtype=torch.uint8, device=x.device)
+        xg = torch.empty(1, dtype=torch.float32, device=x.device)
+    else:
+        xq, xs, xg = out
+    _check("nvfp4_quantize_act_dynamic", library().nvfp4_quantize_act_dynamic(
+        x.data_ptr(), m, k, xg.data_ptr(), xq.data_ptr(), xs.data_ptr(), _stream(x)))
+    return xq, xs, xg
+
+
 def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
                       kernel: int = KERNEL_AUTO, pdl: bool = False,
                       test_wait_timeout: bool = False) -> torch.Tensor:
@@ -211,6 +228,7 @@ linear = nvfp4_linear
 global_scale = nvfp4_global_scale
 pack_weight = nvfp4_pack_weight
 quantize_act = nvfp4_quantize_act
+quantize_act_dynamic = nvfp4_quantize_act_dynamic
 gemm_smallm = nvfp4_gemm_smallm
 gemm_select = nvfp4_gemm_select
 device_status = nvfp4_device_status

@@ -85,6 +85,20 @@ int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g, u
     return nvfp4_quantize_act_ex(x, m, k, x_g, x_q, x_s, 0u, stream);
 }
 
+int nvfp4_quantize_act_dynamic(const float* x, int64_t m, int64_t k, float* x_g, uint8_t* x_q,
+                               uint8_t* x_s, void* stream)
+{
+    if (m < 0 || k < 0 || (k % 16) != 0 || x_g == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    if (m > 0 && k > 0 && (x == nullptr || x_q == nullptr || x_s == nullptr ||
+                           !aligned(x, 16) || !aligned(x_q, 8) || !aligned(x_g, 4)))
+        return NVFP4_ERR_INVALID_ARG;
+    const int st = nvfp4_global_scale(x, m * k, x_g, stream);
+    if (st != NVFP4_OK)
+        return st;
+    return nvfp4_quantize_act_ex(x, m, k, x_g, x_q, x_s, 0u, stream);
+}
+
 namespace {
 
 // Kernel for a GEMM of this shape and operand alignment (negative status on

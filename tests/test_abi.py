@@ -129,3 +129,10 @@ def test_linear_rejects_bad_arguments(lib):
     assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, None) == 1
     assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0x400, None) == 1
     assert f(FAKE, 0, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 0
+
+
+def test_dynamic_quantize_rejects_bad_arguments(lib):
+    q = lib.nvfp4_quantize_act_dynamic
+    assert q(FAKE, 1, 20, FAKE, FAKE, FAKE, None) == 1       # K not a multiple of 16
+    assert q(FAKE, 1, 32, None, FAKE, FAKE, None) == 1       # no x_g output
+    assert q(FAKE + 4, 1, 32, FAKE, FAKE, FAKE, None) == 1   # X misaligned

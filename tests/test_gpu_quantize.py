@@ -185,3 +185,15 @@ def test_quantize_codes_at_every_threshold_for_many_scales(nv):
         xq, xs = nv.quantize_act(dev(x), dev(np.array([g], np.float32)))
         np.testing.assert_array_equal(host(xs), os_)
         np.testing.assert_array_equal(host(xq), oq)
+
+
+@pytest.mark.parametrize("m,k", [(1, 4096), (3, 12288), (8, 512), (2, 48)])
+def test_quantize_dynamic_scale_bit_exact(nv, m, k):
+    """Dynamic tensor scale: x_g = amax/2688 from this X, then the codes."""
+    x = synthetic.activations(m, k, seed=900 + m + k)
+    gx = oracle.global_scale(x)
+    oq, os_ = oracle.quantize(x, gx)
+    xq, xs, xg = nv.quantize_act_dynamic(dev(x))
+    assert np.float32(host(xg)[0]) == gx
+    np.testing.assert_array_equal(host(xq), oq)
+    np.testing.assert_array_equal(host(xs), os_)
