@@ -175,13 +175,17 @@ class DecodeStack:
     activation buffers, and the graphs that replay them."""
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
-                 fused: bool = True):
+                 fused: bool = True, kernel: int = 0):
         self.nv, self.torch = nv, torch
         self.m = m
         self.pdl = pdl
         self.fused = fused
+        self.kernel = kernel
         self.layers = layers
         self.lins = synthetic.LINEARS_8B
+        # one workspace for every call of the step (calls run one after another)
+        wsz = max(nv.gemm_workspace_size(m, lin.n, lin.k, kernel) for lin in self.lins)
+        self.workspace = (torch.zeros(wsz, dtype=torch.uint8, device="cuda") if wsz else None)
         dev = torch.device("cuda")
         gen = torch.Generator(device=dev)
         self.w = []          # [layer][j] -> (wq, ws, wg)
@@ -222,13 +226,19 @@ class DecodeStack:
                     torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev)) for lin in self.lins]
         torch.cuda.synchronize()
 
+    def chosen(self, lin) -> int:
+        """Kernel id the step's calls of this linear run."""
+        wsz = self.workspace.numel() if self.workspace is not None else 0
+        return self.nv.gemm_select(self.m, lin.n, lin.k, self.kernel, wsz)
+
     def step(self):
         nv = self.nv
         for l in range(self.layers):
             for j in range(4):
                 wq, ws, wg = self.w[l][j]
                 nv.linear(self.x[l][j], self.xg[l][j], wq, ws, wg, out=self.y[l][j],
-                          x_out=self.xq[j], pdl=self.pdl, fused=self.fused)
+                          x_out=self.xq[j], kernel=self.kernel, pdl=self.pdl, fused=self.fused,
+                          workspace=self.workspace)
 
     def quantize_all(self):
         """Fill the per-shape activation buffers (before GEMM-only timing)."""
@@ -242,7 +252,7 @@ class DecodeStack:
                 xq, xs = self.xq[jj]
                 wq, ws, wg = self.w[l][jj]
                 nv.gemm_smallm(xq, xs, self.xg[l][jj], wq, ws, wg, out=self.y[l][jj],
-                               pdl=self.pdl)
+                               kernel=self.kernel, pdl=self.pdl, workspace=self.workspace)
 
     def capture(self, fn):
         torch = self.torch
@@ -303,10 +313,11 @@ def time_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
     xg = nv.global_scale(xd)
     xq, xs = nv.quantize_act(xd, xg)
     y = torch.empty((m, lin.n), device="cuda")
+    wsp = nv.workspace(m, lin.n, lin.k, kernel)
 
     def calls():
         for wq, ws, wg in weights:
-            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel, pdl=pdl)
+            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel, pdl=pdl, workspace=wsp)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -322,23 +333,35 @@ def time_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
     return {"us_per_call": round(us, 3), "GBps": round(b / (us * 1e-6) / 1e9, 1)}
 
 
+def takes(nv, m, lin, kid) -> bool:
+    """Whether kernel `kid` runs this shape when given the workspace it asks for."""
+    wsz = nv.library().nvfp4_gemm_workspace_size(m, lin.n, lin.k, kid)
+    return wsz >= 0 and nv.gemm_select(m, lin.n, lin.k, kid, wsz) == kid
+
+
+def auto_choice(nv, m, lin) -> int:
+    """The library's kernel for this shape, offered the workspace it asks for."""
+    return nv.gemm_select(m, lin.n, lin.k, nv.KERNEL_AUTO,
+                          nv.gemm_workspace_size(m, lin.n, lin.k))
+
+
 def sweep(nv, torch, stack, peaks, args) -> dict:
     """µs/call and GB/s of every linear shape for every M of the sweep, with
     the library's kernel choice and with each kernel that takes the shape."""
     kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA,
-               "generic": nv.KERNEL_GENERIC}
+               "splitk": nv.KERNEL_SPLITK, "generic": nv.KERNEL_GENERIC}
     out = {"8B": {}, "32B": {}}
     reps = 5
     w8 = {j: [stack.w[l][j] for l in range(stack.layers)] for j in range(4)}
     for m in synthetic.M_SWEEP_8B:
         row = {}
         for j, lin in enumerate(synthetic.LINEARS_8B):
-            auto = nv.gemm_select(m, lin.n, lin.k)
+            auto = auto_choice(nv, m, lin)
             ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
             for name, kid in kernels.items():
                 if name == "generic" and not args.sweep_generic:
                     continue
-                if nv.gemm_select(m, lin.n, lin.k, kid) != kid:
+                if not takes(nv, m, lin, kid):
                     continue
                 ent[name] = time_linear(nv, torch, w8[j], lin, m, kid, stack.pdl, reps)
             ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
@@ -349,12 +372,12 @@ def sweep(nv, torch, stack, peaks, args) -> dict:
         copies = max(3, -(-400_000_000 // per_copy))
         ws = make_weights(nv, torch, lin, synthetic.WEIGHT_STD_32B, copies, seed=4000 + 100 * j)
         for m in synthetic.M_SWEEP_32B:
-            auto = nv.gemm_select(m, lin.n, lin.k)
+            auto = auto_choice(nv, m, lin)
             ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
             for name, kid in kernels.items():
                 if name == "generic" and not args.sweep_generic:
                     continue
-                if nv.gemm_select(m, lin.n, lin.k, kid) != kid:
+                if not takes(nv, m, lin, kid):
                     continue
                 ent[name] = time_linear(nv, torch, ws, lin, m, kid, stack.pdl, reps)
             ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
@@ -379,7 +402,7 @@ def run_ours(args) -> dict:
     peaks = load_peaks()
 
     stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
-                        fused=args.fused)
+                        fused=args.fused, kernel=KERNELS[args.kernel](nv))
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -387,8 +410,7 @@ def run_ours(args) -> dict:
             step_graph.replay()
         torch.cuda.synchronize()
         return None
-    launches_per_step = sum(1 if (stack.fused and nv.gemm_select(args.m, lin.n, lin.k)
-                                  == nv.KERNEL_GEMV) else 2
+    launches_per_step = sum(1 if (stack.fused and stack.chosen(lin) == nv.KERNEL_GEMV) else 2
                             for lin in stack.lins) * stack.layers
     bytes_step = stack.bytes_per_step()
     alg_step = bytes_step["gemm"] + bytes_step["quant"]
@@ -433,7 +455,7 @@ def run_ours(args) -> dict:
         b = algorithmic_bytes(args.m, lin.n, lin.k)["gemm"]
         gbs = b / (us * 1e-6) / 1e9
         per_linear[lin.name] = {"n": lin.n, "k": lin.k, "us_per_call": round(us, 3),
-                                "kernel": nv.KERNEL_NAMES.get(nv.gemm_select(args.m, lin.n, lin.k)),
+                                "kernel": nv.KERNEL_NAMES.get(stack.chosen(lin)),
                                 "GBps": round(gbs, 1),
                                 "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
         del g
@@ -592,6 +614,11 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
             "seconds": round(sec, 2)}
 
 
+KERNELS = {"auto": lambda nv: nv.KERNEL_AUTO, "generic": lambda nv: nv.KERNEL_GENERIC,
+           "gemv": lambda nv: nv.KERNEL_GEMV, "mma": lambda nv: nv.KERNEL_MMA,
+           "tma": lambda nv: nv.KERNEL_TMA, "splitk": lambda nv: nv.KERNEL_SPLITK}
+
+
 def run_single(args) -> None:
     """One linear shape, repeated: the case the kernel-level ncu captures run.
     Seeded N(0, 0.02^2) weights packed on the device, one seeded activation
@@ -603,8 +630,7 @@ def run_single(args) -> None:
     import nvfp4_w4a4_decode_gb300 as nv
     from nvfp4_w4a4_decode_gb300 import build as nvbuild
     m, n, k = args.single
-    kernel = {"auto": nv.KERNEL_AUTO, "generic": nv.KERNEL_GENERIC, "gemv": nv.KERNEL_GEMV,
-              "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA}[args.kernel]
+    kernel = KERNELS[args.kernel](nv)
     nvbuild.build()
     nv.library()
     gen = torch.Generator(device="cuda")
@@ -617,15 +643,16 @@ def run_single(args) -> None:
     xq, xs = nv.quantize_act(x, xg)
     torch.cuda.synchronize()
     y = torch.empty((m, n), device="cuda")
+    wsp = nv.workspace(m, n, k, kernel)
     for _ in range(args.reps):
-        nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel)
+        nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel, workspace=wsp)
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for _ in range(20):
-            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel)
+            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, kernel=kernel, workspace=wsp)
     g.replay()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
@@ -692,7 +719,8 @@ def main():
                     help="also time the shape-general kernel in the sweep")
     ap.add_argument("--single", type=int, nargs=3, metavar=("M", "N", "K"),
                     help="time one linear shape (for kernel-level profiling) and exit")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "generic", "gemv", "mma", "tma"])
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNELS),
+                    help="GEMM kernel for the decode step (and for --single)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--profile-step", action="store_true",
                     help="replay only the step graph (warmup + steps times) and exit")

@@ -32,7 +32,9 @@
  *   - Every pointer is DEVICE memory of the current CUDA device.  Nothing is
  *     allocated, freed or synchronised; work is queued on `stream` (a
  *     cudaStream_t; NULL = the legacy default stream) and the call returns
- *     once it is queued.  No state is kept between calls.
+ *     once it is queued.  The library keeps no state between calls; the only
+ *     state that outlives a call is in a caller-owned workspace (the _ws
+ *     entry points), whose counters every completed call leaves at zero.
  *   - Argument checks run on the host before anything is launched; a failed
  *     check returns NVFP4_ERR_INVALID_ARG or NVFP4_ERR_UNSUPPORTED and
  *     launches nothing.  A launch failure returns NVFP4_ERR_CUDA.
@@ -44,6 +46,7 @@
 #ifndef NVFP4_GB300_H
 #define NVFP4_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -133,7 +136,16 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       (cp.async.bulk + mbarrier ring in shared memory):
  *                       M <= 8, K a multiple of 256 (per cluster rank), N
  *                       below 2^30.
- *   The GEMV and MMA kernels need x_q/w_q 32-byte and x_s/w_s 4-byte
+ * NVFP4_KERNEL_SPLITK  the split-K tensor-core kernel (mma.sync f16, swap-AB,
+ *                       FP32 accumulation) in which every warp streams its own
+ *                       (16 rows x K-chunk) work items with no CTA barrier:
+ *                       M <= 8, K a multiple of 256.  K is cut into chunks of
+ *                       at most 4096 elements; when there is more than one,
+ *                       the partial tiles are combined in a workspace (the
+ *                       _ws entry points), so without one it takes only
+ *                       K <= 4096.  The last partial of a tile to arrive sums
+ *                       them in chunk order: results do not depend on timing.
+ *   The GEMV, MMA and SPLITK kernels need x_q/w_q 32-byte and x_s/w_s 4-byte
  *   aligned, the TMA kernel all four 32-byte aligned; a request a kernel
  *   cannot take returns NVFP4_ERR_UNSUPPORTED.
  * NVFP4_FLAG_TEST_WAIT_TIMEOUT  test hook of the TMA kernel: the first stage
@@ -154,6 +166,7 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_KERNEL_GEMV 2u
 #define NVFP4_KERNEL_MMA 3u
 #define NVFP4_KERNEL_TMA 4u
+#define NVFP4_KERNEL_SPLITK 5u
 #define NVFP4_KERNEL_MASK 0xFFu
 #define NVFP4_FLAG_PDL 0x100u
 #define NVFP4_FLAG_FUSED_QUANTIZE 0x200u
@@ -192,6 +205,36 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
  */
 int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options);
 
+/* nvfp4_gemm_select for a call that offers `workspace_bytes` of workspace
+ * (the _ws entry points). */
+int nvfp4_gemm_select_ws(int64_t m, int64_t n, int64_t k, uint32_t options,
+                         size_t workspace_bytes);
+
+/*
+ * Workspace of the _ws entry points: the bytes that the GEMM of shape
+ * (m, n, k) under `options` uses on the current device when offered as much
+ * as it wants (0 when it needs none), or minus a status code for an invalid
+ * shape or request.  Host only.
+ *
+ * The workspace is caller-owned device memory, 16-byte aligned, that must be
+ * ZERO before its first use: its first part holds per-tile arrival counters
+ * (the rest partial sums).  Every call that completes leaves the counters at
+ * zero again, so zeroing once at allocation is enough, and one workspace can
+ * serve calls of any shapes as long as it is always passed with the same
+ * size (the counter region's extent depends on the size only).  Calls that
+ * can run at the same time (on other streams) must use separate workspaces:
+ * two overlapping calls on one workspace race.  A smaller workspace than this
+ * size restricts the kernel's plan to one that fits (NVFP4_ERR_UNSUPPORTED
+ * when none does; 0 bytes: plans that need none).
+ */
+int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t options);
+
+/* nvfp4_gemm_smallm_ex with a workspace (NULL with 0 bytes for none). */
+int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
+                         float* y, int64_t m, int64_t n, int64_t k, uint32_t options,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * One W4A4 decode linear: quantise X[m][k] with the static tensor scale *x_g
  * (exactly as nvfp4_quantize_act: the codes and scales are written to x_q and
@@ -212,6 +255,12 @@ int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options);
 int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
                  const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
                  uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream);
+
+/* nvfp4_linear with a workspace for the GEMM (as nvfp4_gemm_smallm_ws). */
+int nvfp4_linear_ws(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                    const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                    uint8_t* x_q, uint8_t* x_s, uint32_t options, void* workspace,
+                    size_t workspace_bytes, void* stream);
 
 /*
  * Device status word of the library on the current device: the OR of the

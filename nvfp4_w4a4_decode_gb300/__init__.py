@@ -24,6 +24,7 @@ __all__ = [
     "Nvfp4Error", "library", "nvfp4_global_scale", "nvfp4_pack_weight",
     "nvfp4_quantize_act", "nvfp4_gemm_smallm", "global_scale", "pack_weight",
     "quantize_act", "gemm_smallm", "nvfp4_linear", "linear", "MAX_M",
+    "nvfp4_gemm_workspace_size", "nvfp4_workspace", "gemm_workspace_size", "workspace",
 ]
 
 MAX_M = 8
@@ -50,11 +51,17 @@ SIGNATURES = {
     "nvfp4_linear": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p],
                      ctypes.c_int),
     "nvfp4_quantize_act_dynamic": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
+    "nvfp4_gemm_workspace_size": ([_i64, _i64, _i64, ctypes.c_uint32], _i64),
+    "nvfp4_gemm_select_ws": ([_i64, _i64, _i64, ctypes.c_uint32, ctypes.c_size_t], ctypes.c_int),
+    "nvfp4_gemm_smallm_ws": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_uint32, _p,
+                              ctypes.c_size_t, _p], ctypes.c_int),
+    "nvfp4_linear_ws": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p,
+                         ctypes.c_size_t, _p], ctypes.c_int),
 }
 
-KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA, KERNEL_SPLITK = 0, 1, 2, 3, 4, 5
 KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma",
-                KERNEL_TMA: "tma"}
+                KERNEL_TMA: "tma", KERNEL_SPLITK: "splitk"}
 FLAG_PDL = 0x100
 FLAG_FUSED_QUANTIZE = 0x200
 FLAG_TEST_WAIT_TIMEOUT = 0x10000
@@ -156,14 +163,47 @@ def nvfp4_quantize_act_dynamic(x: torch.Tensor, out=None):
     return xq, xs, xg
 
 
+def nvfp4_gemm_workspace_size(m: int, n: int, k: int, kernel: int = KERNEL_AUTO) -> int:
+    """Bytes of workspace the GEMM of this shape uses (0: none)."""
+    v = int(library().nvfp4_gemm_workspace_size(m, n, k, int(kernel) & 0xFF))
+    if v < 0:
+        raise Nvfp4Error("nvfp4_gemm_workspace_size", -v)
+    return v
+
+
+def nvfp4_workspace(m: int, n: int, k: int, kernel: int = KERNEL_AUTO,
+                    device=None) -> torch.Tensor | None:
+    """A zeroed workspace for GEMMs of this shape (None when none is needed).
+    It can be reused by any number of calls that do not overlap in time."""
+    size = nvfp4_gemm_workspace_size(m, n, k, kernel)
+    if size == 0:
+        return None
+    return torch.zeros(size, dtype=torch.uint8,
+                       device=device if device is not None else torch.cuda.current_device())
+
+
+def _ws_args(workspace, m, n, k, kernel, device):
+    """(pointer, bytes, keep-alive) of the workspace for one call; a zeroed
+    one is made for this call when none is given and the GEMM wants one."""
+    if workspace is None:
+        workspace = nvfp4_workspace(m, n, k, kernel, device) if m and n and k else None
+    if workspace is None:
+        return None, 0, None
+    _dev(workspace, torch.uint8, "workspace")
+    return workspace.data_ptr(), workspace.numel(), workspace
+
+
 def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
                       kernel: int = KERNEL_AUTO, pdl: bool = False,
-                      test_wait_timeout: bool = False) -> torch.Tensor:
+                      test_wait_timeout: bool = False,
+                      workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32.
 
-    ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA); ``pdl`` lets
-    the launch overlap the previous kernel (weights must not be written by
-    it)."""
+    ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA,
+    KERNEL_TMA, KERNEL_SPLITK); ``pdl`` lets the launch overlap the previous
+    kernel (weights must not be written by it); ``workspace`` (from
+    ``nvfp4_workspace``) is made per call when the kernel needs one and none
+    is given."""
     for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
         _dev(t, torch.uint8, name)
     _dev(xg, torch.float32, "xg")
@@ -175,15 +215,18 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
         raise ValueError("operand shapes disagree")
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
     opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0)
-    _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm_ex(
+    wp, wn, _keep = _ws_args(workspace, m, n, k, kernel, xq.device)
+    _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm_ws(
         xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
-        wg.data_ptr(), y.data_ptr(), m, n, k, opts, _stream(xq)))
+        wg.data_ptr(), y.data_ptr(), m, n, k, opts, wp, wn, _stream(xq)))
     return y
 
 
-def nvfp4_gemm_select(m: int, n: int, k: int, kernel: int = KERNEL_AUTO) -> int:
-    """Kernel id the library runs for this shape (negative status if none)."""
-    return library().nvfp4_gemm_select(m, n, k, kernel)
+def nvfp4_gemm_select(m: int, n: int, k: int, kernel: int = KERNEL_AUTO,
+                      workspace_bytes: int = 0) -> int:
+    """Kernel id the library runs for this shape when offered
+    ``workspace_bytes`` of workspace (negative status if none)."""
+    return library().nvfp4_gemm_select_ws(m, n, k, kernel, workspace_bytes)
 
 
 def nvfp4_device_status(clear: bool = True, stream=None) -> int:
@@ -196,10 +239,11 @@ def nvfp4_device_status(clear: bool = True, stream=None) -> int:
 
 def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=None,
                  kernel: int = KERNEL_AUTO, pdl: bool = False,
-                 fused: bool = False) -> torch.Tensor:
+                 fused: bool = False, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """One W4A4 decode linear: quantise X[m, k] on the fly and multiply by the
     packed W[n, k].  ``fused`` asks for one kernel (where the CUDA-core stream
-    takes the shape); ``x_out`` = (x_q, x_s) receive the quantised activations."""
+    takes the shape); ``x_out`` = (x_q, x_s) receive the quantised activations;
+    ``workspace`` as in ``nvfp4_gemm_smallm``."""
     _dev(x, torch.float32, "x")
     for t, name in ((wq, "wq"), (ws, "ws")):
         _dev(t, torch.uint8, name)
@@ -216,9 +260,10 @@ def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=
         xq, xs = x_out
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
     opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_FUSED_QUANTIZE if fused else 0)
-    _check("nvfp4_linear", library().nvfp4_linear(
+    wp, wn, _keep = _ws_args(workspace, m, n, k, kernel, x.device)
+    _check("nvfp4_linear", library().nvfp4_linear_ws(
         x.data_ptr(), m, n, k, xg.data_ptr(), wq.data_ptr(), ws.data_ptr(), wg.data_ptr(),
-        y.data_ptr(), xq.data_ptr(), xs.data_ptr(), opts, _stream(x)))
+        y.data_ptr(), xq.data_ptr(), xs.data_ptr(), opts, wp, wn, _stream(x)))
     return y
 
 
@@ -231,4 +276,6 @@ quantize_act = nvfp4_quantize_act
 quantize_act_dynamic = nvfp4_quantize_act_dynamic
 gemm_smallm = nvfp4_gemm_smallm
 gemm_select = nvfp4_gemm_select
+gemm_workspace_size = nvfp4_gemm_workspace_size
+workspace = nvfp4_workspace
 device_status = nvfp4_device_status

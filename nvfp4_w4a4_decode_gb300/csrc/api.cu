@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/nvfp4.h): argument checks, then launches on
-// the caller's stream.  No allocation, no synchronisation, no global state.
+// the caller's stream.  No allocation, no synchronisation, no global state
+// (the split-K kernel's counters live in the caller's workspace).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -102,9 +103,9 @@ int nvfp4_quantize_act_dynamic(const float* x, int64_t m, int64_t k, float* x_g,
 namespace {
 
 // Kernel for a GEMM of this shape and operand alignment (negative status on
-// a request that cannot be met).
+// a request that cannot be met).  ws_bytes is the workspace on offer.
 int select_kernel(int64_t m, int64_t n, int64_t k, uint32_t options, bool ptrs_ok_fast,
-                  bool ptrs_ok_tma)
+                  bool ptrs_ok_tma, int64_t ws_bytes)
 {
     const uint32_t req = options & NVFP4_KERNEL_MASK;
     const bool gemv_ok = nvfp4::gemv_supported(m, k) && ptrs_ok_fast;
@@ -124,24 +125,17 @@ int select_kernel(int64_t m, int64_t n, int64_t k, uint32_t options, bool ptrs_o
     case NVFP4_KERNEL_GEMV: return gemv_ok ? (int)NVFP4_KERNEL_GEMV : -(int)NVFP4_ERR_UNSUPPORTED;
     case NVFP4_KERNEL_MMA: return mma_ok ? (int)NVFP4_KERNEL_MMA : -(int)NVFP4_ERR_UNSUPPORTED;
     case NVFP4_KERNEL_TMA: return tma_ok ? (int)NVFP4_KERNEL_TMA : -(int)NVFP4_ERR_UNSUPPORTED;
+    case NVFP4_KERNEL_SPLITK:
+        return nvfp4::splitk_shape_ok(m, k) && ptrs_ok_fast &&
+                       nvfp4::splitk_plan_ok(m, n, k, ws_bytes)
+                   ? (int)NVFP4_KERNEL_SPLITK
+                   : -(int)NVFP4_ERR_UNSUPPORTED;
     default: return -(int)NVFP4_ERR_UNSUPPORTED;
     }
 }
 
-}  // namespace
-
-int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options)
-{
-    if (m < 1 || n < 1 || k < 16 || (k % 16) != 0)
-        return -NVFP4_ERR_INVALID_ARG;
-    if (m > 8)
-        return -NVFP4_ERR_UNSUPPORTED;
-    return select_kernel(m, n, k, options, true, true);
-}
-
-int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
-                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
-                         int64_t m, int64_t n, int64_t k, uint32_t options, void* stream)
+// Shape and option checks shared by the GEMM entry points (NVFP4_OK to go on).
+int check_gemm_args(int64_t m, int64_t n, int64_t k, uint32_t options)
 {
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
         return NVFP4_ERR_INVALID_ARG;
@@ -152,6 +146,18 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
         return NVFP4_ERR_INVALID_ARG;
     if (m > 8)
         return NVFP4_ERR_UNSUPPORTED;
+    return NVFP4_OK;
+}
+
+int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t* w_q,
+         const uint8_t* w_s, const float* w_g, float* y, int64_t m, int64_t n, int64_t k,
+         uint32_t options, void* workspace, size_t workspace_bytes, void* stream)
+{
+    const int chk = check_gemm_args(m, n, k, options);
+    if (chk != NVFP4_OK)
+        return chk;
+    if (workspace == nullptr ? workspace_bytes != 0 : !aligned(workspace, 16))
+        return NVFP4_ERR_INVALID_ARG;
     if (m == 0 || n == 0)
         return NVFP4_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -167,7 +173,8 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
     const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
                            aligned(w_s, 4);
     const bool tma_ptrs = fast_ptrs && aligned(x_s, 32) && aligned(w_s, 32);
-    const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs);
+    const int64_t ws_bytes = workspace ? (int64_t)workspace_bytes : 0;
+    const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs, ws_bytes);
     if (kern < 0)
         return -kern;
     const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
@@ -179,14 +186,62 @@ int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_
         return from_cuda(nvfp4::launch_gemm_mma(a, pdl));
     case NVFP4_KERNEL_TMA:
         return from_cuda(nvfp4::launch_gemm_tma(a, pdl, (options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) != 0));
+    case NVFP4_KERNEL_SPLITK:
+        return from_cuda(nvfp4::launch_gemm_splitk(a, pdl, workspace, ws_bytes));
     default:
         return from_cuda(nvfp4::launch_gemm_generic(a));
     }
 }
 
-int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
-                 const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
-                 uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream)
+}  // namespace
+
+int nvfp4_gemm_select_ws(int64_t m, int64_t n, int64_t k, uint32_t options,
+                         size_t workspace_bytes)
+{
+    if (m < 1 || n < 1 || k < 16 || (k % 16) != 0)
+        return -NVFP4_ERR_INVALID_ARG;
+    if (m > 8)
+        return -NVFP4_ERR_UNSUPPORTED;
+    return select_kernel(m, n, k, options, true, true, (int64_t)workspace_bytes);
+}
+
+int nvfp4_gemm_select(int64_t m, int64_t n, int64_t k, uint32_t options)
+{
+    return nvfp4_gemm_select_ws(m, n, k, options, 0);
+}
+
+int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t options)
+{
+    if (m < 1 || n < 1 || k < 16 || (k % 16) != 0)
+        return -NVFP4_ERR_INVALID_ARG;
+    if (m > 8)
+        return -NVFP4_ERR_UNSUPPORTED;
+    const int kern = select_kernel(m, n, k, options, true, true, INT64_MAX);
+    if (kern < 0)
+        return kern;
+    return kern == (int)NVFP4_KERNEL_SPLITK ? nvfp4::splitk_workspace_bytes(m, n, k) : 0;
+}
+
+int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                         int64_t m, int64_t n, int64_t k, uint32_t options, void* stream)
+{
+    return gemm(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, nullptr, 0, stream);
+}
+
+int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                         int64_t m, int64_t n, int64_t k, uint32_t options, void* workspace,
+                         size_t workspace_bytes, void* stream)
+{
+    return gemm(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, workspace, workspace_bytes,
+                stream);
+}
+
+int nvfp4_linear_ws(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                    const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                    uint8_t* x_q, uint8_t* x_s, uint32_t options, void* workspace,
+                    size_t workspace_bytes, void* stream)
 {
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
         return NVFP4_ERR_INVALID_ARG;
@@ -194,6 +249,8 @@ int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x
         return NVFP4_ERR_INVALID_ARG;
     if (m > 8)
         return NVFP4_ERR_UNSUPPORTED;
+    if (workspace == nullptr ? workspace_bytes != 0 : !aligned(workspace, 16))
+        return NVFP4_ERR_INVALID_ARG;
     if (m == 0 || n == 0)
         return NVFP4_OK;
     const bool fuse = (options & NVFP4_FLAG_FUSED_QUANTIZE) != 0;
@@ -208,7 +265,8 @@ int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x
         const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
                                aligned(w_s, 4);
         const bool tma_ptrs = fast_ptrs && aligned(x_s, 32) && aligned(w_s, 32);
-        const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs);
+        const int64_t ws_bytes = workspace ? (int64_t)workspace_bytes : 0;
+        const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs, ws_bytes);
         if (kern < 0)
             return -kern;
         if (kern == (int)NVFP4_KERNEL_GEMV) {
@@ -220,7 +278,16 @@ int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x
     const int st = nvfp4_quantize_act_ex(x, m, k, x_g, x_q, x_s, pdl ? NVFP4_FLAG_PDL : 0u, stream);
     if (st != NVFP4_OK)
         return st;
-    return nvfp4_gemm_smallm_ex(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, stream);
+    return gemm(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, workspace, workspace_bytes,
+                stream);
+}
+
+int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                 const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                 uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream)
+{
+    return nvfp4_linear_ws(x, m, n, k, x_g, w_q, w_s, w_g, y, x_q, x_s, options, nullptr, 0,
+                           stream);
 }
 
 int nvfp4_device_status(void* stream, uint32_t* flags, int clear)

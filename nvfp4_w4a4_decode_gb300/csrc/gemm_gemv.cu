@@ -42,6 +42,15 @@ namespace nvfp4 {
 
 namespace {
 
+// Resident CTAs per SM the launch asks for (at most what fits).  One leaves
+// half of the register file free, so that the next kernel on the stream can
+// become resident under programmatic dependent launch and prefetch its
+// weights while this one finishes.
+#ifndef NVFP4_GEMV_CTAS_PER_SM
+#define NVFP4_GEMV_CTAS_PER_SM 2
+#endif
+constexpr int kCtasPerSm = NVFP4_GEMV_CTAS_PER_SM;
+
 struct GemvParams {
     const uint8_t* xq;     // quantised activations (unfused) ...
     const uint8_t* xs;
@@ -306,8 +315,8 @@ cudaError_t launch_typed(const GemmArgs& a, const Shape& sh, const FusedAct* fa)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
-    if (per_sm > 2)
-        per_sm = 2;
+    if (per_sm > kCtasPerSm)
+        per_sm = kCtasPerSm;
     const int64_t groups = (a.n + sh.P - 1) / sh.P;
     int64_t grid = (int64_t)device_sm_count(dev) * per_sm;
     if (grid > groups)

@@ -59,9 +59,10 @@ struct MmaParams {
 // One (tile, range) item of a lane: 16 code bytes of rows g and g + 8 and
 // their two block scales each.
 struct Item {
-    uint4 a;      // row g
-    uint4 b;      // row g + 8
-    uint32_t s;   // scale bytes: row g in bits 0..15, row g + 8 in bits 16..31
+    uint4 a;       // row g
+    uint4 b;       // row g + 8
+    uint32_t s0;   // scale bytes of row g (two bytes) ...
+    uint32_t s1;   // ... and of row g + 8, each in the register its load wrote
 };
 
 __device__ __forceinline__ uint32_t ld_u16_stream(const uint8_t* p)
@@ -115,8 +116,8 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ void mma_item(float (&acc)[4], const Item& it, const uint4* bsrc,
                                          int bstride, bool has_b)
 {
-    const uint32_t sa = e4m3x2_to_f16x2(it.s & 0xFFFFu);
-    const uint32_t sb = e4m3x2_to_f16x2(it.s >> 16);
+    const uint32_t sa = e4m3x2_to_f16x2(it.s0);
+    const uint32_t sb = e4m3x2_to_f16x2(it.s1);
     const uint32_t wa[4] = {it.a.x, it.a.y, it.a.z, it.a.w};
     const uint32_t wb[4] = {it.b.x, it.b.y, it.b.z, it.b.w};
 #pragma unroll
@@ -189,9 +190,10 @@ __global__ void __launch_bounds__(512, 2) mma_kernel(const MmaParams prm)
         const uint8_t* ps = ps0 + it * tstep_s + i * scale_i;
         slot.a = oka ? ld_stream_u4(pa) : make_uint4(0u, 0u, 0u, 0u);
         slot.b = okb ? ld_stream_u4(pa + row8_a) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t s0 = oka ? ld_u16_stream(ps) : 0u;
-        const uint32_t s1 = okb ? ld_u16_stream(ps + row8_s) : 0u;
-        slot.s = s0 | (s1 << 16);
+        // each scale stays in its own register until it is used (combining
+        // the two here would stall the loop on these loads right away)
+        slot.s0 = oka ? ld_u16_stream(ps) : 0u;
+        slot.s1 = okb ? ld_u16_stream(ps + row8_s) : 0u;
     };
     Item ring[2];
     issue(ring[0], 0);

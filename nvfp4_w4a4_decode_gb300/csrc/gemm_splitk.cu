@@ -1,0 +1,473 @@
+// gemm_splitk.cu -- small-M W4A4 linear on the tensor cores, K split into
+// chunks and every warp streaming its own work items (mma.sync m16n8k16, f16
+// operands, FP32 accumulation, swap-AB: weight rows are the MMA's 16-row side
+// and the M <= 8 activation rows its 8 columns).  Used for the whole M <= 8
+// range: the ReSET README ("Core components" item 2) streams the weights past
+// the activations for decode; this kernel keeps that pattern (each weight
+// byte read once, activations resident on chip) and moves the MAC onto the
+// tensor cores.
+//
+// Exactness.  Every 16-block scale is folded into its operand before the MMA
+// (e2m1 * dec(scale) is exact in f16), so the tensor core sees the exact
+// dequantised products and only FP32 accumulation rounds; gX * gW is applied
+// at the end.  Because each element carries its own scale, the order of K
+// inside an MMA is free: each lane takes the bytes that make its loads whole
+// 32-byte sectors.
+//
+// Work layout.  K is cut into chunks of kc elements (a multiple of 256).  CTA
+// (c, y) of the (nchunks, Cy) grid owns chunk c; its warp w owns the tiles
+// (16 weight rows) y * NW + w + j * Cy * NW.  A warp works alone after the
+// prologue: it streams the 256-element sub-items of its tiles, tile by tile,
+// through a register ring of kRing sub-items, accumulates a tile's 16 x 8
+// block in four registers per lane, and at the end of the tile's chunk
+//   * writes Y directly when K is one chunk, or
+//   * stores its partial in the workspace and counts it in; the warp that
+//     stores a tile's last partial sums all of them in chunk order (so the
+//     result does not depend on which warp finishes last), writes Y and
+//     resets the tile's counter to zero for the next call.
+// There is no CTA barrier after the prologue and no wait on another CTA.
+// Per sub-item, lane (g, t) = (lane / 4, lane % 4) loads of rows g and g + 8
+// the code bytes [16t, 16t + 16) and [64 + 16t, 64 + 16t + 16) of the row's
+// 128 (so one load instruction covers two whole sectors per row) and the
+// matching scale bytes {2t, 2t + 1} and {8 + 2t, 9 + 2t}.
+// The activations of the chunk are decoded once per CTA, scaled, into shared
+// memory in fragment order (one conflict-free 16-byte read per two MMAs).
+#include "formats.cuh"
+#include "kernels.cuh"
+#include "launch_cache.cuh"
+#include "mma_frag.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+// Tuning constants (compile-time; the defaults are the measured choice).
+#ifndef NVFP4_SPLITK_RING
+#define NVFP4_SPLITK_RING 3
+#endif
+#ifndef NVFP4_SPLITK_MINB
+#define NVFP4_SPLITK_MINB 2
+#endif
+constexpr int kWarps = 8;                  // warps per CTA
+constexpr int kRing = NVFP4_SPLITK_RING;   // sub-items in flight per warp
+constexpr int kMinBlocks = NVFP4_SPLITK_MINB;  // resident CTAs per SM the registers allow
+constexpr int kSub = 256;        // elements of K per sub-item
+constexpr int kMaxChunk = 4096;  // 64 KB of activation fragments per CTA
+
+struct SplitkParams {
+    const uint8_t* xq;
+    const uint8_t* xs;
+    const float* xg;
+    const uint8_t* wq;
+    const uint8_t* ws;
+    const float* wg;
+    float* y;
+    float4* part;     // [tiles][nchunks][32 lanes] partial tiles (nchunks > 1)
+    unsigned* count;  // [tiles] partials stored so far; zero between calls
+    int m;
+    int64_t n;
+    int64_t k;
+    int kc;  // chunk length
+};
+
+// One sub-item of a lane: 16 + 16 code bytes of rows g and g + 8 and their
+// four block scales each.  Each 16-bit scale load keeps its own register: a
+// value combined from two loads would make the loop wait for them where it
+// is combined, not where it is used, and defeat the ring.
+struct Sub {
+    uint4 a0, a1;       // row g
+    uint4 b0, b1;       // row g + 8
+    uint32_t sa0, sa1;  // row g scale bytes {2t, 2t+1} and {8+2t, 9+2t}
+    uint32_t sb0, sb1;  // row g + 8, same
+};
+
+// Code word w (0..7) of a lane with quad position t holds the 8 elements at
+// offset (w < 4 ? 0 : 128) + 32 t + 8 (w & 3) of the sub-item: words 0..3 are
+// its first 16 bytes, 4..7 the second; the activation fragments follow the
+// same order.
+
+template <bool PDL>
+__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const SplitkParams prm)
+{
+    extern __shared__ __align__(16) uint4 xfrag[];  // [kc / 256][8 words][32 lanes]
+    if constexpr (PDL)
+        asm volatile("griddepcontrol.launch_dependents;");
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int chunk = blockIdx.x, nch = gridDim.x;
+    const int64_t n = prm.n, kh = prm.k / 2, kb = prm.k / 16;
+    const int nsub = prm.kc / kSub;
+    const int64_t k0 = (int64_t)chunk * prm.kc;
+    const int64_t ntiles = (n + 15) / 16;
+    const int64_t tile0 = (int64_t)blockIdx.y * kWarps + warp;
+    const int64_t tstride = (int64_t)gridDim.y * kWarps;
+
+    // refill cursor: the next sub-item's tile and index, and this lane's
+    // addresses in rows g and g + 8 of that tile.  Rows past n read row n - 1
+    // instead (they only reach D rows that are never stored), so the loads
+    // need no per-lane condition; sub-items past the warp's last tile are not
+    // loaded.
+    int64_t f_tile = tile0;
+    int f_sub = 0;
+    const uint8_t *fa, *fb, *qa, *qb;
+    auto point = [&](int64_t tile) {
+        const int64_t r = tile * 16 + g;
+        const int64_t ra = r < n ? r : n - 1, rb = r + 8 < n ? r + 8 : n - 1;
+        fa = prm.wq + ra * kh + k0 / 2 + 16 * t;
+        fb = prm.wq + rb * kh + k0 / 2 + 16 * t;
+        qa = prm.ws + ra * kb + k0 / 16 + 2 * t;
+        qb = prm.ws + rb * kb + k0 / 16 + 2 * t;
+    };
+    point(tile0);
+    auto load = [&](Sub& sl) {
+        if (f_tile >= ntiles)
+            return;
+        sl.a0 = ld_stream_u4(fa);
+        sl.a1 = ld_stream_u4(fa + 64);
+        sl.b0 = ld_stream_u4(fb);
+        sl.b1 = ld_stream_u4(fb + 64);
+        sl.sa0 = ld_stream_u16(qa);
+        sl.sa1 = ld_stream_u16(qa + 8);
+        sl.sb0 = ld_stream_u16(qb);
+        sl.sb1 = ld_stream_u16(qb + 8);
+        if (++f_sub == nsub) {
+            f_sub = 0;
+            f_tile += tstride;
+            point(f_tile);
+        } else {
+            fa += kSub / 2;
+            fb += kSub / 2;
+            qa += kSub / 16;
+            qb += kSub / 16;
+        }
+    };
+
+    Sub ring[kRing];
+#pragma unroll
+    for (int s = 0; s < kRing; ++s) {
+        ring[s].a0 = ring[s].a1 = ring[s].b0 = ring[s].b1 = make_uint4(0u, 0u, 0u, 0u);
+        ring[s].sa0 = ring[s].sa1 = ring[s].sb0 = ring[s].sb1 = 0u;
+        load(ring[s]);
+    }
+
+    // the activations are written by the previous kernel on the stream
+    if constexpr (PDL)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int M = prm.m;
+    // Activation fragments of the chunk.  A task is 32 consecutive elements
+    // of one activation row (16 code bytes and their two block scales) that
+    // fill the fragment words w = 4h .. 4h + 3 of lane (gg, tt) in sub-item
+    // `sub`; task = ((sub * 2 + h) * 8 + gg) * 4 + tt.  A thread issues the
+    // loads of all its tasks before it decodes any (one round trip to L2).
+    {
+        constexpr int kUnroll = 4;
+        const int ntask = nsub * 64;
+        for (int base = threadIdx.x; base < ntask; base += kUnroll * kWarps * 32) {
+            uint4 c[kUnroll];
+            uint32_t sc[kUnroll];
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) {
+                const int task = base + j * kWarps * 32;
+                const int gg = (task >> 2) & 7, tt = task & 3, h = (task >> 5) & 1, sub = task >> 6;
+                c[j] = make_uint4(0u, 0u, 0u, 0u);
+                sc[j] = 0u;
+                if (task < ntask && gg < M) {
+                    const int64_t e = k0 + (int64_t)sub * kSub + 128 * h + 32 * tt;
+                    c[j] = __ldg(reinterpret_cast<const uint4*>(prm.xq + gg * kh + e / 2));
+                    sc[j] = __ldg(reinterpret_cast<const unsigned short*>(prm.xs + gg * kb + e / 16));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) {
+                const int task = base + j * kWarps * 32;
+                if (task >= ntask)
+                    break;
+                const int lq = task & 31, h = (task >> 5) & 1, sub = task >> 6;
+                const uint32_t s01 = e4m3x2_to_f16x2_bits(sc[j]);
+                const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t scl = q < 2 ? f16x2_dup_lo(s01) : f16x2_dup_hi(s01);
+                    uint32_t hq[4];
+                    e2m1x8_to_f16(words[q], hq);
+                    xfrag[sub * 256 + (4 * h + q) * 32 + lq] =
+                        make_uint4(f16x2_mul(hq[0], scl), f16x2_mul(hq[1], scl),
+                                   f16x2_mul(hq[2], scl), f16x2_mul(hq[3], scl));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const float gxw = __fmul_rn(__ldg(prm.xg), __ldg(prm.wg));
+
+    // two accumulator sets (the first and second MMA of each word) halve the
+    // dependent MMA chain; they are added at the end of the tile
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+
+    // 16 MMAs over one sub-item: word w of the lane's codes (rows g, g + 8)
+    // feeds MMAs 2w and 2w + 1 with the word's block scale folded in.
+    auto consume = [&](const Sub& sl, const uint4* bsrc) {
+        const uint32_t sa01 = e4m3x2_to_f16x2_bits(sl.sa0);
+        const uint32_t sa23 = e4m3x2_to_f16x2_bits(sl.sa1);
+        const uint32_t sb01 = e4m3x2_to_f16x2_bits(sl.sb0);
+        const uint32_t sb23 = e4m3x2_to_f16x2_bits(sl.sb1);
+        const uint32_t wa[8] = {sl.a0.x, sl.a0.y, sl.a0.z, sl.a0.w,
+                                sl.a1.x, sl.a1.y, sl.a1.z, sl.a1.w};
+        const uint32_t wb[8] = {sl.b0.x, sl.b0.y, sl.b0.z, sl.b0.w,
+                                sl.b1.x, sl.b1.y, sl.b1.z, sl.b1.w};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t pa = w < 4 ? sa01 : sa23, pb = w < 4 ? sb01 : sb23;
+            const uint32_t sA = (w & 2) ? f16x2_dup_hi(pa) : f16x2_dup_lo(pa);
+            const uint32_t sB = (w & 2) ? f16x2_dup_hi(pb) : f16x2_dup_lo(pb);
+            uint32_t ha[4], hb[4];
+            e2m1x8_to_f16(wa[w], ha);
+            e2m1x8_to_f16(wb[w], hb);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ha[q] = f16x2_mul(ha[q], sA);
+                hb[q] = f16x2_mul(hb[q], sB);
+            }
+            const uint4 xb = bsrc[w * 32];
+            mma_m16n8k16(acc, ha[0], hb[0], ha[1], hb[1], xb.x, xb.y);
+            mma_m16n8k16(acc2, ha[2], hb[2], ha[3], hb[3], xb.z, xb.w);
+        }
+    };
+
+    // End of a tile's chunk: Y directly, or the workspace and, for the last
+    // partial of the tile, the fixed-order sum.
+    auto flush = [&](int64_t tile) {
+        float v0 = acc[0] + acc2[0], v1 = acc[1] + acc2[1], v2 = acc[2] + acc2[2],
+              v3 = acc[3] + acc2[3];
+        if (nch > 1) {
+            float4* slot = prm.part + tile * nch * 32 + lane;
+            __stcg(slot + chunk * 32, make_float4(v0, v1, v2, v3));
+            __threadfence();
+            __syncwarp();
+            unsigned prev = 0u;
+            if (lane == 0) {
+                __threadfence();
+                prev = atomicAdd(prm.count + tile, 1u);
+            }
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+            if (prev != (unsigned)nch - 1)
+                return;
+            __threadfence();
+            __syncwarp();
+            // chunk order; the loads of 4 partials are issued before their sums
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < nch; c0 += 4) {
+                float4 p[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (c0 + j < nch)
+                        p[j] = __ldcg(slot + (c0 + j) * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (c0 + j < nch) {
+                        s.x += p[j].x;
+                        s.y += p[j].y;
+                        s.z += p[j].z;
+                        s.w += p[j].w;
+                    }
+            }
+            v0 = s.x;
+            v1 = s.y;
+            v2 = s.z;
+            v3 = s.w;
+            if (lane == 0)
+                atomicExch(prm.count + tile, 0u);
+        }
+        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+        const int c0 = 2 * t, c1 = c0 + 1;
+        if (c0 < M) {
+            if (r0 < n)
+                prm.y[c0 * n + r0] = v0 * gxw;
+            if (r1 < n)
+                prm.y[c0 * n + r1] = v2 * gxw;
+        }
+        if (c1 < M) {
+            if (r0 < n)
+                prm.y[c1 * n + r0] = v1 * gxw;
+            if (r1 < n)
+                prm.y[c1 * n + r1] = v3 * gxw;
+        }
+    };
+
+    const int64_t mytiles = tile0 < ntiles ? (ntiles - 1 - tile0) / tstride + 1 : 0;
+    const int64_t nitems = mytiles * nsub;
+    int64_t c_tile = tile0;
+    int c_sub = 0;
+    for (int64_t e = 0; e < nitems; e += kRing) {
+#pragma unroll
+        for (int s = 0; s < kRing; ++s) {
+            if (e + s < nitems) {
+                consume(ring[s], xfrag + c_sub * 256 + lane);
+                load(ring[s]);
+                if (++c_sub == nsub) {
+                    flush(c_tile);
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                    acc2[0] = acc2[1] = acc2[2] = acc2[3] = 0.f;
+                    c_sub = 0;
+                    c_tile += tstride;
+                }
+            }
+        }
+    }
+}
+
+struct SplitkPlan {
+    int kc, nch;
+    int64_t cy;
+};
+
+// Workspace layout: the per-tile counters in the first counter_region(size)
+// bytes, the partial tiles after them.  The split depends only on the
+// workspace's size, never on the shape, so calls of different shapes that
+// share one workspace keep each other's partials out of the counters (which
+// must stay zero between calls).  A split call has at least two 512-byte
+// partials per tile, so its counters (4 bytes per tile) always fit.
+int64_t counter_region(int64_t ws_bytes)
+{
+    return (ws_bytes / 128 + 255) / 256 * 256;
+}
+
+bool plan_fits(int64_t ntiles, int nch, int64_t ws_bytes)
+{
+    if (nch <= 1)
+        return true;
+    const int64_t p0 = counter_region(ws_bytes);
+    const int64_t parts = ntiles * nch * 32 * (int64_t)sizeof(float4);
+    return ntiles * 4 <= p0 && parts <= ws_bytes - p0;
+}
+
+int64_t workspace_bytes_for(int64_t ntiles, int nch)
+{
+    if (nch <= 1)
+        return 0;
+    const int64_t parts = ntiles * nch * 32 * (int64_t)sizeof(float4);
+    int64_t ws = (parts + parts / 127 + 511) / 256 * 256;
+    while (!plan_fits(ntiles, nch, ws))
+        ws += 256;
+    return ws;
+}
+
+// CTAs of the kernel resident on the current device (the occupancy at the
+// largest chunk; the shared memory limit is raised first, since the query
+// counts against the limit in force).
+int64_t resident_ctas()
+{
+    const int dev = current_device();
+    const size_t smem = (size_t)kMaxChunk * 16;
+    int per_sm = 0;
+    if (ensure_smem_limit(splitk_kernel<false>, smem, dev) != cudaSuccess ||
+        ensure_smem_limit(splitk_kernel<true>, smem, dev) != cudaSuccess ||
+        cached_occupancy(splitk_kernel<true>, kWarps * 32, smem, 0, dev, &per_sm) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    return (int64_t)device_sm_count(dev) * per_sm;
+}
+
+// Chunk length: multiples of 256 that divide K, at most 4096.  The cost of a
+// candidate is the work of the busiest warp (its tiles times the chunk, plus
+// a reduction allowance per tile when partials go through the workspace);
+// the cheapest wins, ties to the longer chunk.  Candidates whose workspace
+// exceeds `ws_limit` are skipped (0: only single-chunk plans).
+bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* out)
+{
+    if (m < 1 || m > 8 || n < 1 || k < kSub || k % kSub != 0)
+        return false;
+    const int64_t slots = resident_ctas();
+    const int64_t ntiles = (n + 15) / 16;
+    const int64_t kReduce = 256;
+    bool found = false;
+    int64_t best = 0;
+    for (int64_t kc = (k < kMaxChunk ? k : kMaxChunk) / kSub * kSub; kc >= kSub; kc -= kSub) {
+        if (k % kc)
+            continue;
+        const int64_t nch = k / kc;
+        if (nch > 65535 || !plan_fits(ntiles, (int)nch, ws_limit))
+            continue;
+        int64_t cy = slots / nch;
+        const int64_t cy_max = (ntiles + kWarps - 1) / kWarps;
+        if (cy > cy_max)
+            cy = cy_max;
+        if (cy < 1)
+            cy = 1;
+        const int64_t per_warp = (ntiles + cy * kWarps - 1) / (cy * kWarps);
+        const int64_t cost = per_warp * (kc + (nch > 1 ? kReduce : 0));
+        if (!found || cost < best) {
+            found = true;
+            best = cost;
+            out->kc = (int)kc;
+            out->nch = (int)nch;
+            out->cy = cy;
+        }
+    }
+    return found;
+}
+
+template <bool PDL>
+cudaError_t launch_t(const GemmArgs& a, const SplitkPlan& p, void* workspace, int64_t ws_bytes)
+{
+    const size_t smem = (size_t)p.kc * 16;
+    auto kern = splitk_kernel<PDL>;
+    const int dev = current_device();
+    if (smem > 48 * 1024) {
+        const cudaError_t e = ensure_smem_limit(kern, (size_t)kMaxChunk * 16, dev);
+        if (e != cudaSuccess)
+            return e;
+    }
+    SplitkParams prm = {a.xq, a.xs, a.xg, a.wq, a.ws, a.wg, a.y, nullptr, nullptr,
+                        a.m,  a.n,  a.k,  p.kc};
+    if (p.nch > 1) {
+        unsigned char* base = static_cast<unsigned char*>(workspace);
+        prm.count = reinterpret_cast<unsigned*>(base);
+        prm.part = reinterpret_cast<float4*>(base + counter_region(ws_bytes));
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.nch, (unsigned)p.cy, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+}  // namespace
+
+bool splitk_shape_ok(int64_t m, int64_t k)
+{
+    return m >= 1 && m <= 8 && k >= kSub && k % kSub == 0;
+}
+
+bool splitk_plan_ok(int64_t m, int64_t n, int64_t k, int64_t workspace_bytes)
+{
+    SplitkPlan p;
+    return plan_splitk(m, n, k, workspace_bytes, &p);
+}
+
+int64_t splitk_workspace_bytes(int64_t m, int64_t n, int64_t k)
+{
+    SplitkPlan p;
+    if (!plan_splitk(m, n, k, INT64_MAX, &p))
+        return 0;
+    return workspace_bytes_for((n + 15) / 16, p.nch);
+}
+
+cudaError_t launch_gemm_splitk(const GemmArgs& a, bool pdl, void* workspace,
+                               int64_t workspace_bytes)
+{
+    SplitkPlan p;
+    if (!plan_splitk(a.m, a.n, a.k, workspace ? workspace_bytes : 0, &p))
+        return cudaErrorInvalidValue;
+    return pdl ? launch_t<true>(a, p, workspace, workspace_bytes)
+               : launch_t<false>(a, p, workspace, workspace_bytes);
+}
+
+}  // namespace nvfp4

@@ -56,6 +56,19 @@ bool tma_supported(int64_t m, int64_t n, int64_t k);
 // true when the TMA kernel keeps the whole K in one CTA (no cluster split)
 bool tma_single_cta_k(int64_t m, int64_t k);
 cudaError_t launch_gemm_tma(const GemmArgs& a, bool pdl, bool test_timeout);
+// Split-K tensor-core kernel, one work stream per warp: m in 1..8, k a
+// multiple of 256; x_q/w_q 16-byte and x_s/w_s 2-byte aligned.  When K is cut
+// into more than one chunk the partial tiles go through a workspace of
+// splitk_workspace_bytes() bytes (the plan with an unlimited workspace); it
+// must be zero before its first use and every completed launch leaves it
+// zero.  With a smaller workspace (or none) the plan is restricted to what
+// fits; splitk_plan_ok() says whether one does.
+bool splitk_shape_ok(int64_t m, int64_t k);
+bool splitk_plan_ok(int64_t m, int64_t n, int64_t k, int64_t workspace_bytes);
+int64_t splitk_workspace_bytes(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_gemm_splitk(const GemmArgs& a, bool pdl, void* workspace,
+                               int64_t workspace_bytes);
+
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
 
 }  // namespace nvfp4

@@ -136,3 +136,25 @@ def test_dynamic_quantize_rejects_bad_arguments(lib):
     assert q(FAKE, 1, 20, FAKE, FAKE, FAKE, None) == 1       # K not a multiple of 16
     assert q(FAKE, 1, 32, None, FAKE, FAKE, None) == 1       # no x_g output
     assert q(FAKE + 4, 1, 32, FAKE, FAKE, FAKE, None) == 1   # X misaligned
+
+
+def test_workspace_entry_points_host_only(lib):
+    """Workspace size and checks of the _ws entry points answer on the host."""
+    SPLITK = nv.KERNEL_SPLITK
+    assert lib.nvfp4_gemm_workspace_size(1, 100, 4096, nv.KERNEL_GEMV) == 0
+    assert lib.nvfp4_gemm_workspace_size(8, 6144, 4096, SPLITK) >= 0
+    assert lib.nvfp4_gemm_workspace_size(8, 6144, 12288, SPLITK) > 0    # K > one chunk
+    assert lib.nvfp4_gemm_workspace_size(9, 100, 4096, SPLITK) == -2
+    assert lib.nvfp4_gemm_workspace_size(1, 100, 40, SPLITK) == -1
+    assert lib.nvfp4_gemm_workspace_size(1, 100, 4000, SPLITK) == -2   # K % 256 != 0
+    assert nv.gemm_select(3, 100, 4096, SPLITK) == SPLITK    # one chunk: no workspace needed
+    assert nv.gemm_select(3, 100, 8192, SPLITK) == -2        # needs a workspace
+    ok = [FAKE] * 7
+    g = lib.nvfp4_gemm_smallm_ws
+    assert g(*ok, 1, 16, 256, SPLITK, None, 64, None) == 1           # bytes without a pointer
+    assert g(*ok, 1, 16, 256, SPLITK, FAKE + 8, 64, None) == 1       # misaligned workspace
+    assert g(*ok, 9, 16, 256, SPLITK, FAKE, 64, None) == 2
+    assert g(*ok, 0, 16, 256, SPLITK, FAKE, 64, None) == 0           # empty: nothing to do
+    f = lib.nvfp4_linear_ws
+    assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None, 8, None) == 1
+    assert f(FAKE, 0, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 8, None) == 0

@@ -139,15 +139,18 @@ def test_gemm_deterministic_and_no_overrun(nv):
 
 
 def full_size_case(nv, m, n, k, std, seed, samples=64):
-    """Full-size linear: whole GPU path; the oracle evaluates ``samples``
-    output rows n (all m) from its own quantisation of those rows."""
+    """Full-size linear: whole GPU path (the library's choice of kernel and
+    the split-K tensor-core kernel, in the launch configuration the benchmark
+    uses); the oracle evaluates ``samples`` output rows n (all m) from its own
+    quantisation of those rows.  Returns the larger of the two errors."""
     w = synthetic.weights(n, k, std, seed=seed)
     x = synthetic.activations(m, k, seed=seed + 1)
     xd = dev(x)
     xg = nv.global_scale(xd)
     wq, ws, wg = nv.pack_weight(dev(w))
     xq, xs = nv.quantize_act(xd, xg)
-    y = host(nv.gemm_smallm(xq, xs, xg, wq, ws, wg))
+    ys = [host(nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=kern)).copy()
+          for kern in (nv.KERNEL_AUTO, nv.KERNEL_SPLITK)]
     del wq, ws
     gx = oracle.global_scale(x)
     gw = oracle.global_scale(w)
@@ -159,7 +162,7 @@ def full_size_case(nv, m, n, k, std, seed, samples=64):
     # the row rms of the full output is estimated from the GPU-independent
     # sampled reference
     row_rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
-    err = sampled_error(y[:, rows], ref, row_rms)
+    err = max(sampled_error(y[:, rows], ref, row_rms) for y in ys)
     torch.cuda.empty_cache()
     return err
 
@@ -363,6 +366,135 @@ def test_tma_bounded_wait_times_out_and_recovers(nv):
     wq_o, ws_o, gw = oracle.pack_weight(w)
     assert gemm_error(y, oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)) <= GEMM_TOL
     assert nv.device_status() == 0
+
+
+# Split-K tensor-core kernel: every M; K of one chunk and of 3..100 chunks,
+# including chunk lengths that are not powers of two (1280, 1536) and 17
+# chunks of 256 (K = 4352); fewer rows than a tile, ragged last tiles, more
+# tiles than warps.
+SPLITK_SHAPES = [(256, 5), (512, 37), (1280, 16 * 70 + 5), (4096, 16 * 37 + 5), (4352, 33),
+                 (5120, 300), (8192, 33), (12288, 64), (25600, 21), (4096, 40000),
+                 (12288, 16 * 300 + 9)]
+
+
+def splitk_case(nv, m, n, k, seed):
+    x = synthetic.activations(m, k, seed=seed)
+    w = synthetic.weights(n, k, 0.02, seed=seed + 1)
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    return (xq, xs, xg, wq, ws, wg), (xq_o, xs_o, gx, wq_o, ws_o, gw)
+
+
+def check_rows(y, oracle_ops, n):
+    xq_o, xs_o, gx, wq_o, ws_o, gw = oracle_ops
+    if n <= 4096:
+        ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+        return gemm_error(y, ref)
+    rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(n).integers(0, n, 62)]))
+    ref = oracle.gemm(xq_o, xs_o, gx, wq_o[rows], ws_o[rows], gw)
+    rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+    return sampled_error(y[:, rows], ref, rms)
+
+
+@pytest.mark.parametrize("k,n", SPLITK_SHAPES)
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 8])
+def test_splitk_kernel(nv, m, n, k):
+    ops, oops = splitk_case(nv, m, n, k, seed=k + 13 * m + n)
+    wsp = nv.workspace(m, n, k, nv.KERNEL_SPLITK)
+    assert (wsp is None) == (nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) == 0)
+    y = host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK, workspace=wsp)).copy()
+    assert check_rows(y, oops, n) <= GEMM_TOL
+    # same workspace again (its counters were reset), with PDL: same bytes
+    y2 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK, pdl=True, workspace=wsp)
+    np.testing.assert_array_equal(host(y2), y)
+    if k <= 4096:  # without a workspace: one chunk per tile, another plan
+        y3 = host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK))
+        assert check_rows(y3, oops, n) <= GEMM_TOL
+
+
+def test_splitk_needs_workspace_beyond_one_chunk(nv):
+    m, n, k = 2, 64, 8192
+    assert nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) > 0
+    assert nv.gemm_select(m, n, k, nv.KERNEL_SPLITK) == -2   # no workspace on offer
+    ops, _ = splitk_case(nv, m, n, k, seed=5)
+    lib = nv.library()
+    y = torch.empty((m, n), device="cuda")
+    st = lib.nvfp4_gemm_smallm_ws(*[t.data_ptr() for t in ops[:6]], y.data_ptr(), m, n, k,
+                                  nv.KERNEL_SPLITK, None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    assert st == 2
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")    # too small for any split
+    st = lib.nvfp4_gemm_smallm_ws(*[t.data_ptr() for t in ops[:6]], y.data_ptr(), m, n, k,
+                                  nv.KERNEL_SPLITK, small.data_ptr(), small.numel(),
+                                  torch.cuda.current_stream().cuda_stream)
+    assert st == 2
+
+
+def test_splitk_workspace_shared_across_shapes(nv):
+    """One workspace, sized for the largest, serves a sequence of shapes and
+    orders (every call leaves its counters at zero); results equal those of
+    fresh workspaces."""
+    shapes = [(8, 6144, 4096), (1, 4096, 12288), (4, 5120, 25600), (8, 6144, 4096)]
+    cases = [splitk_case(nv, m, n, k, seed=40 + i)[0] for i, (m, n, k) in enumerate(shapes)]
+    size = max(nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) for m, n, k in shapes)
+    shared = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    got = [host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK, workspace=shared)).copy()
+           for ops in cases]
+    for ops, g in zip(cases, got):
+        np.testing.assert_array_equal(host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK)), g)
+
+
+def test_splitk_decades_of_scales(nv):
+    """Extreme block scales stay exact in the folded FP16 operands (weights and
+    activations drawn block by block over many decades)."""
+    m, n, k = 8, 96, 8192
+    x = synthetic.log_uniform_blocks(m, k, seed=23)
+    w = synthetic.log_uniform_blocks(n, k, seed=24)
+    gx = oracle.global_scale(x)
+    xq_o, xs_o = oracle.quantize(x, gx)
+    wq_o, ws_o, gw = oracle.pack_weight(w)
+    ref = oracle.gemm(xq_o, xs_o, gx, wq_o, ws_o, gw)
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    xq, xs = nv.quantize_act(xd, xg)
+    y = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_SPLITK)
+    assert gemm_error(host(y), ref) <= GEMM_TOL
+
+
+def test_splitk_graph_chain_with_pdl(nv):
+    """The four 8B linears at M = 8 as split-K calls with PDL, captured in a
+    graph on one shared workspace, replay to the eager results."""
+    lin = synthetic.LINEARS_8B
+    cases = [splitk_case(nv, 8, l.n, l.k, seed=90 + j)[0] for j, l in enumerate(lin)]
+    size = max(nv.gemm_workspace_size(8, l.n, l.k, nv.KERNEL_SPLITK) for l in lin)
+    shared = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((8, l.n), device="cuda") for l in lin]
+    eager = [host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK)).copy() for ops in cases]
+
+    def step():
+        for j, ops in enumerate(cases):
+            nv.gemm_smallm(*ops, out=outs[j], kernel=nv.KERNEL_SPLITK, pdl=True, workspace=shared)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for o in outs:
+        o.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    for j in range(4):
+        np.testing.assert_array_equal(host(outs[j]), eager[j])
 
 
 # ---- fused quantise + GEMM (nvfp4_linear) --------------------------------------
