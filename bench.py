@@ -563,18 +563,22 @@ def kernel_source_hash() -> str:
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(rows_per_linear: int, seed: int = 99):
-    """Packed operands for a bounded sample of the workload: all four linears
-    of one layer, ``rows_per_linear`` output rows each (packing not timed)."""
+def oracle_sample(rows_per_linear: int, seed: int = 99, layers: int = 1):
+    """Packed operands for a bounded sample of the workload: the four linears
+    of ``layers`` layers (distinct seeded weights), ``rows_per_linear`` output
+    rows each (packing not timed)."""
     import oracle
     items = []
-    for j, lin in enumerate(synthetic.LINEARS_8B):
-        rows = min(rows_per_linear, lin.n)
-        w = synthetic.weights(rows, lin.k, synthetic.WEIGHT_STD_8B, seed=seed + j)
-        x = synthetic.activations(1, lin.k, seed=seed + 10 + j)
-        wq, ws, gw = oracle.pack_weight(w)
-        gx = oracle.global_scale(x)
-        items.append((x, gx, wq, ws, gw, rows, lin.k))
+    for l in range(layers):
+        for j, lin in enumerate(synthetic.LINEARS_8B):
+            rows = min(rows_per_linear, lin.n)
+            s = synthetic.weight_seed(seed, l, j)
+            w = synthetic.weights(rows, lin.k, synthetic.WEIGHT_STD_8B, seed=s)
+            x = synthetic.activations(1, lin.k, seed=s + 1)
+            wq, ws, gw = oracle.pack_weight(w)
+            del w
+            gx = oracle.global_scale(x)
+            items.append((x, gx, wq, ws, gw, rows, lin.k))
     return items
 
 
@@ -593,24 +597,35 @@ def sample_bytes(items):
     return tot
 
 
-def calibrate_rows(budget_s: float) -> int:
+def calibrate_sample(budget_s: float):
+    """(rows per linear, layers) of an oracle sample that takes about
+    ``budget_s`` seconds on this host: a probe of 8 rows per linear sets the
+    cost per row; below one whole layer the rows are cut, above it whole
+    layers are added (at most the 36 of the step)."""
     probe = oracle_sample(8)
     t0 = time.perf_counter()
     oracle_pass(probe)
     dt = max(time.perf_counter() - t0, 1e-4)
-    return int(max(8, min(24576, 8 * budget_s / dt)))
+    per_elem = dt / sum(8 * lin.k for lin in synthetic.LINEARS_8B)
+    full_layer = per_elem * sum(lin.n * lin.k for lin in synthetic.LINEARS_8B)
+    if full_layer >= budget_s:
+        rows = int(budget_s / per_elem / sum(lin.k for lin in synthetic.LINEARS_8B))
+        return max(8, rows), 1
+    return max(lin.n for lin in synthetic.LINEARS_8B), int(min(36, max(1, round(budget_s / full_layer))))
 
 
 def cpu_baseline(budget_s: float = 12.0) -> dict:
-    rows = calibrate_rows(budget_s)
-    items = oracle_sample(rows)
+    rows, layers = calibrate_sample(budget_s)
+    items = oracle_sample(rows, layers=layers)
     t0 = time.perf_counter()
     oracle_pass(items)
     sec = time.perf_counter() - t0
     v = sample_bytes(items) / sec / 1e9
+    what = (f"{layers} whole layers (all output rows)" if layers > 1 or rows >= 24576
+            else f"one layer, {rows} output rows per linear")
     return {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"one layer's four 8B-shaped linears at M=1, {rows} output rows each "
-                      f"(quantise X + FP64 GEMM from packed bytes), {sec:.1f} s, single thread",
+            "sample": f"the four 8B-shaped linears at M=1 of {what}: quantise X + FP64 GEMM "
+                      f"from packed bytes, {sec:.1f} s, single thread",
             "seconds": round(sec, 2)}
 
 
@@ -673,8 +688,11 @@ def run_reference(args) -> dict | None:
         return None
     import oracle
     oracle.build()
-    rows = calibrate_rows(budget_s=args.ref_step_seconds)
-    items = oracle_sample(rows)
+    # each step a bounded sample, sized so that the whole run (warm-up and
+    # timed steps) takes about two and a half minutes of host time
+    budget = args.ref_step_seconds or max(0.05, 150.0 / (args.steps + args.warmup))
+    rows, layers = calibrate_sample(budget)
+    items = oracle_sample(rows, layers=layers)
     for _ in range(args.warmup):
         oracle_pass(items)
     times = []
@@ -684,13 +702,16 @@ def run_reference(args) -> dict | None:
         times.append(time.perf_counter() - t0)
     sec = sum(times) / len(times)
     v = sample_bytes(items) / sec / 1e9
-    sample = (f"per step: one layer's four 8B-shaped linears at M=1, {rows} output rows each "
-              f"(quantise X + FP64 GEMM from packed bytes), single thread")
+    what = (f"{layers} whole layers" if layers > 1 or rows >= 24576
+            else f"one layer, {rows} output rows per linear")
+    sample = (f"per step: the four 8B-shaped linears at M=1 of {what} (quantise X + FP64 GEMM "
+              f"from packed bytes), {sec:.2f} s, single thread")
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "m": 1, "sample_rows_per_linear": rows},
+            "config": {"workload": WORKLOAD, "m": 1, "sample_rows_per_linear": rows,
+                       "sample_layers": layers},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -706,7 +727,8 @@ def main():
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--layers", type=int, default=synthetic.DECODE_LAYERS_8B)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=0.0,
+                    help="host seconds per reference step (default: ~150 s over the run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", action="store_true",
                     help="one kernel per linear (quantisation in the GEMM prologue) instead of "

@@ -148,6 +148,13 @@ def test_workspace_entry_points_host_only(lib):
     assert lib.nvfp4_gemm_workspace_size(1, 100, 40, SPLITK) == -1
     assert lib.nvfp4_gemm_workspace_size(1, 100, 4000, SPLITK) == -2   # K % 256 != 0
     assert nv.gemm_select(3, 100, 4096, SPLITK) == SPLITK    # one chunk: no workspace needed
+    for m, n, k in ((4, 6144, 4096), (8, 4096, 12288), (3, 5120, 25600)):
+        need = lib.nvfp4_gemm_workspace_size(m, n, k, nv.KERNEL_AUTO)
+        assert need == lib.nvfp4_gemm_workspace_size(m, n, k, SPLITK)
+        assert nv.gemm_select(m, n, k, nv.KERNEL_AUTO, need) == SPLITK     # offered: taken
+        if need:
+            assert nv.gemm_select(m, n, k, nv.KERNEL_AUTO, need - 256) != SPLITK
+    assert lib.nvfp4_gemm_workspace_size(1, 6144, 4096, nv.KERNEL_AUTO) == 0   # gemv
     assert nv.gemm_select(3, 100, 8192, SPLITK) == -2        # needs a workspace
     ok = [FAKE] * 7
     g = lib.nvfp4_gemm_smallm_ws
