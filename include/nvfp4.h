@@ -236,6 +236,34 @@ int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The split-K GEMM without any allocation (the pages have no counterpart to
+ * this entry point; it exists for callers that cannot provide a workspace):
+ * as nvfp4_gemm_smallm_ws with NVFP4_KERNEL_SPLITK and a workspace of at
+ * least nvfp4_gemm_workspace_size() bytes -- same plan, same result bits --
+ * except that the scratch is a library-owned static device array of
+ * nvfp4_gemm_static_scratch_bytes() (4 MiB) per device.  Its address is
+ * looked up once per device, on the first call, which also clears its
+ * counter region on `stream` (the counters must start at zero; the array is
+ * zero when the library loads and every completed call leaves them zero).
+ * Nothing is allocated or freed.
+ *   options   NVFP4_KERNEL_AUTO or NVFP4_KERNEL_SPLITK, optionally
+ *             NVFP4_FLAG_PDL (anything else: NVFP4_ERR_INVALID_ARG)
+ * Returns NVFP4_ERR_UNSUPPORTED, launching nothing, when the shape is not
+ * one the split-K kernel takes, the operands are not aligned for it, or the
+ * scratch the call needs exceeds the static array.  All calls on a device
+ * share the one array: calls that may overlap in time (other streams, other
+ * host threads without ordering) race and give wrong results; calls on one
+ * stream are ordered and safe.
+ */
+int nvfp4_gemm_smallm_static(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                             const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
+                             float* y, int64_t m, int64_t n, int64_t k, uint32_t options,
+                             void* stream);
+
+/* Bytes of the static scratch array behind nvfp4_gemm_smallm_static. */
+int64_t nvfp4_gemm_static_scratch_bytes(void);
+
+/*
  * One W4A4 decode linear: quantise X[m][k] with the static tensor scale *x_g
  * (exactly as nvfp4_quantize_act: the codes and scales are written to x_q and
  * x_s) and compute Y[m][n] = X . W^T from them (as nvfp4_gemm_smallm_ex with

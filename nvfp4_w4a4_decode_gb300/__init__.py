@@ -25,6 +25,7 @@ __all__ = [
     "nvfp4_quantize_act", "nvfp4_gemm_smallm", "global_scale", "pack_weight",
     "quantize_act", "gemm_smallm", "nvfp4_linear", "linear", "MAX_M",
     "nvfp4_gemm_workspace_size", "nvfp4_workspace", "gemm_workspace_size", "workspace",
+    "nvfp4_gemm_smallm_static", "gemm_smallm_static",
 ]
 
 MAX_M = 8
@@ -53,6 +54,9 @@ SIGNATURES = {
     "nvfp4_quantize_act_dynamic": ([_p, _i64, _i64, _p, _p, _p, _p], ctypes.c_int),
     "nvfp4_gemm_workspace_size": ([_i64, _i64, _i64, ctypes.c_uint32], _i64),
     "nvfp4_gemm_select_ws": ([_i64, _i64, _i64, ctypes.c_uint32, ctypes.c_size_t], ctypes.c_int),
+    "nvfp4_gemm_smallm_static": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_uint32,
+                                  _p], ctypes.c_int),
+    "nvfp4_gemm_static_scratch_bytes": ([], _i64),
     "nvfp4_gemm_smallm_ws": ([_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_uint32, _p,
                               ctypes.c_size_t, _p], ctypes.c_int),
     "nvfp4_linear_ws": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p,
@@ -222,6 +226,29 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
     return y
 
 
+def nvfp4_gemm_smallm_static(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
+                             pdl: bool = False) -> torch.Tensor:
+    """The split-K GEMM on the library's static scratch array (no workspace,
+    no allocation in the library): same result bits as ``nvfp4_gemm_smallm``
+    with KERNEL_SPLITK and a full workspace.  Calls that may overlap in time
+    share the one array and race."""
+    for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
+        _dev(t, torch.uint8, name)
+    _dev(xg, torch.float32, "xg")
+    _dev(wg, torch.float32, "wg")
+    m, kh = xq.shape
+    n = wq.shape[0]
+    k = kh * 2
+    if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
+        raise ValueError("operand shapes disagree")
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    _check("nvfp4_gemm_smallm_static", library().nvfp4_gemm_smallm_static(
+        xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
+        wg.data_ptr(), y.data_ptr(), m, n, k, KERNEL_SPLITK | (FLAG_PDL if pdl else 0),
+        _stream(xq)))
+    return y
+
+
 def nvfp4_gemm_select(m: int, n: int, k: int, kernel: int = KERNEL_AUTO,
                       workspace_bytes: int = 0) -> int:
     """Kernel id the library runs for this shape when offered
@@ -277,5 +304,6 @@ quantize_act_dynamic = nvfp4_quantize_act_dynamic
 gemm_smallm = nvfp4_gemm_smallm
 gemm_select = nvfp4_gemm_select
 gemm_workspace_size = nvfp4_gemm_workspace_size
+gemm_smallm_static = nvfp4_gemm_smallm_static
 workspace = nvfp4_workspace
 device_status = nvfp4_device_status

@@ -295,6 +295,39 @@ int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x
                            stream);
 }
 
+int nvfp4_gemm_smallm_static(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
+                             const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                             int64_t m, int64_t n, int64_t k, uint32_t options, void* stream)
+{
+    const uint32_t req = options & NVFP4_KERNEL_MASK;
+    if (req != NVFP4_KERNEL_AUTO && req != NVFP4_KERNEL_SPLITK)
+        return NVFP4_ERR_INVALID_ARG;
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL)) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    const int chk = check_gemm_args(m, n, k, options);
+    if (chk != NVFP4_OK)
+        return chk;
+    if (m == 0 || n == 0)
+        return NVFP4_OK;
+    if (y == nullptr || x_q == nullptr || x_s == nullptr || x_g == nullptr || w_q == nullptr ||
+        w_s == nullptr || w_g == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(y, 4) || !aligned(x_g, 4) || !aligned(w_g, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x_q, 32) || !aligned(w_q, 32) || !aligned(x_s, 4) || !aligned(w_s, 4))
+        return NVFP4_ERR_UNSUPPORTED;
+    if (!nvfp4::splitk_shape_ok(m, k) || !nvfp4::splitk_static_fits(m, n, k))
+        return NVFP4_ERR_UNSUPPORTED;
+    const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k,
+                               static_cast<cudaStream_t>(stream)};
+    return from_cuda(nvfp4::launch_gemm_splitk_static(a, (options & NVFP4_FLAG_PDL) != 0));
+}
+
+int64_t nvfp4_gemm_static_scratch_bytes(void)
+{
+    return nvfp4::splitk_static_scratch_bytes();
+}
+
 int nvfp4_device_status(void* stream, uint32_t* flags, int clear)
 {
     if (flags == nullptr)

@@ -32,6 +32,9 @@
 // matching scale bytes {2t, 2t + 1} and {8 + 2t, 9 + 2t}.
 // The activations of the chunk are decoded once per CTA, scaled, into shared
 // memory in fragment order (one conflict-free 16-byte read per two MMAs).
+#include <mutex>
+#include <unordered_map>
+
 #include "formats.cuh"
 #include "kernels.cuh"
 #include "launch_cache.cuh"
@@ -439,7 +442,60 @@ cudaError_t launch_t(const GemmArgs& a, const SplitkPlan& p, void* workspace, in
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
+// Scratch of the allocation-free entry point: a fixed array in the module's
+// device image, zero when the module is loaded.  Every call on a device
+// shares it, so calls that may overlap in time race.
+constexpr int64_t kStaticScratchBytes = int64_t(4) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of the static scratch on the current device, looked up
+// once per device; the first lookup also clears the counter region on
+// `stream` (the counters must start at zero; every completed call leaves
+// them at zero).
+cudaError_t static_scratch(cudaStream_t stream, void** out)
+{
+    static std::mutex mu;
+    static std::unordered_map<int, void*> addr;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaMemsetAsync(p, 0, (size_t)counter_region(kStaticScratchBytes), stream);
+    if (e != cudaSuccess)
+        return e;
+    addr[dev] = p;
+    *out = p;
+    return cudaSuccess;
+}
+
 }  // namespace
+
+int64_t splitk_static_scratch_bytes()
+{
+    return kStaticScratchBytes;
+}
+
+bool splitk_static_fits(int64_t m, int64_t n, int64_t k)
+{
+    SplitkPlan p;
+    return plan_splitk(m, n, k, INT64_MAX, &p) && plan_fits((n + 15) / 16, p.nch, kStaticScratchBytes);
+}
+
+cudaError_t launch_gemm_splitk_static(const GemmArgs& a, bool pdl)
+{
+    void* scratch = nullptr;
+    const cudaError_t e = static_scratch(a.stream, &scratch);
+    if (e != cudaSuccess)
+        return e;
+    return launch_gemm_splitk(a, pdl, scratch, kStaticScratchBytes);
+}
 
 bool splitk_shape_ok(int64_t m, int64_t k)
 {

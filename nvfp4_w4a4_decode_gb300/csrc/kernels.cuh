@@ -69,6 +69,14 @@ int64_t splitk_workspace_bytes(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_gemm_splitk(const GemmArgs& a, bool pdl, void* workspace,
                                int64_t workspace_bytes);
 
+// The split-K kernel on a library-owned static scratch array of
+// splitk_static_scratch_bytes() (no allocation): splitk_static_fits() says
+// whether the plan a workspace of any size would get fits in it (then the
+// results equal those of launch_gemm_splitk with such a workspace).
+int64_t splitk_static_scratch_bytes();
+bool splitk_static_fits(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_gemm_splitk_static(const GemmArgs& a, bool pdl);
+
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
 
 }  // namespace nvfp4
