@@ -113,16 +113,16 @@ int select_kernel(int64_t m, int64_t n, int64_t k, uint32_t options, bool ptrs_o
     const bool tma_ok = nvfp4::tma_supported(m, n, k) && ptrs_ok_tma;
     switch (req) {
     case NVFP4_KERNEL_AUTO:
-        // measured on GB300 over the 8B / 32B decode shapes: the CUDA-core
-        // stream wins at M <= 2; at larger M the split-K tensor-core kernel
-        // when the call offers the workspace its plan wants; without one the
-        // TMA-fed tensor-core kernel when K fits one CTA, else the
-        // register-streaming one
-        if (gemv_ok)
-            return (int)NVFP4_KERNEL_GEMV;
-        if (nvfp4::splitk_shape_ok(m, k) && ptrs_ok_fast &&
+        // measured on GB300 over the 8B / 32B decode shapes: at M >= 2 the
+        // split-K tensor-core kernel when the call offers the workspace its
+        // plan wants; the CUDA-core stream at M = 1 (and at M = 2 without a
+        // workspace); otherwise the TMA-fed tensor-core kernel when K fits
+        // one CTA, else the register-streaming one
+        if (m >= 2 && nvfp4::splitk_shape_ok(m, k) && ptrs_ok_fast &&
             ws_bytes >= nvfp4::splitk_workspace_bytes(m, n, k))
             return (int)NVFP4_KERNEL_SPLITK;
+        if (gemv_ok)
+            return (int)NVFP4_KERNEL_GEMV;
         if (tma_ok && nvfp4::tma_single_cta_k(m, k))
             return (int)NVFP4_KERNEL_TMA;
         return mma_ok ? (int)NVFP4_KERNEL_MMA : (int)NVFP4_KERNEL_GENERIC;

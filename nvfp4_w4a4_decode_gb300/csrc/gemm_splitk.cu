@@ -46,16 +46,36 @@ namespace {
 
 // Tuning constants (compile-time; the defaults are the measured choice).
 #ifndef NVFP4_SPLITK_RING
-#define NVFP4_SPLITK_RING 3
+#define NVFP4_SPLITK_RING 2
 #endif
 #ifndef NVFP4_SPLITK_MINB
 #define NVFP4_SPLITK_MINB 2
+#endif
+// Planner allowances, in sub-items of streaming: a shared-memory reduction
+// per tile when warps share it, a workspace round trip per tile (fence and
+// counter) and the last partial's extra round trips at the end of a launch.
+#ifndef NVFP4_SPLITK_COST_GROUP
+#define NVFP4_SPLITK_COST_GROUP 0.5
+#endif
+#ifndef NVFP4_SPLITK_COST_FLUSH
+#define NVFP4_SPLITK_COST_FLUSH 3.0
+#endif
+#ifndef NVFP4_SPLITK_COST_TAIL
+#define NVFP4_SPLITK_COST_TAIL 3.0
 #endif
 constexpr int kWarps = 8;                  // warps per CTA
 constexpr int kRing = NVFP4_SPLITK_RING;   // sub-items in flight per warp
 constexpr int kMinBlocks = NVFP4_SPLITK_MINB;  // resident CTAs per SM the registers allow
 constexpr int kSub = 256;        // elements of K per sub-item
-constexpr int kMaxChunk = 4096;  // 64 KB of activation fragments per CTA
+constexpr size_t kFragSmem = 64 * 1024;  // activation fragments: 2 M bytes per K element
+constexpr size_t kGroupSmem = 2 * kWarps * 32 * 16;  // partial tiles of the warp groups
+constexpr size_t kMaxSmem = kFragSmem + kGroupSmem;
+
+// Longest chunk whose fragments (M rows, 2 bytes per element) fit.
+__host__ __device__ constexpr int64_t max_chunk(int64_t m)
+{
+    return (int64_t)(kFragSmem / (2 * m)) / kSub * kSub;
+}
 
 struct SplitkParams {
     const uint8_t* xq;
@@ -70,7 +90,8 @@ struct SplitkParams {
     int m;
     int64_t n;
     int64_t k;
-    int kc;  // chunk length
+    int kc;   // chunk length
+    int grp;  // warps that share a tile (1, 2, 4 or 8), splitting its chunk
 };
 
 // One sub-item of a lane: 16 + 16 code bytes of rows g and g + 8 and their
@@ -92,7 +113,9 @@ struct Sub {
 template <bool PDL>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const SplitkParams prm)
 {
-    extern __shared__ __align__(16) uint4 xfrag[];  // [kc / 256][8 words][32 lanes]
+    // [kc / 256][8 words][32 lanes] activation fragments, then (grp > 1)
+    // [2][kWarps][32 lanes] float4 partial tiles of the warp groups
+    extern __shared__ __align__(16) uint4 xfrag[];
     if constexpr (PDL)
         asm volatile("griddepcontrol.launch_dependents;");
 
@@ -103,8 +126,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     const int nsub = prm.kc / kSub;
     const int64_t k0 = (int64_t)chunk * prm.kc;
     const int64_t ntiles = (n + 15) / 16;
-    const int64_t tile0 = (int64_t)blockIdx.y * kWarps + warp;
-    const int64_t tstride = (int64_t)gridDim.y * kWarps;
+    // warp group gi (grp warps) owns tiles; warp rank r of the group takes
+    // sub-items r, r + grp, ... of each tile's chunk
+    const int G = prm.grp, gi = warp / G, r = warp - gi * G, ngrp = kWarps / G;
+    const int64_t tile0 = (int64_t)blockIdx.y * ngrp + gi;
+    const int64_t tstride = (int64_t)gridDim.y * ngrp;
 
     // refill cursor: the next sub-item's tile and index, and this lane's
     // addresses in rows g and g + 8 of that tile.  Rows past n read row n - 1
@@ -112,15 +138,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     // need no per-lane condition; sub-items past the warp's last tile are not
     // loaded.
     int64_t f_tile = tile0;
-    int f_sub = 0;
+    int f_sub = r;
     const uint8_t *fa, *fb, *qa, *qb;
     auto point = [&](int64_t tile) {
-        const int64_t r = tile * 16 + g;
-        const int64_t ra = r < n ? r : n - 1, rb = r + 8 < n ? r + 8 : n - 1;
-        fa = prm.wq + ra * kh + k0 / 2 + 16 * t;
-        fb = prm.wq + rb * kh + k0 / 2 + 16 * t;
-        qa = prm.ws + ra * kb + k0 / 16 + 2 * t;
-        qb = prm.ws + rb * kb + k0 / 16 + 2 * t;
+        const int64_t row = tile * 16 + g;
+        const int64_t ra = row < n ? row : n - 1, rb = row + 8 < n ? row + 8 : n - 1;
+        const int64_t c0 = k0 + (int64_t)r * kSub;
+        fa = prm.wq + ra * kh + c0 / 2 + 16 * t;
+        fb = prm.wq + rb * kh + c0 / 2 + 16 * t;
+        qa = prm.ws + ra * kb + c0 / 16 + 2 * t;
+        qb = prm.ws + rb * kb + c0 / 16 + 2 * t;
     };
     point(tile0);
     auto load = [&](Sub& sl) {
@@ -134,15 +161,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
         sl.sa1 = ld_stream_u16(qa + 8);
         sl.sb0 = ld_stream_u16(qb);
         sl.sb1 = ld_stream_u16(qb + 8);
-        if (++f_sub == nsub) {
-            f_sub = 0;
+        f_sub += G;
+        if (f_sub >= nsub) {
+            f_sub = r;
             f_tile += tstride;
             point(f_tile);
         } else {
-            fa += kSub / 2;
-            fb += kSub / 2;
-            qa += kSub / 16;
-            qb += kSub / 16;
+            fa += G * (kSub / 2);
+            fb += G * (kSub / 2);
+            qa += G * (kSub / 16);
+            qb += G * (kSub / 16);
         }
     };
 
@@ -158,25 +186,30 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     if constexpr (PDL)
         asm volatile("griddepcontrol.wait;" ::: "memory");
     const int M = prm.m;
-    // Activation fragments of the chunk.  A task is 32 consecutive elements
-    // of one activation row (16 code bytes and their two block scales) that
-    // fill the fragment words w = 4h .. 4h + 3 of lane (gg, tt) in sub-item
-    // `sub`; task = ((sub * 2 + h) * 8 + gg) * 4 + tt.  A thread issues the
-    // loads of all its tasks before it decodes any (one round trip to L2).
+    // Activation fragments of the chunk, for the M real columns only: lane
+    // (g, t) with g < M holds word w of sub-item `sub` at
+    // xfrag[(sub * 8 + w) * LW + lane], LW = 4 M lanes per word (the other
+    // lanes' B fragments are zero and not stored).  A task is 32 consecutive
+    // elements of one activation row (16 code bytes and their two block
+    // scales) that fill words w = 4h .. 4h + 3 of lane (gg, tt);
+    // task = ((sub * 2 + h) * M + gg) * 4 + tt.  A thread issues the loads of
+    // all its tasks before it decodes any (one round trip to L2).
+    const int LW = 4 * M;
     {
         constexpr int kUnroll = 4;
-        const int ntask = nsub * 64;
+        const int ntask = nsub * 2 * LW;
         for (int base = threadIdx.x; base < ntask; base += kUnroll * kWarps * 32) {
             uint4 c[kUnroll];
             uint32_t sc[kUnroll];
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
                 const int task = base + j * kWarps * 32;
-                const int gg = (task >> 2) & 7, tt = task & 3, h = (task >> 5) & 1, sub = task >> 6;
                 c[j] = make_uint4(0u, 0u, 0u, 0u);
                 sc[j] = 0u;
-                if (task < ntask && gg < M) {
-                    const int64_t e = k0 + (int64_t)sub * kSub + 128 * h + 32 * tt;
+                if (task < ntask) {
+                    const int lq = task % LW, hs = task / LW;  // hs = sub * 2 + h
+                    const int gg = lq >> 2, tt = lq & 3;
+                    const int64_t e = k0 + (int64_t)(hs >> 1) * kSub + 128 * (hs & 1) + 32 * tt;
                     c[j] = __ldg(reinterpret_cast<const uint4*>(prm.xq + gg * kh + e / 2));
                     sc[j] = __ldg(reinterpret_cast<const unsigned short*>(prm.xs + gg * kb + e / 16));
                 }
@@ -186,7 +219,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
                 const int task = base + j * kWarps * 32;
                 if (task >= ntask)
                     break;
-                const int lq = task & 31, h = (task >> 5) & 1, sub = task >> 6;
+                const int lq = task % LW, hs = task / LW;
                 const uint32_t s01 = e4m3x2_to_f16x2_bits(sc[j]);
                 const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
 #pragma unroll
@@ -194,7 +227,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
                     const uint32_t scl = q < 2 ? f16x2_dup_lo(s01) : f16x2_dup_hi(s01);
                     uint32_t hq[4];
                     e2m1x8_to_f16(words[q], hq);
-                    xfrag[sub * 256 + (4 * h + q) * 32 + lq] =
+                    // word 4h + q of sub-item hs / 2: index (hs / 2 * 8 + 4 (hs & 1) + q)
+                    xfrag[(hs * 4 + q) * LW + lq] =
                         make_uint4(f16x2_mul(hq[0], scl), f16x2_mul(hq[1], scl),
                                    f16x2_mul(hq[2], scl), f16x2_mul(hq[3], scl));
                 }
@@ -209,7 +243,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 
     // 16 MMAs over one sub-item: word w of the lane's codes (rows g, g + 8)
-    // feeds MMAs 2w and 2w + 1 with the word's block scale folded in.
+    // feeds MMAs 2w and 2w + 1 with the word's block scale folded in.  Lanes
+    // of columns g >= M read another column's fragment: B column g only
+    // reaches D column g, which is never stored.
+    const int lane_b = lane % LW;
     auto consume = [&](const Sub& sl, const uint4* bsrc) {
         const uint32_t sa01 = e4m3x2_to_f16x2_bits(sl.sa0);
         const uint32_t sa23 = e4m3x2_to_f16x2_bits(sl.sa1);
@@ -232,17 +269,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
                 ha[q] = f16x2_mul(ha[q], sA);
                 hb[q] = f16x2_mul(hb[q], sB);
             }
-            const uint4 xb = bsrc[w * 32];
+            const uint4 xb = bsrc[w * LW];
             mma_m16n8k16(acc, ha[0], hb[0], ha[1], hb[1], xb.x, xb.y);
             mma_m16n8k16(acc2, ha[2], hb[2], ha[3], hb[3], xb.z, xb.w);
         }
     };
 
-    // End of a tile's chunk: Y directly, or the workspace and, for the last
-    // partial of the tile, the fixed-order sum.
-    auto flush = [&](int64_t tile) {
-        float v0 = acc[0] + acc2[0], v1 = acc[1] + acc2[1], v2 = acc[2] + acc2[2],
-              v3 = acc[3] + acc2[3];
+    // End of a tile's chunk (one warp per tile): Y directly, or the workspace
+    // and, for the last partial of the tile, the fixed-order sum.
+    auto flush = [&](int64_t tile, float v0, float v1, float v2, float v3) {
         if (nch > 1) {
             float4* slot = prm.part + tile * nch * 32 + lane;
             __stcg(slot + chunk * 32, make_float4(v0, v1, v2, v3));
@@ -298,21 +333,57 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
         }
     };
 
+    // End of a warp's share of a tile: with warp groups, the group's warps
+    // leave their partials in shared memory (double-buffered, so one barrier
+    // per tile suffices) and rank 0 adds them in rank order and flushes.
+    float4* red = reinterpret_cast<float4*>(xfrag + nsub * 8 * LW);
+    int rbuf = 0;
+    auto tile_end = [&](int64_t tile) {
+        float v0 = acc[0] + acc2[0], v1 = acc[1] + acc2[1], v2 = acc[2] + acc2[2],
+              v3 = acc[3] + acc2[3];
+        if (G > 1) {
+            red[(rbuf * kWarps + warp) * 32 + lane] = make_float4(v0, v1, v2, v3);
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(G * 32) : "memory");
+            const float4* src = red + (rbuf * kWarps + gi * G) * 32 + lane;
+            rbuf ^= 1;
+            if (r != 0)
+                return;
+            float4 s4 = src[0];
+            for (int q = 1; q < G; ++q) {
+                const float4 p = src[q * 32];
+                s4.x += p.x;
+                s4.y += p.y;
+                s4.z += p.z;
+                s4.w += p.w;
+            }
+            v0 = s4.x;
+            v1 = s4.y;
+            v2 = s4.z;
+            v3 = s4.w;
+        }
+        flush(tile, v0, v1, v2, v3);
+    };
+
     const int64_t mytiles = tile0 < ntiles ? (ntiles - 1 - tile0) / tstride + 1 : 0;
-    const int64_t nitems = mytiles * nsub;
+    const int per_tile = nsub / G;  // sub-items of each warp per tile
+    const int64_t nitems = mytiles * per_tile;
     int64_t c_tile = tile0;
-    int c_sub = 0;
+    const int b_first = r * 8 * LW, b_step = G * 8 * LW;  // fragment offsets of this warp's sub-items
+    int c_b = b_first, c_left = per_tile;
+    const uint4* xb = xfrag + lane_b;
     for (int64_t e = 0; e < nitems; e += kRing) {
 #pragma unroll
         for (int s = 0; s < kRing; ++s) {
             if (e + s < nitems) {
-                consume(ring[s], xfrag + c_sub * 256 + lane);
+                consume(ring[s], xb + c_b);
                 load(ring[s]);
-                if (++c_sub == nsub) {
-                    flush(c_tile);
+                c_b += b_step;
+                if (--c_left == 0) {
+                    tile_end(c_tile);
                     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
                     acc2[0] = acc2[1] = acc2[2] = acc2[3] = 0.f;
-                    c_sub = 0;
+                    c_b = b_first;
+                    c_left = per_tile;
                     c_tile += tstride;
                 }
             }
@@ -321,7 +392,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
 }
 
 struct SplitkPlan {
-    int kc, nch;
+    int kc, nch, grp;
     int64_t cy;
 };
 
@@ -362,7 +433,7 @@ int64_t workspace_bytes_for(int64_t ntiles, int nch)
 int64_t resident_ctas()
 {
     const int dev = current_device();
-    const size_t smem = (size_t)kMaxChunk * 16;
+    const size_t smem = kMaxSmem;
     int per_sm = 0;
     if (ensure_smem_limit(splitk_kernel<false>, smem, dev) != cudaSuccess ||
         ensure_smem_limit(splitk_kernel<true>, smem, dev) != cudaSuccess ||
@@ -372,40 +443,53 @@ int64_t resident_ctas()
     return (int64_t)device_sm_count(dev) * per_sm;
 }
 
-// Chunk length: multiples of 256 that divide K, at most 4096.  The cost of a
-// candidate is the work of the busiest warp (its tiles times the chunk, plus
-// a reduction allowance per tile when partials go through the workspace);
-// the cheapest wins, ties to the longer chunk.  Candidates whose workspace
-// exceeds `ws_limit` are skipped (0: only single-chunk plans).
+// Chunk length kc: multiples of 256 that divide K, at most 4096; warps per
+// tile grp: 1, 2, 4 or 8, dividing kc / 256.  The cost of a candidate, in
+// units of one sub-item of streaming, is the busiest warp's sub-items plus
+// allowances for what adds latency: a shared-memory reduction per tile when
+// warps share it, and, when partials go through the workspace, one per tile
+// and the last partial's round trips at the end.  The cheapest wins; ties go
+// to the earlier candidate (longer chunk, fewer warps per tile).  Candidates
+// whose workspace exceeds `ws_limit` are skipped (0: single-chunk plans only).
 bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* out)
 {
     if (m < 1 || m > 8 || n < 1 || k < kSub || k % kSub != 0)
         return false;
     const int64_t slots = resident_ctas();
     const int64_t ntiles = (n + 15) / 16;
-    const int64_t kReduce = 256;
     bool found = false;
-    int64_t best = 0;
-    for (int64_t kc = (k < kMaxChunk ? k : kMaxChunk) / kSub * kSub; kc >= kSub; kc -= kSub) {
+    double best = 0.0;
+    const int64_t kc_max = max_chunk(m);
+    for (int64_t kc = (k < kc_max ? k : kc_max) / kSub * kSub; kc >= kSub; kc -= kSub) {
         if (k % kc)
             continue;
-        const int64_t nch = k / kc;
+        const int64_t nch = k / kc, nsub = kc / kSub;
         if (nch > 65535 || !plan_fits(ntiles, (int)nch, ws_limit))
             continue;
-        int64_t cy = slots / nch;
-        const int64_t cy_max = (ntiles + kWarps - 1) / kWarps;
-        if (cy > cy_max)
-            cy = cy_max;
-        if (cy < 1)
-            cy = 1;
-        const int64_t per_warp = (ntiles + cy * kWarps - 1) / (cy * kWarps);
-        const int64_t cost = per_warp * (kc + (nch > 1 ? kReduce : 0));
-        if (!found || cost < best) {
-            found = true;
-            best = cost;
-            out->kc = (int)kc;
-            out->nch = (int)nch;
-            out->cy = cy;
+        for (int grp = 1; grp <= kWarps; grp *= 2) {
+            if (nsub % grp)
+                continue;
+            const int64_t ngrp = kWarps / grp;
+            int64_t cy = slots / nch;
+            const int64_t cy_max = (ntiles + ngrp - 1) / ngrp;
+            if (cy > cy_max)
+                cy = cy_max;
+            if (cy < 1)
+                cy = 1;
+            const int64_t per_group = (ntiles + cy * ngrp - 1) / (cy * ngrp);
+            const double per_tile = (double)(nsub / grp) +
+                                    (grp > 1 ? NVFP4_SPLITK_COST_GROUP : 0.0) +
+                                    (nch > 1 ? NVFP4_SPLITK_COST_FLUSH : 0.0);
+            const double cost =
+                (double)per_group * per_tile + (nch > 1 ? NVFP4_SPLITK_COST_TAIL : 0.0);
+            if (!found || cost < best) {
+                found = true;
+                best = cost;
+                out->kc = (int)kc;
+                out->nch = (int)nch;
+                out->grp = grp;
+                out->cy = cy;
+            }
         }
     }
     return found;
@@ -414,16 +498,16 @@ bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* 
 template <bool PDL>
 cudaError_t launch_t(const GemmArgs& a, const SplitkPlan& p, void* workspace, int64_t ws_bytes)
 {
-    const size_t smem = (size_t)p.kc * 16;
+    const size_t smem = (size_t)p.kc * 2 * a.m + (p.grp > 1 ? kGroupSmem : 0);
     auto kern = splitk_kernel<PDL>;
     const int dev = current_device();
     if (smem > 48 * 1024) {
-        const cudaError_t e = ensure_smem_limit(kern, (size_t)kMaxChunk * 16, dev);
+        const cudaError_t e = ensure_smem_limit(kern, kMaxSmem, dev);
         if (e != cudaSuccess)
             return e;
     }
     SplitkParams prm = {a.xq, a.xs, a.xg, a.wq, a.ws, a.wg, a.y, nullptr, nullptr,
-                        a.m,  a.n,  a.k,  p.kc};
+                        a.m,  a.n,  a.k,  p.kc, p.grp};
     if (p.nch > 1) {
         unsigned char* base = static_cast<unsigned char*>(workspace);
         prm.count = reinterpret_cast<unsigned*>(base);

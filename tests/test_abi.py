@@ -155,7 +155,9 @@ def test_workspace_entry_points_host_only(lib):
         if need:
             assert nv.gemm_select(m, n, k, nv.KERNEL_AUTO, need - 256) != SPLITK
     assert lib.nvfp4_gemm_workspace_size(1, 6144, 4096, nv.KERNEL_AUTO) == 0   # gemv
-    assert nv.gemm_select(3, 100, 8192, SPLITK) == -2        # needs a workspace
+    assert nv.gemm_select(1, 6144, 4096, nv.KERNEL_AUTO, 1 << 30) == nv.KERNEL_GEMV
+    assert nv.gemm_select(8, 100, 8192, SPLITK) == -2        # M = 8: K > 4096 needs a workspace
+    assert nv.gemm_select(2, 100, 12288, SPLITK) == SPLITK   # M = 2: K up to 16384 in one chunk
     ok = [FAKE] * 7
     g = lib.nvfp4_gemm_smallm_ws
     assert g(*ok, 1, 16, 256, SPLITK, None, 64, None) == 1           # bytes without a pointer

@@ -412,13 +412,14 @@ def test_splitk_kernel(nv, m, n, k):
     # same workspace again (its counters were reset), with PDL: same bytes
     y2 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK, pdl=True, workspace=wsp)
     np.testing.assert_array_equal(host(y2), y)
-    if k <= 4096:  # without a workspace: one chunk per tile, another plan
+    if nv.gemm_select(m, n, k, nv.KERNEL_SPLITK) == nv.KERNEL_SPLITK:
+        # without a workspace: K in one chunk, another plan
         y3 = host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK))
         assert check_rows(y3, oops, n) <= GEMM_TOL
 
 
 def test_splitk_needs_workspace_beyond_one_chunk(nv):
-    m, n, k = 2, 64, 8192
+    m, n, k = 8, 64, 8192
     assert nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) > 0
     assert nv.gemm_select(m, n, k, nv.KERNEL_SPLITK) == -2   # no workspace on offer
     ops, _ = splitk_case(nv, m, n, k, seed=5)
