@@ -201,18 +201,18 @@ __global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
         const int64_t left = valid_iters - (base + STAGES);  // refills still in range
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
-            const uint4 cw = rw[s];
-            const uint32_t cs = rs[s];
+            // decode the stage first, then refill its registers (refilling
+            // first would need a copy of the stage's old contents)
+            uint32_t wh[16];
+            e2m1x8_to_f16(rw[s].x, *reinterpret_cast<uint32_t(*)[4]>(&wh[0]));
+            e2m1x8_to_f16(rw[s].y, *reinterpret_cast<uint32_t(*)[4]>(&wh[4]));
+            e2m1x8_to_f16(rw[s].z, *reinterpret_cast<uint32_t(*)[4]>(&wh[8]));
+            e2m1x8_to_f16(rw[s].w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
+            const float2 sw = e4m3x2_to_float2(rs[s]);
             if (s < left) {
                 rw[s] = ld_stream_u4(wn + s * wstep);
                 rs[s] = ld_u16_nc(sn + s * sstep);
             }
-            uint32_t wh[16];
-            e2m1x8_to_f16(cw.x, *reinterpret_cast<uint32_t(*)[4]>(&wh[0]));
-            e2m1x8_to_f16(cw.y, *reinterpret_cast<uint32_t(*)[4]>(&wh[4]));
-            e2m1x8_to_f16(cw.z, *reinterpret_cast<uint32_t(*)[4]>(&wh[8]));
-            e2m1x8_to_f16(cw.w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
-            const float2 sw = e4m3x2_to_float2(cs);
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 uint32_t p0 = 0u, p1 = 0u;
