@@ -547,15 +547,20 @@ def profile_traffic(kernel: str):
         return None
 
 
+# the sources the M = 1 step's kernels (activation quantiser, CUDA-core
+# stream) and their launch path are built from
+TRAFFIC_SOURCES = ("api.cu", "formats.cuh", "gemm_gemv.cu", "kernels.cuh", "launch_cache.cuh",
+                   "quantize.cu")
+
+
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_w4a4_decode_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
