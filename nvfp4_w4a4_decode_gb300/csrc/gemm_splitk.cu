@@ -189,37 +189,35 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     // Activation fragments of the chunk, for the M real columns only: lane
     // (g, t) with g < M holds word w of sub-item `sub` at
     // xfrag[(sub * 8 + w) * LW + lane], LW = 4 M lanes per word (the other
-    // lanes' B fragments are zero and not stored).  A task is 32 consecutive
-    // elements of one activation row (16 code bytes and their two block
-    // scales) that fill words w = 4h .. 4h + 3 of lane (gg, tt);
-    // task = ((sub * 2 + h) * M + gg) * 4 + tt.  A thread issues the loads of
-    // all its tasks before it decodes any (one round trip to L2).
+    // lanes' B fragments are not stored).  Unit hs = 2 sub + h of the chunk
+    // is 128 elements of each of the M rows; warp hs % 8 decodes it, lane
+    // (gg, tt) < LW taking the 32 elements (16 code bytes, two block scales)
+    // that fill its words 4h .. 4h + 3.  A warp issues the loads of all its
+    // units before it decodes any (one round trip to L2).
     const int LW = 4 * M;
-    {
+    if (lane < LW) {
         constexpr int kUnroll = 4;
-        const int ntask = nsub * 2 * LW;
-        for (int base = threadIdx.x; base < ntask; base += kUnroll * kWarps * 32) {
+        const int nhs = nsub * 2, gg = lane >> 2, tt = lane & 3;
+        const uint8_t* xq_row = prm.xq + gg * kh + (k0 + 32 * tt) / 2;
+        const uint8_t* xs_row = prm.xs + gg * kb + (k0 + 32 * tt) / 16;
+        for (int base = warp; base < nhs; base += kUnroll * kWarps) {
             uint4 c[kUnroll];
             uint32_t sc[kUnroll];
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
-                const int task = base + j * kWarps * 32;
+                const int hs = base + j * kWarps;
                 c[j] = make_uint4(0u, 0u, 0u, 0u);
                 sc[j] = 0u;
-                if (task < ntask) {
-                    const int lq = task % LW, hs = task / LW;  // hs = sub * 2 + h
-                    const int gg = lq >> 2, tt = lq & 3;
-                    const int64_t e = k0 + (int64_t)(hs >> 1) * kSub + 128 * (hs & 1) + 32 * tt;
-                    c[j] = __ldg(reinterpret_cast<const uint4*>(prm.xq + gg * kh + e / 2));
-                    sc[j] = __ldg(reinterpret_cast<const unsigned short*>(prm.xs + gg * kb + e / 16));
+                if (hs < nhs) {  // element offset hs * 128 within the chunk
+                    c[j] = __ldg(reinterpret_cast<const uint4*>(xq_row + hs * 64));
+                    sc[j] = __ldg(reinterpret_cast<const unsigned short*>(xs_row + hs * 8));
                 }
             }
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
-                const int task = base + j * kWarps * 32;
-                if (task >= ntask)
+                const int hs = base + j * kWarps;
+                if (hs >= nhs)
                     break;
-                const int lq = task % LW, hs = task / LW;
                 const uint32_t s01 = e4m3x2_to_f16x2_bits(sc[j]);
                 const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
 #pragma unroll
@@ -227,8 +225,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
                     const uint32_t scl = q < 2 ? f16x2_dup_lo(s01) : f16x2_dup_hi(s01);
                     uint32_t hq[4];
                     e2m1x8_to_f16(words[q], hq);
-                    // word 4h + q of sub-item hs / 2: index (hs / 2 * 8 + 4 (hs & 1) + q)
-                    xfrag[(hs * 4 + q) * LW + lq] =
+                    // word 4 (hs & 1) + q of sub-item hs / 2
+                    xfrag[(hs * 4 + q) * LW + lane] =
                         make_uint4(f16x2_mul(hq[0], scl), f16x2_mul(hq[1], scl),
                                    f16x2_mul(hq[2], scl), f16x2_mul(hq[3], scl));
                 }
