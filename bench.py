@@ -41,13 +41,13 @@ WORKLOAD = ("8B-shaped decode linears qkv/o/gate_up/down (K->N 4096->6144, 4096-
             "distinct weights per step under one CUDA graph")
 
 
-def algorithmic_bytes(m: int, n: int, k: int) -> dict:
+def algorithmic_bytes(m: int, n: int, k: int, x_bytes: int = 4, y_bytes: int = 4) -> dict:
     """Bytes a call must move at minimum: packed weights and scales once,
-    packed activations, both tensor scales, FP32 output; and the activation
-    quantiser's FP32 read plus packed write."""
+    packed activations, both tensor scales, the output (FP32 or BF16); and the
+    activation quantiser's read of X (FP32 or BF16) plus packed write."""
     wbytes = n * k // 2 + n * k // 16
-    gemm = wbytes + m * k // 2 + m * k // 16 + 8 + 4 * m * n
-    quant = 4 * m * k + m * k // 2 + m * k // 16 + 4
+    gemm = wbytes + m * k // 2 + m * k // 16 + 8 + y_bytes * m * n
+    quant = x_bytes * m * k + m * k // 2 + m * k // 16 + 4
     return {"weights": wbytes, "gemm": gemm, "quant": quant}
 
 
@@ -175,9 +175,11 @@ class DecodeStack:
     activation buffers, and the graphs that replay them."""
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
-                 fused: bool = True, kernel: int = 0):
+                 fused: bool = True, kernel: int = 0, bf16: bool = False):
         self.nv, self.torch = nv, torch
         self.m = m
+        self.bf16 = bf16   # BF16 activations in and BF16 outputs out
+        io = torch.bfloat16 if bf16 else torch.float32
         self.pdl = pdl
         self.fused = fused
         self.kernel = kernel
@@ -204,8 +206,8 @@ class DecodeStack:
         # and outputs move between host and device in one copy each
         xsz = sum(m * lin.k for lin in self.lins) * layers
         ysz = sum(m * lin.n for lin in self.lins) * layers
-        self.x_flat = torch.empty(xsz, dtype=torch.float32, device=dev)
-        self.y_flat = torch.empty(ysz, dtype=torch.float32, device=dev)
+        self.x_flat = torch.empty(xsz, dtype=io, device=dev)
+        self.y_flat = torch.empty(ysz, dtype=io, device=dev)
         self.x, self.xg, self.y = [], [], []
         xo = yo = 0
         for l in range(layers):
@@ -213,10 +215,11 @@ class DecodeStack:
             for j, lin in enumerate(self.lins):
                 xa = synthetic.activations(m, lin.k, seed=synthetic.weight_seed(seed + 7, l, j))
                 xd = self.x_flat[xo:xo + m * lin.k].view(m, lin.k)
-                xd.copy_(torch.from_numpy(xa))
+                xd.copy_(torch.from_numpy(xa))     # rounded to BF16 when the I/O is BF16
                 xo += m * lin.k
                 xr.append(xd)
-                gr.append(nv.global_scale(xd))     # static calibration, not timed
+                # static calibration, not timed (from the FP32 values of X)
+                gr.append(nv.global_scale(xd.float().contiguous()))
                 yr.append(self.y_flat[yo:yo + m * lin.n].view(m, lin.n))
                 yo += m * lin.n
             self.x.append(xr)
@@ -270,8 +273,9 @@ class DecodeStack:
 
     def bytes_per_step(self):
         tot = {"weights": 0, "gemm": 0, "quant": 0}
+        io = 2 if self.bf16 else 4
         for lin in self.lins:
-            b = algorithmic_bytes(self.m, lin.n, lin.k)
+            b = algorithmic_bytes(self.m, lin.n, lin.k, io, io)
             for key in tot:
                 tot[key] += self.layers * b[key]
         return tot
@@ -402,7 +406,7 @@ def run_ours(args) -> dict:
     peaks = load_peaks()
 
     stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
-                        fused=args.fused, kernel=KERNELS[args.kernel](nv))
+                        fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16)
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -452,7 +456,8 @@ def run_ours(args) -> dict:
         g = stack.capture(lambda j=j: stack.gemm_only(j))
         ms = time_graph(torch, g, reps=max(3, args.steps // 2))
         us = ms * 1e3 / stack.layers
-        b = algorithmic_bytes(args.m, lin.n, lin.k)["gemm"]
+        io = 2 if stack.bf16 else 4
+        b = algorithmic_bytes(args.m, lin.n, lin.k, io, io)["gemm"]
         gbs = b / (us * 1e-6) / 1e9
         per_linear[lin.name] = {"n": lin.n, "k": lin.k, "us_per_call": round(us, 3),
                                 "kernel": nv.KERNEL_NAMES.get(stack.chosen(lin)),
@@ -464,7 +469,9 @@ def run_ours(args) -> dict:
     e2e = run_e2e(torch, stack, step_graph, args)
     sweep_detail = None if args.no_sweep else sweep(nv, torch, stack, peaks, args)
 
-    traffic = profile_traffic("gemm_smallm")
+    # the committed capture is of the default step (M = 1, FP32 I/O, two launches)
+    default_step = args.m == 1 and not args.bf16 and not args.fused and args.kernel == "auto"
+    traffic = profile_traffic("gemm_smallm") if default_step else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4),
@@ -478,7 +485,8 @@ def run_ours(args) -> dict:
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "graph": "one CUDA graph per step",
                    "pdl": not args.no_pdl,
-                   "fused_quantize": args.fused},
+                   "fused_quantize": args.fused,
+                   "io": "bf16 X in, bf16 Y out" if args.bf16 else "fp32 X in, fp32 Y out"},
         "roofline": {"bound": "hbm", "kernel": "nvfp4_gemm_smallm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
@@ -505,9 +513,9 @@ def run_e2e(torch, stack, step_graph, args) -> dict:
     same graph of C-ABI calls) and reads all of its outputs back to pinned host
     memory -- both copies inside the timed region."""
     x_host = stack.x_flat.cpu().pin_memory()
-    y_host = torch.empty(stack.y_flat.shape, dtype=torch.float32).pin_memory()
-    h2d = x_host.numel() * 4
-    d2h = y_host.numel() * 4
+    y_host = torch.empty(stack.y_flat.shape, dtype=stack.y_flat.dtype).pin_memory()
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size()
 
     def one_step():
         stack.x_flat.copy_(x_host, non_blocking=True)
@@ -568,13 +576,13 @@ def kernel_source_hash() -> str:
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(rows_per_linear: int, seed: int = 99, layers: int = 1):
+def oracle_sample(rows_per_linear: int, seed: int = 99, layers: int = 1, first_layer: int = 0):
     """Packed operands for a bounded sample of the workload: the four linears
-    of ``layers`` layers (distinct seeded weights), ``rows_per_linear`` output
-    rows each (packing not timed)."""
+    of ``layers`` layers from ``first_layer`` on (distinct seeded weights),
+    ``rows_per_linear`` output rows each (packing not timed)."""
     import oracle
     items = []
-    for l in range(layers):
+    for l in range(first_layer, first_layer + layers):
         for j, lin in enumerate(synthetic.LINEARS_8B):
             rows = min(rows_per_linear, lin.n)
             s = synthetic.weight_seed(seed, l, j)
@@ -620,8 +628,18 @@ def calibrate_sample(budget_s: float):
 
 
 def cpu_baseline(budget_s: float = 12.0) -> dict:
+    """The oracle on the host: a bounded sample of the step sized to about
+    ``budget_s`` seconds.  When whole layers fit, one layer is timed first
+    (untimed warm-up of the sample) to fix how many layers the budget holds."""
     rows, layers = calibrate_sample(budget_s)
-    items = oracle_sample(rows, layers=layers)
+    items = oracle_sample(rows, layers=1)
+    if rows >= max(lin.n for lin in synthetic.LINEARS_8B):
+        t0 = time.perf_counter()
+        oracle_pass(items)
+        one = max(time.perf_counter() - t0, 1e-3)
+        layers = int(min(36, max(1, round(budget_s / one))))
+        if layers > 1:
+            items += oracle_sample(rows, layers=layers - 1, first_layer=1)
     t0 = time.perf_counter()
     oracle_pass(items)
     sec = time.perf_counter() - t0
@@ -735,6 +753,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="host seconds per reference step (default: ~150 s over the run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16", action="store_true",
+                    help="BF16 activations in and BF16 outputs out (FP32 otherwise)")
     ap.add_argument("--fused", action="store_true",
                     help="one kernel per linear (quantisation in the GEMM prologue) instead of "
                          "quantiser + GEMM")

@@ -153,6 +153,13 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       wait runs out (after a few microseconds) and the
  *                       kernel records NVFP4_DEVICE_WAIT_TIMEOUT; Y is left
  *                       unspecified.  For testing the timeout path only.
+ * NVFP4_FLAG_X_BF16     (activation quantisation, linear) X is BF16 (raw
+ *                       bits, uint16 [m][k], 8-byte aligned) instead of FP32;
+ *                       each value is widened to FP32 exactly and quantised by
+ *                       the same recipe, so the codes equal those of the FP32
+ *                       copy of X.
+ * NVFP4_FLAG_Y_BF16     (GEMM, linear) Y is BF16 (uint16 [m][n], 2-byte
+ *                       aligned): the FP32 result rounded to nearest even.
  * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
  *                       while the previous kernel on the stream is still
  *                       running and waits for it before it touches anything
@@ -170,6 +177,8 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_KERNEL_MASK 0xFFu
 #define NVFP4_FLAG_PDL 0x100u
 #define NVFP4_FLAG_FUSED_QUANTIZE 0x200u
+#define NVFP4_FLAG_X_BF16 0x400u
+#define NVFP4_FLAG_Y_BF16 0x800u
 #define NVFP4_FLAG_TEST_WAIT_TIMEOUT 0x10000u
 
 /* Bits of the device status word (nvfp4_device_status). */
@@ -186,15 +195,17 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 int nvfp4_quantize_act_dynamic(const float* x, int64_t m, int64_t k, float* x_g,
                                uint8_t* x_q, uint8_t* x_s, void* stream);
 
-/* nvfp4_quantize_act with options (only NVFP4_FLAG_PDL is meaningful). */
-int nvfp4_quantize_act_ex(const float* x, int64_t m, int64_t k, const float* x_g,
+/* nvfp4_quantize_act with options: NVFP4_FLAG_PDL, NVFP4_FLAG_X_BF16 (x is
+ * then BF16, see above). */
+int nvfp4_quantize_act_ex(const void* x, int64_t m, int64_t k, const float* x_g,
                           uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream);
 
 /* nvfp4_gemm_smallm with a kernel choice and flags (see above).  Same
- * arguments, same result up to FP32 rounding order. */
+ * arguments, same result up to FP32 rounding order; y is FP32, or BF16 with
+ * NVFP4_FLAG_Y_BF16. */
 int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
                          const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
-                         float* y, int64_t m, int64_t n, int64_t k,
+                         void* y, int64_t m, int64_t n, int64_t k,
                          uint32_t options, void* stream);
 
 /*
@@ -232,7 +243,7 @@ int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t opti
 /* nvfp4_gemm_smallm_ex with a workspace (NULL with 0 bytes for none). */
 int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
                          const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
-                         float* y, int64_t m, int64_t n, int64_t k, uint32_t options,
+                         void* y, int64_t m, int64_t n, int64_t k, uint32_t options,
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
@@ -247,7 +258,8 @@ int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_
  * zero when the library loads and every completed call leaves them zero).
  * Nothing is allocated or freed.
  *   options   NVFP4_KERNEL_AUTO or NVFP4_KERNEL_SPLITK, optionally
- *             NVFP4_FLAG_PDL (anything else: NVFP4_ERR_INVALID_ARG)
+ *             NVFP4_FLAG_PDL and NVFP4_FLAG_Y_BF16 (anything else:
+ *             NVFP4_ERR_INVALID_ARG)
  * Returns NVFP4_ERR_UNSUPPORTED, launching nothing, when the shape is not
  * one the split-K kernel takes, the operands are not aligned for it, or the
  * scratch the call needs exceeds the static array.  All calls on a device
@@ -257,7 +269,7 @@ int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_
  */
 int nvfp4_gemm_smallm_static(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
                              const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
-                             float* y, int64_t m, int64_t n, int64_t k, uint32_t options,
+                             void* y, int64_t m, int64_t n, int64_t k, uint32_t options,
                              void* stream);
 
 /* Bytes of the static scratch array behind nvfp4_gemm_smallm_static. */
@@ -284,9 +296,11 @@ int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x
                  const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
                  uint8_t* x_q, uint8_t* x_s, uint32_t options, void* stream);
 
-/* nvfp4_linear with a workspace for the GEMM (as nvfp4_gemm_smallm_ws). */
-int nvfp4_linear_ws(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
-                    const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+/* nvfp4_linear with a workspace for the GEMM (as nvfp4_gemm_smallm_ws) and
+ * the dtype flags: NVFP4_FLAG_X_BF16 (x is BF16; the fused one-kernel form is
+ * then not used) and NVFP4_FLAG_Y_BF16 (y is BF16). */
+int nvfp4_linear_ws(const void* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                    const uint8_t* w_q, const uint8_t* w_s, const float* w_g, void* y,
                     uint8_t* x_q, uint8_t* x_s, uint32_t options, void* workspace,
                     size_t workspace_bytes, void* stream);
 

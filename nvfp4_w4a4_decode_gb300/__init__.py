@@ -68,6 +68,8 @@ KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma
                 KERNEL_TMA: "tma", KERNEL_SPLITK: "splitk"}
 FLAG_PDL = 0x100
 FLAG_FUSED_QUANTIZE = 0x200
+FLAG_X_BF16 = 0x400
+FLAG_Y_BF16 = 0x800
 FLAG_TEST_WAIT_TIMEOUT = 0x10000
 DEVICE_WAIT_TIMEOUT = 1
 
@@ -135,9 +137,29 @@ def nvfp4_pack_weight(w: torch.Tensor):
     return wq, ws, wg
 
 
-def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None, pdl: bool = False):
-    """Quantise X[m, k] with tensor scale xg -> (x_q [m, k/2], x_s [m, k/16])."""
+def _x_flag(x: torch.Tensor) -> int:
+    """The dtype flag of an activation tensor (FP32 or BF16)."""
+    if x.dtype == torch.bfloat16:
+        _dev(x, torch.bfloat16, "x")
+        return FLAG_X_BF16
     _dev(x, torch.float32, "x")
+    return 0
+
+
+def _y_out(out, m: int, n: int, dtype, device):
+    """The output tensor and its dtype flag (FP32 or BF16)."""
+    if out is None:
+        out = torch.empty((m, n), dtype=dtype, device=device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"output must be float32 or bfloat16, got {out.dtype}")
+    _dev(out, out.dtype, "out")
+    return out, (FLAG_Y_BF16 if out.dtype == torch.bfloat16 else 0)
+
+
+def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None, pdl: bool = False):
+    """Quantise X[m, k] (float32 or bfloat16) with tensor scale xg ->
+    (x_q [m, k/2], x_s [m, k/16])."""
+    xflag = _x_flag(x)
     _dev(xg, torch.float32, "xg")
     m, k = x.shape
     if out is None:
@@ -147,7 +169,7 @@ def nvfp4_quantize_act(x: torch.Tensor, xg: torch.Tensor, out=None, pdl: bool = 
         xq, xs = out
     _check("nvfp4_quantize_act", library().nvfp4_quantize_act_ex(
         x.data_ptr(), m, k, xg.data_ptr(), xq.data_ptr(), xs.data_ptr(),
-        FLAG_PDL if pdl else 0, _stream(x)))
+        (FLAG_PDL if pdl else 0) | xflag, _stream(x)))
     return xq, xs
 
 
@@ -200,14 +222,16 @@ def _ws_args(workspace, m, n, k, kernel, device):
 def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
                       kernel: int = KERNEL_AUTO, pdl: bool = False,
                       test_wait_timeout: bool = False,
-                      workspace: torch.Tensor | None = None) -> torch.Tensor:
+                      workspace: torch.Tensor | None = None,
+                      out_dtype=torch.float32) -> torch.Tensor:
     """Y[m, n] = dequant(X) . dequant(W)^T for m <= 8, float32.
 
     ``kernel`` forces one kernel (KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA,
     KERNEL_TMA, KERNEL_SPLITK); ``pdl`` lets the launch overlap the previous
     kernel (weights must not be written by it); ``workspace`` (from
     ``nvfp4_workspace``) is made per call when the kernel needs one and none
-    is given."""
+    is given.  The output is float32, or bfloat16 (``out_dtype`` or the dtype
+    of ``out``): the float32 result rounded to nearest even."""
     for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
         _dev(t, torch.uint8, name)
     _dev(xg, torch.float32, "xg")
@@ -217,8 +241,9 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
     k = kh * 2
     if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
         raise ValueError("operand shapes disagree")
-    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    y, yflag = _y_out(out, m, n, out_dtype, xq.device)
     opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0)
+    opts |= yflag
     wp, wn, _keep = _ws_args(workspace, m, n, k, kernel, xq.device)
     _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm_ws(
         xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
@@ -227,7 +252,7 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
 
 
 def nvfp4_gemm_smallm_static(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
-                             pdl: bool = False) -> torch.Tensor:
+                             pdl: bool = False, out_dtype=torch.float32) -> torch.Tensor:
     """The split-K GEMM on the library's static scratch array (no workspace,
     no allocation in the library): same result bits as ``nvfp4_gemm_smallm``
     with KERNEL_SPLITK and a full workspace.  Calls that may overlap in time
@@ -241,10 +266,10 @@ def nvfp4_gemm_smallm_static(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = 
     k = kh * 2
     if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
         raise ValueError("operand shapes disagree")
-    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    y, yflag = _y_out(out, m, n, out_dtype, xq.device)
     _check("nvfp4_gemm_smallm_static", library().nvfp4_gemm_smallm_static(
         xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
-        wg.data_ptr(), y.data_ptr(), m, n, k, KERNEL_SPLITK | (FLAG_PDL if pdl else 0),
+        wg.data_ptr(), y.data_ptr(), m, n, k, KERNEL_SPLITK | (FLAG_PDL if pdl else 0) | yflag,
         _stream(xq)))
     return y
 
@@ -266,12 +291,14 @@ def nvfp4_device_status(clear: bool = True, stream=None) -> int:
 
 def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=None,
                  kernel: int = KERNEL_AUTO, pdl: bool = False,
-                 fused: bool = False, workspace: torch.Tensor | None = None) -> torch.Tensor:
+                 fused: bool = False, workspace: torch.Tensor | None = None,
+                 out_dtype=torch.float32) -> torch.Tensor:
     """One W4A4 decode linear: quantise X[m, k] on the fly and multiply by the
     packed W[n, k].  ``fused`` asks for one kernel (where the CUDA-core stream
     takes the shape); ``x_out`` = (x_q, x_s) receive the quantised activations;
-    ``workspace`` as in ``nvfp4_gemm_smallm``."""
-    _dev(x, torch.float32, "x")
+    ``workspace`` as in ``nvfp4_gemm_smallm``.  X may be float32 or bfloat16;
+    the output is float32 or bfloat16 (``out_dtype`` or the dtype of ``out``)."""
+    xflag = _x_flag(x)
     for t, name in ((wq, "wq"), (ws, "ws")):
         _dev(t, torch.uint8, name)
     _dev(xg, torch.float32, "xg")
@@ -285,8 +312,9 @@ def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=
         xs = torch.empty((m, k // 16), dtype=torch.uint8, device=x.device)
     else:
         xq, xs = x_out
-    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
+    y, yflag = _y_out(out, m, n, out_dtype, x.device)
     opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_FUSED_QUANTIZE if fused else 0)
+    opts |= xflag | yflag
     wp, wn, _keep = _ws_args(workspace, m, n, k, kernel, x.device)
     _check("nvfp4_linear", library().nvfp4_linear_ws(
         x.data_ptr(), m, n, k, xg.data_ptr(), wq.data_ptr(), ws.data_ptr(), wg.data_ptr(),

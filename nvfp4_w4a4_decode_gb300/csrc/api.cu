@@ -62,21 +62,24 @@ int nvfp4_pack_weight(const float* w, int64_t n, int64_t k, uint8_t* w_q, uint8_
     cudaError_t e = nvfp4::launch_global_scale(w, empty ? 0 : n * k, w_g, s);
     if (e != cudaSuccess || empty)
         return from_cuda(e);
-    return from_cuda(nvfp4::launch_quantize(w, n, k, w_g, w_q, w_s, s));
+    return from_cuda(nvfp4::launch_quantize(w, false, n, k, w_g, w_q, w_s, s));
 }
 
-int nvfp4_quantize_act_ex(const float* x, int64_t m, int64_t k, const float* x_g, uint8_t* x_q,
+int nvfp4_quantize_act_ex(const void* x, int64_t m, int64_t k, const float* x_g, uint8_t* x_q,
                           uint8_t* x_s, uint32_t options, void* stream)
 {
-    if (m < 0 || k < 0 || (k % 16) != 0 || (options & ~(uint32_t)NVFP4_FLAG_PDL) != 0)
+    if (m < 0 || k < 0 || (k % 16) != 0 ||
+        (options & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_X_BF16)) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if (m == 0 || k == 0)
         return NVFP4_OK;
     if (x == nullptr || x_g == nullptr || x_q == nullptr || x_s == nullptr)
         return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(x_q, 8) || !aligned(x_g, 4))
+    const bool bf16 = (options & NVFP4_FLAG_X_BF16) != 0;
+    if (!aligned(x, bf16 ? 8 : 16) || !aligned(x_q, 8) || !aligned(x_g, 4))
         return NVFP4_ERR_INVALID_ARG;
-    return from_cuda(nvfp4::launch_quantize(x, m, k, x_g, x_q, x_s, static_cast<cudaStream_t>(stream),
+    return from_cuda(nvfp4::launch_quantize(x, bf16, m, k, x_g, x_q, x_s,
+                                            static_cast<cudaStream_t>(stream),
                                             (options & NVFP4_FLAG_PDL) != 0));
 }
 
@@ -144,7 +147,7 @@ int check_gemm_args(int64_t m, int64_t n, int64_t k, uint32_t options)
 {
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
         return NVFP4_ERR_INVALID_ARG;
-    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL |
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 |
                                NVFP4_FLAG_TEST_WAIT_TIMEOUT)) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if ((options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) && (options & NVFP4_KERNEL_MASK) != NVFP4_KERNEL_TMA)
@@ -155,7 +158,7 @@ int check_gemm_args(int64_t m, int64_t n, int64_t k, uint32_t options)
 }
 
 int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t* w_q,
-         const uint8_t* w_s, const float* w_g, float* y, int64_t m, int64_t n, int64_t k,
+         const uint8_t* w_s, const float* w_g, void* y, int64_t m, int64_t n, int64_t k,
          uint32_t options, void* workspace, size_t workspace_bytes, void* stream)
 {
     const int chk = check_gemm_args(m, n, k, options);
@@ -166,10 +169,12 @@ int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t
     if (m == 0 || n == 0)
         return NVFP4_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (y == nullptr || !aligned(y, 4))
+    const bool y_bf16 = (options & NVFP4_FLAG_Y_BF16) != 0;
+    const size_t y_elem = y_bf16 ? 2 : 4;
+    if (y == nullptr || !aligned(y, y_elem))
         return NVFP4_ERR_INVALID_ARG;
     if (k == 0)
-        return from_cuda(cudaMemsetAsync(y, 0, sizeof(float) * (size_t)(m * n), s));
+        return from_cuda(cudaMemsetAsync(y, 0, y_elem * (size_t)(m * n), s));
     if (x_q == nullptr || x_s == nullptr || x_g == nullptr || w_q == nullptr || w_s == nullptr ||
         w_g == nullptr)
         return NVFP4_ERR_INVALID_ARG;
@@ -183,7 +188,7 @@ int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t
     if (kern < 0)
         return -kern;
     const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
-    const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k, s};
+    const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, {y, y_bf16 ? 1 : 0}, (int)m, n, k, s};
     switch (kern) {
     case NVFP4_KERNEL_GEMV:
         return from_cuda(nvfp4::launch_gemm_gemv(a, pdl));
@@ -228,14 +233,14 @@ int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t opti
 }
 
 int nvfp4_gemm_smallm_ex(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
-                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, void* y,
                          int64_t m, int64_t n, int64_t k, uint32_t options, void* stream)
 {
     return gemm(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, nullptr, 0, stream);
 }
 
 int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
-                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                         const uint8_t* w_q, const uint8_t* w_s, const float* w_g, void* y,
                          int64_t m, int64_t n, int64_t k, uint32_t options, void* workspace,
                          size_t workspace_bytes, void* stream)
 {
@@ -243,14 +248,15 @@ int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_
                 stream);
 }
 
-int nvfp4_linear_ws(const float* x, int64_t m, int64_t n, int64_t k, const float* x_g,
-                    const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+int nvfp4_linear_ws(const void* x, int64_t m, int64_t n, int64_t k, const float* x_g,
+                    const uint8_t* w_q, const uint8_t* w_s, const float* w_g, void* y,
                     uint8_t* x_q, uint8_t* x_s, uint32_t options, void* workspace,
                     size_t workspace_bytes, void* stream)
 {
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
         return NVFP4_ERR_INVALID_ARG;
-    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_FUSED_QUANTIZE)) != 0)
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_FUSED_QUANTIZE |
+                               NVFP4_FLAG_X_BF16 | NVFP4_FLAG_Y_BF16)) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if (m > 8)
         return NVFP4_ERR_UNSUPPORTED;
@@ -258,15 +264,18 @@ int nvfp4_linear_ws(const float* x, int64_t m, int64_t n, int64_t k, const float
         return NVFP4_ERR_INVALID_ARG;
     if (m == 0 || n == 0)
         return NVFP4_OK;
-    const bool fuse = (options & NVFP4_FLAG_FUSED_QUANTIZE) != 0;
-    options &= ~(uint32_t)NVFP4_FLAG_FUSED_QUANTIZE;
-    if (k > 0 && (x == nullptr || x_q == nullptr || x_s == nullptr || !aligned(x, 16) ||
-                  !aligned(x_q, 8)))
+    const bool x_bf16 = (options & NVFP4_FLAG_X_BF16) != 0;
+    const bool y_bf16 = (options & NVFP4_FLAG_Y_BF16) != 0;
+    // the fused prologue reads FP32 activations: BF16 input takes two launches
+    const bool fuse = (options & NVFP4_FLAG_FUSED_QUANTIZE) != 0 && !x_bf16;
+    options &= ~(uint32_t)(NVFP4_FLAG_FUSED_QUANTIZE | NVFP4_FLAG_X_BF16);
+    if (k > 0 && (x == nullptr || x_q == nullptr || x_s == nullptr ||
+                  !aligned(x, x_bf16 ? 8 : 16) || !aligned(x_q, 8)))
         return NVFP4_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
     if (fuse && k > 0 && w_q != nullptr && w_s != nullptr && w_g != nullptr && x_g != nullptr &&
-        y != nullptr && aligned(y, 4) && aligned(x_g, 4) && aligned(w_g, 4)) {
+        y != nullptr && aligned(y, y_bf16 ? 2 : 4) && aligned(x_g, 4) && aligned(w_g, 4)) {
         const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
                                aligned(w_s, 4);
         const bool tma_ptrs = fast_ptrs && aligned(x_s, 32) && aligned(w_s, 32);
@@ -275,12 +284,15 @@ int nvfp4_linear_ws(const float* x, int64_t m, int64_t n, int64_t k, const float
         if (kern < 0)
             return -kern;
         if (kern == (int)NVFP4_KERNEL_GEMV) {
-            const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k, s};
-            const nvfp4::FusedAct fa = {x, x_q, x_s};
+            const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, {y, y_bf16 ? 1 : 0},
+                                       (int)m, n, k, s};
+            const nvfp4::FusedAct fa = {static_cast<const float*>(x), x_q, x_s};
             return from_cuda(nvfp4::launch_gemm_gemv(a, pdl, &fa));
         }
     }
-    const int st = nvfp4_quantize_act_ex(x, m, k, x_g, x_q, x_s, pdl ? NVFP4_FLAG_PDL : 0u, stream);
+    const int st = nvfp4_quantize_act_ex(
+        x, m, k, x_g, x_q, x_s, (pdl ? NVFP4_FLAG_PDL : 0u) | (x_bf16 ? NVFP4_FLAG_X_BF16 : 0u),
+        stream);
     if (st != NVFP4_OK)
         return st;
     return gemm(x_q, x_s, x_g, w_q, w_s, w_g, y, m, n, k, options, workspace, workspace_bytes,
@@ -296,14 +308,15 @@ int nvfp4_linear(const float* x, int64_t m, int64_t n, int64_t k, const float* x
 }
 
 int nvfp4_gemm_smallm_static(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
-                             const uint8_t* w_q, const uint8_t* w_s, const float* w_g, float* y,
+                             const uint8_t* w_q, const uint8_t* w_s, const float* w_g, void* y,
                              int64_t m, int64_t n, int64_t k, uint32_t options, void* stream)
 {
     const uint32_t req = options & NVFP4_KERNEL_MASK;
     if (req != NVFP4_KERNEL_AUTO && req != NVFP4_KERNEL_SPLITK)
         return NVFP4_ERR_INVALID_ARG;
-    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL)) != 0)
+    if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16)) != 0)
         return NVFP4_ERR_INVALID_ARG;
+    const bool y_bf16 = (options & NVFP4_FLAG_Y_BF16) != 0;
     const int chk = check_gemm_args(m, n, k, options);
     if (chk != NVFP4_OK)
         return chk;
@@ -312,13 +325,13 @@ int nvfp4_gemm_smallm_static(const uint8_t* x_q, const uint8_t* x_s, const float
     if (y == nullptr || x_q == nullptr || x_s == nullptr || x_g == nullptr || w_q == nullptr ||
         w_s == nullptr || w_g == nullptr)
         return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(y, 4) || !aligned(x_g, 4) || !aligned(w_g, 4))
+    if (!aligned(y, y_bf16 ? 2 : 4) || !aligned(x_g, 4) || !aligned(w_g, 4))
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x_q, 32) || !aligned(w_q, 32) || !aligned(x_s, 4) || !aligned(w_s, 4))
         return NVFP4_ERR_UNSUPPORTED;
     if (!nvfp4::splitk_shape_ok(m, k) || !nvfp4::splitk_static_fits(m, n, k))
         return NVFP4_ERR_UNSUPPORTED;
-    const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, y, (int)m, n, k,
+    const nvfp4::GemmArgs a = {x_q, x_s, x_g, w_q, w_s, w_g, {y, y_bf16 ? 1 : 0}, (int)m, n, k,
                                static_cast<cudaStream_t>(stream)};
     return from_cuda(nvfp4::launch_gemm_splitk_static(a, (options & NVFP4_FLAG_PDL) != 0));
 }

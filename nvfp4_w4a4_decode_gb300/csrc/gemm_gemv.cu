@@ -61,7 +61,7 @@ struct GemvParams {
     const uint8_t* wq;
     const uint8_t* ws;
     const float* wg;
-    float* y;
+    OutY y;
     int64_t n;
     int64_t k;
     int G;  // threads per row
@@ -201,17 +201,34 @@ __global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
         const int64_t left = valid_iters - (base + STAGES);  // refills still in range
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
-            // decode the stage first, then refill its registers (refilling
-            // first would need a copy of the stage's old contents)
+            // M = 1 with 8 stages: decode the stage first, then refill its
+            // registers (refilling first needs a copy of the stage's old
+            // contents); the variants tighter on registers (M = 2, 4 stages
+            // for 1024-thread CTAs) refill first, which measured faster there
             uint32_t wh[16];
-            e2m1x8_to_f16(rw[s].x, *reinterpret_cast<uint32_t(*)[4]>(&wh[0]));
-            e2m1x8_to_f16(rw[s].y, *reinterpret_cast<uint32_t(*)[4]>(&wh[4]));
-            e2m1x8_to_f16(rw[s].z, *reinterpret_cast<uint32_t(*)[4]>(&wh[8]));
-            e2m1x8_to_f16(rw[s].w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
-            const float2 sw = e4m3x2_to_float2(rs[s]);
-            if (s < left) {
-                rw[s] = ld_stream_u4(wn + s * wstep);
-                rs[s] = ld_u16_nc(sn + s * sstep);
+            float2 sw;
+            if constexpr (STAGES == 8 && M == 1) {
+                e2m1x8_to_f16(rw[s].x, *reinterpret_cast<uint32_t(*)[4]>(&wh[0]));
+                e2m1x8_to_f16(rw[s].y, *reinterpret_cast<uint32_t(*)[4]>(&wh[4]));
+                e2m1x8_to_f16(rw[s].z, *reinterpret_cast<uint32_t(*)[4]>(&wh[8]));
+                e2m1x8_to_f16(rw[s].w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
+                sw = e4m3x2_to_float2(rs[s]);
+                if (s < left) {
+                    rw[s] = ld_stream_u4(wn + s * wstep);
+                    rs[s] = ld_u16_nc(sn + s * sstep);
+                }
+            } else {
+                const uint4 cw = rw[s];
+                const uint32_t cs = rs[s];
+                if (s < left) {
+                    rw[s] = ld_stream_u4(wn + s * wstep);
+                    rs[s] = ld_u16_nc(sn + s * sstep);
+                }
+                e2m1x8_to_f16(cw.x, *reinterpret_cast<uint32_t(*)[4]>(&wh[0]));
+                e2m1x8_to_f16(cw.y, *reinterpret_cast<uint32_t(*)[4]>(&wh[4]));
+                e2m1x8_to_f16(cw.z, *reinterpret_cast<uint32_t(*)[4]>(&wh[8]));
+                e2m1x8_to_f16(cw.w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
+                sw = e4m3x2_to_float2(cs);
             }
 #pragma unroll
             for (int m = 0; m < M; ++m) {
@@ -268,7 +285,7 @@ __global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
             const int64_t it = base + s;
             const int64_t r = ((int64_t)blockIdx.x + it * C) * P + pp;
             if (it < iters && r < n)
-                prm.y[m * n + r] = sum * gxw;
+                store_y(prm.y, m * n + r, sum * gxw);
         }
         buf ^= 1;  // the next block writes the other buffer; one barrier per block suffices
     }

@@ -19,7 +19,7 @@ template <int M>
 __global__ void __launch_bounds__(256) gemm_generic_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, const float* __restrict__ xg,
     const uint8_t* __restrict__ wq, const uint8_t* __restrict__ ws, const float* __restrict__ wg,
-    float* __restrict__ y, int64_t n, int64_t k)
+    const OutY y, int64_t n, int64_t k)
 {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(
         const float gxw = __fmul_rn(__ldg(xg), __ldg(wg));
 #pragma unroll
         for (int m = 0; m < M; ++m)
-            y[m * n + row] = acc[m] * gxw;
+            store_y(y, m * n + row, acc[m] * gxw);
     }
 }
 

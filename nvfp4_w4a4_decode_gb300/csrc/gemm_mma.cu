@@ -49,7 +49,7 @@ struct MmaParams {
     const uint8_t* wq;
     const uint8_t* ws;
     const float* wg;
-    float* y;
+    OutY y;
     int m;
     int64_t n;
     int64_t k;
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(512, 2) mma_kernel(const MmaParams prm)
                         float sum = 0.0f;
                         for (int w = 0; w < NW; ++w)
                             sum += src[(size_t)w * 128];
-                        prm.y[(int64_t)col * n + r] = sum * gxw;
+                        store_y(prm.y, (int64_t)col * n + r, sum * gxw);
                     }
                     if (lane == 0)
                         s_count[ts] = 0u;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(512, 2) mma_kernel(const MmaParams prm)
                 const int it = base + tp;
                 const int r = rowA0 - g + it * tile_rows + row;
                 if (col < M && it < niters && r < nrows)
-                    prm.y[(int64_t)col * n + r] = sum * gxw;
+                    store_y(prm.y, (int64_t)col * n + r, sum * gxw);
             } else {
                 part[buf][tp][v] = sum;
             }
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(512, 2) mma_kernel(const MmaParams prm)
                 const int it = base + tp;
                 const int r = rowA0 - g + it * tile_rows + row;
                 if (col < M && it < niters && r < nrows)
-                    prm.y[(int64_t)col * n + r] = sum * gxw;
+                    store_y(prm.y, (int64_t)col * n + r, sum * gxw);
             }
         }
         buf ^= 1;

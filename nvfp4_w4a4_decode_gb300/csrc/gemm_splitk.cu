@@ -84,7 +84,7 @@ struct SplitkParams {
     const uint8_t* wq;
     const uint8_t* ws;
     const float* wg;
-    float* y;
+    OutY y;
     float4* part;     // [tiles][nchunks][32 lanes] partial tiles (nchunks > 1)
     unsigned* count;  // [tiles] partials stored so far; zero between calls
     int m;
@@ -319,15 +319,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
         const int c0 = 2 * t, c1 = c0 + 1;
         if (c0 < M) {
             if (r0 < n)
-                prm.y[c0 * n + r0] = v0 * gxw;
+                store_y(prm.y, c0 * n + r0, v0 * gxw);
             if (r1 < n)
-                prm.y[c0 * n + r1] = v2 * gxw;
+                store_y(prm.y, c0 * n + r1, v2 * gxw);
         }
         if (c1 < M) {
             if (r0 < n)
-                prm.y[c1 * n + r0] = v1 * gxw;
+                store_y(prm.y, c1 * n + r0, v1 * gxw);
             if (r1 < n)
-                prm.y[c1 * n + r1] = v3 * gxw;
+                store_y(prm.y, c1 * n + r1, v3 * gxw);
         }
     };
 

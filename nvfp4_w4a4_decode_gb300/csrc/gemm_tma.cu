@@ -47,7 +47,7 @@ struct TmaParams {
     const uint8_t* wq;
     const uint8_t* ws;
     const float* wg;
-    float* y;
+    OutY y;
     int m;
     int n;
     int64_t k;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(544, 1) tma_kernel(const TmaParams prm)
             const int row = (lv >> 2) + 8 * (j >> 1), col = 2 * (lv & 3) + (j & 1);
             const int r = row0 + row;
             if (col < M && r < n && !s_abort)
-                prm.y[(int64_t)col * n + r] = sum * gxw;
+                store_y(prm.y, (int64_t)col * n + r, sum * gxw);
         }
     }
     if (nsplit > 1)

@@ -2,10 +2,26 @@
 // the library (the C ABI in api.cu calls these).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace nvfp4 {
+
+// Output of a GEMM: FP32, or BF16 rounded to nearest even from the same FP32
+// value.
+struct OutY {
+    void* p;
+    int bf16;
+};
+
+__device__ __forceinline__ void store_y(const OutY& y, int64_t i, float v)
+{
+    if (y.bf16)
+        reinterpret_cast<__nv_bfloat16*>(y.p)[i] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float*>(y.p)[i] = v;
+}
 
 struct GemmArgs {
     const uint8_t* xq;
@@ -14,7 +30,7 @@ struct GemmArgs {
     const uint8_t* wq;
     const uint8_t* ws;
     const float* wg;
-    float* y;
+    OutY y;
     int m;
     int64_t n;
     int64_t k;
@@ -23,7 +39,8 @@ struct GemmArgs {
 
 cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStream_t stream);
 
-cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float* g,
+// t is FP32, or BF16 when t_bf16 (converted exactly before quantising).
+cudaError_t launch_quantize(const void* t, bool t_bf16, int64_t rows, int64_t k, const float* g,
                             uint8_t* q, uint8_t* s, cudaStream_t stream, bool pdl = false);
 
 // Any shape with k % 16 == 0 and 8-byte aligned code rows.

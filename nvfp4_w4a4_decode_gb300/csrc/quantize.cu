@@ -49,9 +49,10 @@ __global__ void finalize_scale_kernel(float* g)
 // two 32-bit words.  Blocks are numbered row-major, so a warp reads 512
 // contiguous bytes of t and writes 64 contiguous code bytes.  With
 // programmatic dependent launch the kernel lets the next kernel (the GEMM)
-// launch at once, then waits for the producer of t.
-template <bool PDL>
-__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ t, int64_t nblocks,
+// launch at once, then waits for the producer of t.  BF16 input is widened
+// to FP32 exactly (a BF16 value is the top half of its FP32 bits).
+template <bool PDL, bool BF16>
+__global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ t, int64_t nblocks,
                                                        const float* __restrict__ g_ptr,
                                                        uint8_t* __restrict__ q,
                                                        uint8_t* __restrict__ s)
@@ -66,8 +67,15 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
     const bool valid = b < nblocks;
 
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid)
-        v = __ldg(reinterpret_cast<const float4*>(t) + tid);
+    if (valid) {
+        if constexpr (BF16) {
+            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(t) + tid);  // 4 BF16, first low
+            v = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                            __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+        } else {
+            v = __ldg(reinterpret_cast<const float4*>(t) + tid);
+        }
+    }
     float bmax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
     bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 2));
@@ -110,15 +118,13 @@ cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStr
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float* g,
-                            uint8_t* q, uint8_t* s, cudaStream_t stream, bool pdl)
+template <bool BF16>
+cudaError_t launch_quantize_t(const void* t, int64_t nblocks, const float* g, uint8_t* q,
+                              uint8_t* s, cudaStream_t stream, bool pdl)
 {
-    const int64_t nblocks = rows * (k / 16);
-    if (nblocks == 0)
-        return cudaSuccess;
     const int64_t grid = (4 * nblocks + 255) / 256;
     if (!pdl) {
-        quantize_kernel<false><<<(unsigned)grid, 256, 0, stream>>>(t, nblocks, g, q, s);
+        quantize_kernel<false, BF16><<<(unsigned)grid, 256, 0, stream>>>(t, nblocks, g, q, s);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -130,7 +136,17 @@ cudaError_t launch_quantize(const float* t, int64_t rows, int64_t k, const float
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<true>, t, nblocks, g, q, s);
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<true, BF16>, t, nblocks, g, q, s);
+}
+
+cudaError_t launch_quantize(const void* t, bool t_bf16, int64_t rows, int64_t k, const float* g,
+                            uint8_t* q, uint8_t* s, cudaStream_t stream, bool pdl)
+{
+    const int64_t nblocks = rows * (k / 16);
+    if (nblocks == 0)
+        return cudaSuccess;
+    return t_bf16 ? launch_quantize_t<true>(t, nblocks, g, q, s, stream, pdl)
+                  : launch_quantize_t<false>(t, nblocks, g, q, s, stream, pdl);
 }
 
 }  // namespace nvfp4

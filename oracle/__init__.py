@@ -35,6 +35,7 @@ _u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
 _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 _i64 = ctypes.c_int64
 
 
@@ -81,6 +82,10 @@ def _load():
         lib.oracle_gemm_sampled.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p,
                                             ctypes.c_float, _i64, _i64p, _i64p, _i64, _f64p]
         lib.oracle_gemm_sampled.restype = None
+        lib.oracle_bf16_widen.argtypes = [_u16p, _i64, _f32p]
+        lib.oracle_bf16_widen.restype = None
+        lib.oracle_bf16_round.argtypes = [_f32p, _i64, _u16p]
+        lib.oracle_bf16_round.restype = None
         _lib = lib
         return lib
 
@@ -183,3 +188,22 @@ def gemm_sampled(xq, xs, gx, wq, ws, gw, ms, ns) -> np.ndarray:
     _load().oracle_gemm_sampled(xq, xs, float(np.float32(gx)), wq, ws, float(np.float32(gw)),
                                 k, ms, ns, ms.size, y)
     return y
+
+
+# ---- BF16 (production activation / output dtype) ----------------------------
+
+def bf16_to_f32(bits) -> np.ndarray:
+    """BF16 bit patterns (uint16 array) -> FP32 values, exact."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float32)
+    _load().oracle_bf16_widen(b.reshape(-1), b.size, out.reshape(-1))
+    return out
+
+
+def f32_to_bf16(v) -> np.ndarray:
+    """FP32 values -> BF16 bit patterns, round to nearest, ties to even."""
+    f = _f32(v)
+    out = np.empty(f.shape, dtype=np.uint16)
+    _load().oracle_bf16_round(f.reshape(-1), f.size, out.reshape(-1))
+    return out
+

@@ -255,3 +255,46 @@ void oracle_gemm_sampled(const uint8_t* xq, const uint8_t* xs, float gx,
     for (int64_t t = 0; t < count; ++t)
         y[t] = oracle_gemm_one(xq, xs, gx, wq, ws, gw, k, ms[t], ns[t]);
 }
+
+/* ---- BF16, the production activation and output dtype -------------------
+ * BF16 is the upper half of an IEEE binary32: sign | 8 exponent bits | 7
+ * mantissa bits.  Widening puts the 16 bits on top of 16 zero bits, which is
+ * exact.  Narrowing (finite values below the largest BF16) takes the two
+ * BF16 neighbours of v -- v's upper half (towards zero) and the next BF16
+ * away from zero -- and keeps the nearer one, on an exact tie the one whose
+ * last bit is 0: round-to-nearest-even, again read off the grid. */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    const uint32_t bits = (uint32_t)b << 16;
+    float v;
+    memcpy(&v, &bits, sizeof v);
+    return v;
+}
+
+uint16_t oracle_f32_to_bf16(float v)
+{
+    uint32_t bits;
+    memcpy(&bits, &v, sizeof bits);
+    const uint16_t lo = (uint16_t)(bits >> 16);
+    const uint16_t hi = (uint16_t)(lo + 1);
+    const double d = v;
+    const double elo = fabs(d - (double)oracle_bf16_to_f32(lo));
+    const double ehi = fabs((double)oracle_bf16_to_f32(hi) - d);
+    if (elo < ehi)
+        return lo;
+    if (ehi < elo)
+        return hi;
+    return (lo & 1u) ? hi : lo;
+}
+
+void oracle_bf16_widen(const uint16_t* b, int64_t count, float* out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = oracle_bf16_to_f32(b[i]);
+}
+
+void oracle_bf16_round(const float* v, int64_t count, uint16_t* out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = oracle_f32_to_bf16(v[i]);
+}

@@ -127,7 +127,7 @@ def test_linear_rejects_bad_arguments(lib):
     assert f(FAKE, 1, 16, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 1
     assert f(FAKE + 4, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 1
     assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, None) == 1
-    assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0x400, None) == 1
+    assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0x4000, None) == 1
     assert f(FAKE, 0, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 0
 
 

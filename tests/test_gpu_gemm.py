@@ -498,6 +498,72 @@ def test_splitk_graph_chain_with_pdl(nv):
         np.testing.assert_array_equal(host(outs[j]), eager[j])
 
 
+# ---- BF16 output -----------------------------------------------------------------
+
+# Tolerance of a BF16 output against the oracle's FP64 result: the FP32 result
+# is within GEMM_TOL (relative to max(|ref|, row rms)), and rounding it to BF16
+# (8 significant bits: for |y| in [2^e, 2^(e+1)) the spacing is 2^(e-7), so
+# round to nearest moves y by at most 2^(e-8) <= 2^-8 |y|) adds at most
+# 2^-8 |y|, with |y| <= (1 + GEMM_TOL) max(|ref|, rms).
+GEMM_TOL_BF16 = GEMM_TOL + 2.0 ** -8 * (1 + GEMM_TOL)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("kernel,m,n,k", [("generic", 3, 100, 4112), ("gemv", 1, 333, 4096),
+                                          ("gemv", 2, 64, 12288), ("splitk", 1, 300, 4096),
+                                          ("splitk", 8, 16 * 37 + 5, 4096),
+                                          ("splitk", 4, 200, 25600), ("mma", 5, 300, 5120),
+                                          ("tma", 8, 16 * 70 + 5, 2048)])
+def test_bf16_output_is_rounded_fp32_output(nv, kernel, m, n, k):
+    """Y in BF16 is the same kernel's FP32 Y rounded to nearest even (bit for
+    bit, the oracle's rounding), and within GEMM_TOL_BF16 of the FP64 result."""
+    kid = {"generic": nv.KERNEL_GENERIC, "gemv": nv.KERNEL_GEMV, "splitk": nv.KERNEL_SPLITK,
+           "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA}[kernel]
+    ops, oops = splitk_case(nv, m, n, k, seed=k + 17 * m + n)
+    wsp = nv.workspace(m, n, k, kid) if kid == nv.KERNEL_SPLITK else None
+    y32 = host(nv.gemm_smallm(*ops, kernel=kid, workspace=wsp)).copy()
+    y16 = nv.gemm_smallm(*ops, kernel=kid, workspace=wsp, out_dtype=torch.bfloat16)
+    assert y16.dtype == torch.bfloat16
+    np.testing.assert_array_equal(bf16_bits(y16), oracle.f32_to_bf16(y32))
+    yw = oracle.bf16_to_f32(bf16_bits(y16))
+    assert check_rows(yw, oops, n) <= GEMM_TOL_BF16
+
+
+def test_bf16_static_entry_point(nv):
+    m, n, k = 8, 6144, 4096
+    ops, _ = splitk_case(nv, m, n, k, seed=77)
+    y32 = host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK)).copy()
+    y16 = nv.gemm_smallm_static(*ops, out_dtype=torch.bfloat16)
+    np.testing.assert_array_equal(bf16_bits(y16), oracle.f32_to_bf16(y32))
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 256, 1024), (2, 1000, 4096), (4, 96, 4096), (8, 50, 12288)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_linear_bf16_in_and_out(nv, m, n, k, fused):
+    """BF16 X in, BF16 Y out through nvfp4_linear equals BF16 quantise +
+    GEMM with BF16 output (the fused form falls back to two launches)."""
+    x32 = synthetic.activations(m, k, seed=5 * k + m)
+    bits = oracle.f32_to_bf16(x32)
+    xb = torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    xg = nv.global_scale(torch.from_numpy(oracle.bf16_to_f32(bits)).cuda())
+    w = synthetic.weights(n, k, 0.02, seed=7 * n + k)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    wsp = nv.workspace(m, n, k)
+    y = nv.linear(xb, xg, wq, ws, wg, fused=fused, workspace=wsp, out_dtype=torch.bfloat16)
+    xq, xs = nv.quantize_act(xb, xg)
+    y2 = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, workspace=wsp, out_dtype=torch.bfloat16)
+    np.testing.assert_array_equal(bf16_bits(y), bf16_bits(y2))
+    gx = np.float32(host(xg)[0])
+    oxq, oxs = oracle.quantize(oracle.bf16_to_f32(bits), gx)
+    np.testing.assert_array_equal(host(xq), oxq)
+    owq, ows, ogw = oracle.pack_weight(w)
+    ref = oracle.gemm(oxq, oxs, gx, owq, ows, ogw)
+    assert gemm_error(oracle.bf16_to_f32(bf16_bits(y)), ref) <= GEMM_TOL_BF16
+
+
 # ---- fused quantise + GEMM (nvfp4_linear) --------------------------------------
 
 LINEAR_SHAPES = [(1, 256, 1024), (2, 1000, 4096), (1, 16 * 37 + 5, 4096), (2, 77, 12288),

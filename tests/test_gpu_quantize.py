@@ -197,3 +197,22 @@ def test_quantize_dynamic_scale_bit_exact(nv, m, k):
     assert np.float32(host(xg)[0]) == gx
     np.testing.assert_array_equal(host(xq), oq)
     np.testing.assert_array_equal(host(xs), os_)
+
+
+def bf16_tensor(bits: np.ndarray) -> torch.Tensor:
+    """A CUDA bfloat16 tensor holding these BF16 bit patterns."""
+    return torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("m,k", [(1, 4096), (3, 12288), (8, 512), (2, 48), (5, 25600)])
+def test_quantize_act_bf16_input_bit_exact(nv, m, k):
+    """BF16 activations: the codes and scales equal the oracle's for the
+    FP32 values those BF16 numbers are (widening is exact)."""
+    x32 = synthetic.activations(m, k, seed=1000 + m + k)
+    bits = oracle.f32_to_bf16(x32)
+    xw = oracle.bf16_to_f32(bits)
+    gx = oracle.global_scale(xw)
+    oq, os_ = oracle.quantize(xw, gx)
+    xq, xs = nv.quantize_act(bf16_tensor(bits), dev(np.array([gx], np.float32)))
+    np.testing.assert_array_equal(host(xq), oq)
+    np.testing.assert_array_equal(host(xs), os_)

@@ -312,3 +312,47 @@ def test_gemm_sampled_matches_full():
     ms = np.array([0, 3, 2, 1, 3])
     ns = np.array([0, 39, 7, 20, 0])
     np.testing.assert_array_equal(oracle.gemm_sampled(xq, xs, gx, wq, ws, gw, ms, ns), y[ms, ns])
+
+
+# ---- BF16 conversions (production activation / output dtype) ----------------
+
+def test_bf16_golden_facts():
+    """Hand-derived values (tests/golden/bf16_facts.txt: IEEE 754 binary32
+    layout, BF16 = its upper 16 bits, round to nearest even)."""
+    vals, bits = [], []
+    for row in read_golden("bf16_facts.txt"):
+        v, b = row[0], row[1]
+        vals.append(float(v))
+        bits.append(int(b, 16))
+    got = oracle.f32_to_bf16(np.array(vals, np.float32))
+    np.testing.assert_array_equal(got, np.array(bits, np.uint16))
+    np.testing.assert_array_equal(oracle.bf16_to_f32(np.array(bits, np.uint16)),
+                                  oracle.bf16_to_f32(got))
+
+
+def test_bf16_widen_is_upper_half_of_binary32():
+    """Every finite BF16 pattern widens to the binary32 with those 16 bits on
+    top and zeros below (closed form, checked on the bit patterns)."""
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    w = oracle.bf16_to_f32(b)
+    np.testing.assert_array_equal(w.view(np.uint32), b.astype(np.uint32) << 16)
+
+
+def test_bf16_round_matches_torch_and_round_trips():
+    """Narrowing equals torch's BF16 cast (a library rounding routine) on
+    random values over many decades, on every exact tie between neighbours
+    near 1, 2^-100 and 2^100, and one binary32 ulp either side of each; and
+    narrowing a widened BF16 gives it back."""
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal(20000) * np.exp2(rng.uniform(-60, 60, 20000))).astype(np.float32)
+    ties = []
+    for e in (0, -100, 100):
+        j = np.arange(0, 128)
+        lo = (1.0 + j / 128.0) * 2.0 ** e
+        mid = (lo + 2.0 ** e / 256.0).astype(np.float32)            # exact halfway points
+        ties += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(np.inf))]
+    v = np.concatenate([v, *ties, -np.concatenate(ties)]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.f32_to_bf16(v), want)
+    b = np.arange(0, 0x7F80, dtype=np.uint16)                     # every finite positive
+    np.testing.assert_array_equal(oracle.f32_to_bf16(oracle.bf16_to_f32(b)), b)
