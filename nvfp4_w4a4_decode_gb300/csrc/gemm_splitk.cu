@@ -44,13 +44,6 @@ namespace nvfp4 {
 
 namespace {
 
-// Tuning constants (compile-time; the defaults are the measured choice).
-#ifndef NVFP4_SPLITK_RING
-#define NVFP4_SPLITK_RING 2
-#endif
-#ifndef NVFP4_SPLITK_MINB
-#define NVFP4_SPLITK_MINB 2
-#endif
 // Planner allowances, in sub-items of streaming: a shared-memory reduction
 // per tile when warps share it, a workspace round trip per tile (fence and
 // counter) and the last partial's extra round trips at the end of a launch.
@@ -63,13 +56,17 @@ namespace {
 #ifndef NVFP4_SPLITK_COST_TAIL
 #define NVFP4_SPLITK_COST_TAIL 3.0
 #endif
-constexpr int kWarps = 8;                  // warps per CTA
-constexpr int kRing = NVFP4_SPLITK_RING;   // sub-items in flight per warp
-constexpr int kMinBlocks = NVFP4_SPLITK_MINB;  // resident CTAs per SM the registers allow
+#ifndef NVFP4_SPLITK_STAGES
+#define NVFP4_SPLITK_STAGES 3
+#endif
+constexpr int kWarps = 16;                    // warps per CTA (one CTA per SM)
+constexpr int kStages = NVFP4_SPLITK_STAGES;  // sub-items per warp in its shared-memory ring
 constexpr int kSub = 256;        // elements of K per sub-item
+constexpr int kSlotBytes = 16 * 128 + 16 * 16;  // codes and scales of one 16-row sub-item
+constexpr size_t kRingSmem = (size_t)kWarps * kStages * kSlotBytes;
 constexpr size_t kFragSmem = 64 * 1024;  // activation fragments: 2 M bytes per K element
 constexpr size_t kGroupSmem = 2 * kWarps * 32 * 16;  // partial tiles of the warp groups
-constexpr size_t kMaxSmem = kFragSmem + kGroupSmem;
+constexpr size_t kMaxSmem = kRingSmem + kFragSmem + kGroupSmem;
 
 // Longest chunk whose fragments (M rows, 2 bytes per element) fit.
 __host__ __device__ constexpr int64_t max_chunk(int64_t m)
@@ -110,12 +107,34 @@ struct Sub {
 // its first 16 bytes, 4..7 the second; the activation fragments follow the
 // same order.
 
-template <bool PDL>
-__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const SplitkParams prm)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
 {
-    // [kc / 256][8 words][32 lanes] activation fragments, then (grp > 1)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most kStages - 1 of this thread's copy groups are pending.
+__device__ __forceinline__ void cp_async_wait_oldest()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+}
+
+template <bool PDL>
+__global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkParams prm)
+{
+    // [kWarps][kStages] sub-item slots of the warps' copy rings, then
+    // [kc / 256][8 words][4 M lanes] activation fragments, then (grp > 1)
     // [2][kWarps][32 lanes] float4 partial tiles of the warp groups
-    extern __shared__ __align__(16) uint4 xfrag[];
+    extern __shared__ __align__(16) unsigned char smem[];
     if constexpr (PDL)
         asm volatile("griddepcontrol.launch_dependents;");
 
@@ -131,12 +150,14 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     const int G = prm.grp, gi = warp / G, r = warp - gi * G, ngrp = kWarps / G;
     const int64_t tile0 = (int64_t)blockIdx.y * ngrp + gi;
     const int64_t tstride = (int64_t)gridDim.y * ngrp;
+    unsigned char* slots = smem + (size_t)warp * kStages * kSlotBytes;
+    const uint32_t slots_s = (uint32_t)__cvta_generic_to_shared(slots);
+    uint4* xfrag = reinterpret_cast<uint4*>(smem + kRingSmem);
 
-    // refill cursor: the next sub-item's tile and index, and this lane's
-    // addresses in rows g and g + 8 of that tile.  Rows past n read row n - 1
-    // instead (they only reach D rows that are never stored), so the loads
-    // need no per-lane condition; sub-items past the warp's last tile are not
-    // loaded.
+    // copy cursor: the next sub-item's tile and index, and this lane's source
+    // addresses in rows g and g + 8 of that tile.  Rows past n copy row n - 1
+    // instead (they only reach D rows that are never stored); sub-items past
+    // the warp's last tile copy nothing (an empty group keeps the count).
     int64_t f_tile = tile0;
     int f_sub = r;
     const uint8_t *fa, *fb, *qa, *qb;
@@ -146,41 +167,54 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
         const int64_t c0 = k0 + (int64_t)r * kSub;
         fa = prm.wq + ra * kh + c0 / 2 + 16 * t;
         fb = prm.wq + rb * kh + c0 / 2 + 16 * t;
-        qa = prm.ws + ra * kb + c0 / 16 + 2 * t;
-        qb = prm.ws + rb * kb + c0 / 16 + 2 * t;
+        qa = prm.ws + ra * kb + c0 / 16 + 4 * t;
+        qb = prm.ws + rb * kb + c0 / 16 + 4 * t;
     };
     point(tile0);
-    auto load = [&](Sub& sl) {
-        if (f_tile >= ntiles)
-            return;
-        sl.a0 = ld_stream_u4(fa);
-        sl.a1 = ld_stream_u4(fa + 64);
-        sl.b0 = ld_stream_u4(fb);
-        sl.b1 = ld_stream_u4(fb + 64);
-        sl.sa0 = ld_stream_u16(qa);
-        sl.sa1 = ld_stream_u16(qa + 8);
-        sl.sb0 = ld_stream_u16(qb);
-        sl.sb1 = ld_stream_u16(qb + 8);
-        f_sub += G;
-        if (f_sub >= nsub) {
-            f_sub = r;
-            f_tile += tstride;
-            point(f_tile);
-        } else {
-            fa += G * (kSub / 2);
-            fb += G * (kSub / 2);
-            qa += G * (kSub / 16);
-            qb += G * (kSub / 16);
+    // Slot layout: four 512-byte planes of code bytes (rows g | g + 8, first
+    // | second 16 bytes; lane l at 16 l, so every access is conflict-free),
+    // then the 16 scale bytes of each of the 16 rows; lane (g, t) copies
+    // scale bytes [4t, 4t + 4) of rows g and g + 8, the quad the whole row.
+    auto issue = [&](int s) {
+        if (f_tile < ntiles) {
+            const uint32_t d = slots_s + (uint32_t)(s * kSlotBytes);
+            cp_async16(d + 0 * 512 + lane * 16, fa);
+            cp_async16(d + 1 * 512 + lane * 16, fa + 64);
+            cp_async16(d + 2 * 512 + lane * 16, fb);
+            cp_async16(d + 3 * 512 + lane * 16, fb + 64);
+            cp_async4(d + 2048 + g * 16 + 4 * t, qa);
+            cp_async4(d + 2048 + (8 + g) * 16 + 4 * t, qb);
+            f_sub += G;
+            if (f_sub >= nsub) {
+                f_sub = r;
+                f_tile += tstride;
+                point(f_tile);
+            } else {
+                fa += G * (kSub / 2);
+                fb += G * (kSub / 2);
+                qa += G * (kSub / 16);
+                qb += G * (kSub / 16);
+            }
         }
+        cp_async_commit();
+    };
+    auto read_slot = [&](int s) {
+        const unsigned char* d = slots + s * kSlotBytes;
+        Sub sl;
+        sl.a0 = *reinterpret_cast<const uint4*>(d + 0 * 512 + lane * 16);
+        sl.a1 = *reinterpret_cast<const uint4*>(d + 1 * 512 + lane * 16);
+        sl.b0 = *reinterpret_cast<const uint4*>(d + 2 * 512 + lane * 16);
+        sl.b1 = *reinterpret_cast<const uint4*>(d + 3 * 512 + lane * 16);
+        sl.sa0 = *reinterpret_cast<const unsigned short*>(d + 2048 + g * 16 + 2 * t);
+        sl.sa1 = *reinterpret_cast<const unsigned short*>(d + 2048 + g * 16 + 8 + 2 * t);
+        sl.sb0 = *reinterpret_cast<const unsigned short*>(d + 2048 + (8 + g) * 16 + 2 * t);
+        sl.sb1 = *reinterpret_cast<const unsigned short*>(d + 2048 + (8 + g) * 16 + 8 + 2 * t);
+        return sl;
     };
 
-    Sub ring[kRing];
 #pragma unroll
-    for (int s = 0; s < kRing; ++s) {
-        ring[s].a0 = ring[s].a1 = ring[s].b0 = ring[s].b1 = make_uint4(0u, 0u, 0u, 0u);
-        ring[s].sa0 = ring[s].sa1 = ring[s].sb0 = ring[s].sb1 = 0u;
-        load(ring[s]);
-    }
+    for (int s = 0; s < kStages; ++s)
+        issue(s);
 
     // the activations are written by the previous kernel on the stream
     if constexpr (PDL)
@@ -334,7 +368,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     // End of a warp's share of a tile: with warp groups, the group's warps
     // leave their partials in shared memory (double-buffered, so one barrier
     // per tile suffices) and rank 0 adds them in rank order and flushes.
-    float4* red = reinterpret_cast<float4*>(xfrag + nsub * 8 * LW);
+    float4* red = reinterpret_cast<float4*>(xfrag + nsub * 8 * LW);  // after the fragments
     int rbuf = 0;
     auto tile_end = [&](int64_t tile) {
         float v0 = acc[0] + acc2[0], v1 = acc[1] + acc2[1], v2 = acc[2] + acc2[2],
@@ -369,12 +403,18 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
     const int b_first = r * 8 * LW, b_step = G * 8 * LW;  // fragment offsets of this warp's sub-items
     int c_b = b_first, c_left = per_tile;
     const uint4* xb = xfrag + lane_b;
-    for (int64_t e = 0; e < nitems; e += kRing) {
+    for (int64_t e = 0; e < nitems; e += kStages) {
 #pragma unroll
-        for (int s = 0; s < kRing; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             if (e + s < nitems) {
-                consume(ring[s], xb + c_b);
-                load(ring[s]);
+                // the oldest group (this slot) is complete for this lane; the
+                // warp barrier makes every lane's copies (the shared scale
+                // rows) visible to the others
+                cp_async_wait_oldest();
+                __syncwarp();
+                consume(read_slot(s), xb + c_b);
+                __syncwarp();  // every lane is done reading the slot
+                issue(s);
                 c_b += b_step;
                 if (--c_left == 0) {
                     tile_end(c_tile);
@@ -387,6 +427,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) splitk_kernel(const S
             }
         }
     }
+    // no copy is left in flight: every group issued past the last sub-item
+    // was empty
 }
 
 struct SplitkPlan {
@@ -496,7 +538,7 @@ bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* 
 template <bool PDL>
 cudaError_t launch_t(const GemmArgs& a, const SplitkPlan& p, void* workspace, int64_t ws_bytes)
 {
-    const size_t smem = (size_t)p.kc * 2 * a.m + (p.grp > 1 ? kGroupSmem : 0);
+    const size_t smem = kRingSmem + (size_t)p.kc * 2 * a.m + (p.grp > 1 ? kGroupSmem : 0);
     auto kern = splitk_kernel<PDL>;
     const int dev = current_device();
     if (smem > 48 * 1024) {
