@@ -14,24 +14,31 @@
 // inside an MMA is free: each lane takes the bytes that make its loads whole
 // 32-byte sectors.
 //
-// Work layout.  K is cut into chunks of kc elements (a multiple of 256).  CTA
-// (c, y) of the (nchunks, Cy) grid owns chunk c; its warp w owns the tiles
-// (16 weight rows) y * NW + w + j * Cy * NW.  A warp works alone after the
-// prologue: it streams the 256-element sub-items of its tiles, tile by tile,
-// through a register ring of kRing sub-items, accumulates a tile's 16 x 8
-// block in four registers per lane, and at the end of the tile's chunk
+// Work layout.  K is cut into chunks of kc elements (a multiple of 256, at
+// most 32768 / M).  CTA (c, y) of the (nchunks, Cy) grid -- one 16-warp CTA
+// per SM -- owns chunk c.  Its warps form groups of grp warps (1, 2, 4, 8 or
+// 16); group gi owns the tiles (16 weight rows) y * ngrp + gi + j * Cy * ngrp,
+// and warp r of the group takes the sub-items (256 elements of K) r, r + grp,
+// ... of each tile's chunk.  After the prologue a warp streams its sub-items
+// through its own ring of kStages shared-memory slots filled by cp.async
+// (every lane copies its own 16-byte pieces; the quad copies a row's scale
+// bytes, so a warp barrier follows each wait), accumulates a tile's 16 x 8
+// block in registers and, at the end of its share of the tile,
+//   * adds the group's partials (shared memory, one named barrier per tile,
+//     rank order) in rank 0, which then
 //   * writes Y directly when K is one chunk, or
-//   * stores its partial in the workspace and counts it in; the warp that
+//   * stores the partial in the workspace and counts it in; the warp that
 //     stores a tile's last partial sums all of them in chunk order (so the
 //     result does not depend on which warp finishes last), writes Y and
 //     resets the tile's counter to zero for the next call.
-// There is no CTA barrier after the prologue and no wait on another CTA.
-// Per sub-item, lane (g, t) = (lane / 4, lane % 4) loads of rows g and g + 8
+// There is no CTA-wide barrier after the prologue and no wait on another CTA.
+// Per sub-item, lane (g, t) = (lane / 4, lane % 4) copies of rows g and g + 8
 // the code bytes [16t, 16t + 16) and [64 + 16t, 64 + 16t + 16) of the row's
-// 128 (so one load instruction covers two whole sectors per row) and the
-// matching scale bytes {2t, 2t + 1} and {8 + 2t, 9 + 2t}.
+// 128 (so one copy instruction covers two whole sectors per row) and uses the
+// scale bytes {2t, 2t + 1} and {8 + 2t, 9 + 2t}.
 // The activations of the chunk are decoded once per CTA, scaled, into shared
-// memory in fragment order (one conflict-free 16-byte read per two MMAs).
+// memory in fragment order (one conflict-free 16-byte read per two MMAs), for
+// the M real columns only.
 #include <mutex>
 #include <unordered_map>
 
@@ -91,10 +98,9 @@ struct SplitkParams {
     int grp;  // warps that share a tile (1, 2, 4 or 8), splitting its chunk
 };
 
-// One sub-item of a lane: 16 + 16 code bytes of rows g and g + 8 and their
-// four block scales each.  Each 16-bit scale load keeps its own register: a
-// value combined from two loads would make the loop wait for them where it
-// is combined, not where it is used, and defeat the ring.
+// One sub-item of a lane, read from its ring slot: 16 + 16 code bytes of rows
+// g and g + 8 and their four block scales each (two scale bytes per register,
+// as the E4M3-pair conversion takes them).
 struct Sub {
     uint4 a0, a1;       // row g
     uint4 b0, b1;       // row g + 8
