@@ -167,3 +167,26 @@ def test_workspace_entry_points_host_only(lib):
     f = lib.nvfp4_linear_ws
     assert f(FAKE, 1, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None, 8, None) == 1
     assert f(FAKE, 0, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 8, None) == 0
+
+
+def test_splitk_planner_properties_host_only(lib):
+    """For many shapes: the workspace the split-K plan asks for is accepted
+    for that plan; one chunk (no workspace) is possible exactly when K fits
+    one CTA's activation fragments (2 M bytes per element, 64 KB); K not a
+    multiple of 256 and M outside 1..8 are refused."""
+    import random
+    rnd = random.Random(5)
+    SPLITK = nv.KERNEL_SPLITK
+    for _ in range(300):
+        m = rnd.randint(1, 8)
+        k = 256 * rnd.randint(1, 160)
+        n = rnd.randint(1, 70000)
+        need = lib.nvfp4_gemm_workspace_size(m, n, k, SPLITK)
+        assert need >= 0
+        assert lib.nvfp4_gemm_select_ws(m, n, k, SPLITK, need) == SPLITK
+        one_chunk = k <= (65536 // (2 * m)) // 256 * 256
+        assert (lib.nvfp4_gemm_select_ws(m, n, k, SPLITK, 0) == SPLITK) == one_chunk, (m, n, k)
+        if one_chunk:
+            assert need == 0 or need >= 1024 * ((n + 15) // 16)   # 2+ partials of 512 B per tile
+    for m, k in ((1, 4000), (9, 4096), (0, 4096)):
+        assert lib.nvfp4_gemm_select_ws(m, 100, k, SPLITK, 1 << 30) < 0
