@@ -112,8 +112,10 @@ int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g,
  *   x_q, x_s, x_g   activation codes, scales, tensor scale (as above)
  *   w_q, w_s, w_g   weight codes, scales, tensor scale (as above)
  *   y               device float[m][n], overwritten
- * m must be 0..8 (NVFP4_ERR_UNSUPPORTED otherwise).  One kernel launch
- * (a cluster launch on the fast path).  The result does not depend on the
+ * m must be 0..8 (NVFP4_ERR_UNSUPPORTED otherwise).  One kernel launch:
+ * the CUDA-core stream at M = 1, the split-K tensor-core kernel at M >= 2
+ * when its plan needs no workspace (use nvfp4_gemm_smallm_ws to offer one),
+ * else a TMA-fed or cluster tensor-core kernel.  The result does not depend on the
  * launch order of CTAs: every reduction has a fixed order.
  */
 int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
