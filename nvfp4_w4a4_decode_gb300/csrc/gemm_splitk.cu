@@ -156,6 +156,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
     const int G = prm.grp, gi = warp / G, r = warp - gi * G, ngrp = kWarps / G;
     const int64_t tile0 = (int64_t)blockIdx.y * ngrp + gi;
     const int64_t tstride = (int64_t)gridDim.y * ngrp;
+    // this warp's sub-items (fits an int: the planner takes N < 2^27)
+    const int mytiles = tile0 < ntiles ? (int)((ntiles - 1 - tile0) / tstride) + 1 : 0;
+    const int per_tile = nsub / G;  // sub-items of each warp per tile
+    const int nitems = mytiles * per_tile;
+    int copies_left = nitems;
     unsigned char* slots = smem + (size_t)warp * kStages * kSlotBytes;
     const uint32_t slots_s = (uint32_t)__cvta_generic_to_shared(slots);
     uint4* xfrag = reinterpret_cast<uint4*>(smem + kRingSmem);
@@ -182,7 +187,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
     // then the 16 scale bytes of each of the 16 rows; lane (g, t) copies
     // scale bytes [4t, 4t + 4) of rows g and g + 8, the quad the whole row.
     auto issue = [&](int s) {
-        if (f_tile < ntiles) {
+        if (copies_left > 0) {
+            --copies_left;
             const uint32_t d = slots_s + (uint32_t)(s * kSlotBytes);
             cp_async16(d + 0 * 512 + lane * 16, fa);
             cp_async16(d + 1 * 512 + lane * 16, fa + 64);
@@ -402,14 +408,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
         flush(tile, v0, v1, v2, v3);
     };
 
-    const int64_t mytiles = tile0 < ntiles ? (ntiles - 1 - tile0) / tstride + 1 : 0;
-    const int per_tile = nsub / G;  // sub-items of each warp per tile
-    const int64_t nitems = mytiles * per_tile;
     int64_t c_tile = tile0;
     const int b_first = r * 8 * LW, b_step = G * 8 * LW;  // fragment offsets of this warp's sub-items
     int c_b = b_first, c_left = per_tile;
     const uint4* xb = xfrag + lane_b;
-    for (int64_t e = 0; e < nitems; e += kStages) {
+    for (int e = 0; e < nitems; e += kStages) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
             if (e + s < nitems) {
@@ -499,7 +502,7 @@ int64_t resident_ctas()
 // whose workspace exceeds `ws_limit` are skipped (0: single-chunk plans only).
 bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* out)
 {
-    if (m < 1 || m > 8 || n < 1 || k < kSub || k % kSub != 0)
+    if (m < 1 || m > 8 || n < 1 || n >= (int64_t(1) << 27) || k < kSub || k % kSub != 0)
         return false;
     const int64_t slots = resident_ctas();
     const int64_t ntiles = (n + 15) / 16;
