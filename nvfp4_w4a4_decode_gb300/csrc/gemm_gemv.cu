@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
     for (int64_t base = 0; base < iters; base += STAGES) {
         // 3. consume the ring, refilling each stage with the group STAGES ahead
         float acc[STAGES][M];
+        // running addresses of the refills (one add per stage, not a
+        // multiply)
         const uint8_t* wn = w0 + (base + STAGES) * wstep;
         const uint8_t* sn = s0 + (base + STAGES) * sstep;
         const int64_t left = valid_iters - (base + STAGES);  // refills still in range
@@ -214,15 +216,15 @@ __global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
                 e2m1x8_to_f16(rw[s].w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
                 sw = e4m3x2_to_float2(rs[s]);
                 if (s < left) {
-                    rw[s] = ld_stream_u4(wn + s * wstep);
-                    rs[s] = ld_u16_nc(sn + s * sstep);
+                    rw[s] = ld_stream_u4(wn);
+                    rs[s] = ld_u16_nc(sn);
                 }
             } else {
                 const uint4 cw = rw[s];
                 const uint32_t cs = rs[s];
                 if (s < left) {
-                    rw[s] = ld_stream_u4(wn + s * wstep);
-                    rs[s] = ld_u16_nc(sn + s * sstep);
+                    rw[s] = ld_stream_u4(wn);
+                    rs[s] = ld_u16_nc(sn);
                 }
                 e2m1x8_to_f16(cw.x, *reinterpret_cast<uint32_t(*)[4]>(&wh[0]));
                 e2m1x8_to_f16(cw.y, *reinterpret_cast<uint32_t(*)[4]>(&wh[4]));
@@ -230,6 +232,8 @@ __global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
                 e2m1x8_to_f16(cw.w, *reinterpret_cast<uint32_t(*)[4]>(&wh[12]));
                 sw = e4m3x2_to_float2(cs);
             }
+            wn += wstep;
+            sn += sstep;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 uint32_t p0 = 0u, p1 = 0u;
