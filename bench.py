@@ -705,6 +705,46 @@ def run_single(args) -> None:
                       "GBps": round(byt / (us * 1e-6) / 1e9, 1), "y00": float(y[0, 0])}))
 
 
+def run_profile_shapes(args) -> None:
+    """Every linear shape of the workloads once, with the library's kernel
+    choice (workspace offered): the 256 x 512 single GEMV at M = 1, the four
+    8B linears at M = 1, 2, 4, 8 and the four 32B linears at M = 1, 4.  One
+    weight matrix at a time on the device (at most 148 MB), `reps` GEMM launches
+    each; prints the kernel per shape.  The case the per-shape counter capture
+    runs."""
+    import torch
+
+    import nvfp4_w4a4_decode_gb300 as nv
+    from nvfp4_w4a4_decode_gb300 import build as nvbuild
+    nvbuild.build()
+    nv.library()
+    cases = [(synthetic.TINY, 1, synthetic.WEIGHT_STD_8B, "C1")]
+    cases += [(lin, m, synthetic.WEIGHT_STD_8B, "8B") for m in synthetic.M_SWEEP_8B
+              for lin in synthetic.LINEARS_8B]
+    cases += [(lin, m, synthetic.WEIGHT_STD_32B, "32B") for m in synthetic.M_SWEEP_32B
+              for lin in synthetic.LINEARS_32B]
+    gen = torch.Generator(device="cuda")
+    for i, (lin, m, std, fam) in enumerate(cases):
+        gen.manual_seed(7000 + i)
+        w = torch.randn((lin.n, lin.k), generator=gen, device="cuda") * std
+        wq, ws, wg = nv.pack_weight(w)
+        del w
+        x = torch.from_numpy(synthetic.activations(m, lin.k, seed=7100 + i)).cuda()
+        xg = nv.global_scale(x)
+        xq, xs = nv.quantize_act(x, xg)
+        y = torch.empty((m, lin.n), device="cuda")
+        wsp = nv.workspace(m, lin.n, lin.k)
+        kid = nv.gemm_select(m, lin.n, lin.k, nv.KERNEL_AUTO, wsp.numel() if wsp is not None else 0)
+        for _ in range(args.reps):
+            nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y, workspace=wsp)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": i, "family": fam, "linear": lin.name, "m": m, "n": lin.n,
+                          "k": lin.k, "kernel": nv.KERNEL_NAMES.get(kid),
+                          "gemm_bytes": algorithmic_bytes(m, lin.n, lin.k)["gemm"]}), flush=True)
+        del wq, ws, wg, x, xq, xs, y, wsp
+        torch.cuda.empty_cache()
+
+
 def run_reference(args) -> dict | None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -769,6 +809,9 @@ def main():
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNELS),
                     help="GEMM kernel for the decode step (and for --single)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--profile-shapes", action="store_true",
+                    help="run every workload shape once per rep with the library's kernel "
+                         "choice (for a per-shape counter capture) and exit")
     ap.add_argument("--profile-step", action="store_true",
                     help="replay only the step graph (warmup + steps times) and exit")
     args = ap.parse_args()
@@ -776,6 +819,9 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.single:
         run_single(args)
+        return
+    if args.profile_shapes:
+        run_profile_shapes(args)
         return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
