@@ -307,6 +307,20 @@ int nvfp4_linear_ws(const void* x, int64_t m, int64_t n, int64_t k, const float*
                     size_t workspace_bytes, void* stream);
 
 /*
+ * Read-only streaming probe, a measurement aid with no counterpart in the
+ * method: the DRAM read rate a plain stream of 128-bit loads reaches on this
+ * device, the ceiling next to which the GEMM's weight stream is judged.
+ *   buf    device, `bytes` bytes (16-byte aligned; read-only, not owned)
+ *   bytes  a multiple of 16 (0: only the sink is written)
+ *   sink   device uint64_t[1] (8-byte aligned), OUTPUT: zeroed on the stream,
+ *          then the XOR of every 8-byte word of buf (so no load is dropped)
+ * Launches a memset and one kernel (every word loaded once, non-allocating
+ * in L1); asynchronous on `stream`.  NVFP4_ERR_INVALID_ARG for a negative or
+ * ragged size, a null or misaligned pointer.
+ */
+int nvfp4_read_probe(const void* buf, int64_t bytes, uint64_t* sink, void* stream);
+
+/*
  * Device status word of the library on the current device: the OR of the
  * NVFP4_DEVICE_* bits recorded by kernels since it was last cleared (a wait
  * that ran out of its budget sets NVFP4_DEVICE_WAIT_TIMEOUT; the results of

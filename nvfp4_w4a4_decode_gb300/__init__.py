@@ -25,7 +25,7 @@ __all__ = [
     "nvfp4_quantize_act", "nvfp4_gemm_smallm", "global_scale", "pack_weight",
     "quantize_act", "gemm_smallm", "nvfp4_linear", "linear", "MAX_M",
     "nvfp4_gemm_workspace_size", "nvfp4_workspace", "gemm_workspace_size", "workspace",
-    "nvfp4_gemm_smallm_static", "gemm_smallm_static",
+    "nvfp4_gemm_smallm_static", "gemm_smallm_static", "nvfp4_read_probe", "read_probe",
 ]
 
 MAX_M = 8
@@ -61,6 +61,7 @@ SIGNATURES = {
                               ctypes.c_size_t, _p], ctypes.c_int),
     "nvfp4_linear_ws": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p,
                          ctypes.c_size_t, _p], ctypes.c_int),
+    "nvfp4_read_probe": ([_p, _i64, _p, _p], ctypes.c_int),
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA, KERNEL_SPLITK = 0, 1, 2, 3, 4, 5
@@ -281,6 +282,20 @@ def nvfp4_gemm_select(m: int, n: int, k: int, kernel: int = KERNEL_AUTO,
     return library().nvfp4_gemm_select_ws(m, n, k, kernel, workspace_bytes)
 
 
+def nvfp4_read_probe(buf: torch.Tensor, sink: torch.Tensor | None = None) -> torch.Tensor:
+    """Read-only streaming probe over a contiguous CUDA tensor (16-byte
+    aligned, size a multiple of 16 bytes): returns a uint64 device scalar
+    (as int64 storage) holding the XOR of all 8-byte words of ``buf``.  A
+    measurement aid; time it with CUDA events on the current stream."""
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    if sink is None:
+        sink = torch.empty(1, dtype=torch.int64, device=buf.device)
+    _check("nvfp4_read_probe", library().nvfp4_read_probe(
+        buf.data_ptr(), buf.numel() * buf.element_size(), sink.data_ptr(), _stream(buf)))
+    return sink
+
+
 def nvfp4_device_status(clear: bool = True, stream=None) -> int:
     """Device status bits recorded by the kernels (synchronises the stream)."""
     v = ctypes.c_uint32(0)
@@ -335,3 +350,4 @@ gemm_workspace_size = nvfp4_gemm_workspace_size
 gemm_smallm_static = nvfp4_gemm_smallm_static
 workspace = nvfp4_workspace
 device_status = nvfp4_device_status
+read_probe = nvfp4_read_probe

@@ -341,6 +341,16 @@ int64_t nvfp4_gemm_static_scratch_bytes(void)
     return nvfp4::splitk_static_scratch_bytes();
 }
 
+int nvfp4_read_probe(const void* buf, int64_t bytes, uint64_t* sink, void* stream)
+{
+    if (bytes < 0 || bytes % 16 != 0 || sink == nullptr || !aligned(sink, 8) ||
+        (bytes > 0 && (buf == nullptr || !aligned(buf, 16))))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(nvfp4::launch_read_probe(buf, bytes,
+                                              reinterpret_cast<unsigned long long*>(sink),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int nvfp4_device_status(void* stream, uint32_t* flags, int clear)
 {
     if (flags == nullptr)

@@ -96,4 +96,10 @@ cudaError_t launch_gemm_splitk_static(const GemmArgs& a, bool pdl);
 
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
 
+// Read-only streaming probe: zeroes *sink on the stream, then loads every
+// 16-byte word of buf once and XORs all its 8-byte words into *sink.  buf
+// 16-byte aligned, bytes a multiple of 16.
+cudaError_t launch_read_probe(const void* buf, int64_t bytes, unsigned long long* sink,
+                              cudaStream_t stream);
+
 }  // namespace nvfp4

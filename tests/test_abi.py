@@ -169,6 +169,16 @@ def test_workspace_entry_points_host_only(lib):
     assert f(FAKE, 0, 16, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 8, None) == 0
 
 
+def test_read_probe_rejects_bad_arguments(lib):
+    f = lib.nvfp4_read_probe
+    assert f(FAKE, 17, FAKE, None) == 1          # not a multiple of 16
+    assert f(FAKE, -16, FAKE, None) == 1
+    assert f(FAKE + 8, 32, FAKE, None) == 1      # buffer not 16-byte aligned
+    assert f(None, 32, FAKE, None) == 1
+    assert f(FAKE, 32, None, None) == 1          # no sink
+    assert f(FAKE, 32, FAKE + 4, None) == 1      # sink not 8-byte aligned
+
+
 def test_splitk_planner_properties_host_only(lib):
     """For many shapes: the workspace the split-K plan asks for is accepted
     for that plan; one chunk (no workspace) is possible exactly when K fits
