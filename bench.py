@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import queue
 import statistics
 import subprocess
 import sys
@@ -673,10 +674,12 @@ def calibrate_sample(budget_s: float):
     return max(lin.n for lin in synthetic.LINEARS_8B), int(min(36, max(1, round(budget_s / full_layer))))
 
 
-def cpu_baseline(budget_s: float = 12.0) -> dict:
+def cpu_baseline(budget_s: float = 12.0, all_cores: bool = True) -> dict:
     """The oracle on the host: a bounded sample of the step sized to about
     ``budget_s`` seconds.  When whole layers fit, one layer is timed first
-    (untimed warm-up of the sample) to fix how many layers the budget holds."""
+    (untimed warm-up of the sample) to fix how many layers the budget holds.
+    With ``all_cores`` (and more than one core) the reported line is the
+    all-cores run, the single-thread one nested in it."""
     rows, layers = calibrate_sample(budget_s)
     items = oracle_sample(rows, layers=1)
     if rows >= max(lin.n for lin in synthetic.LINEARS_8B):
@@ -692,10 +695,73 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
     v = sample_bytes(items) / sec / 1e9
     what = (f"{layers} whole layers (all output rows)" if layers > 1 or rows >= 24576
             else f"one layer, {rows} output rows per linear")
-    return {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"the four 8B-shaped linears at M=1 of {what}: quantise X + FP64 GEMM "
-                      f"from packed bytes, {sec:.1f} s, single thread",
-            "seconds": round(sec, 2)}
+    single = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+              "sample": f"the four 8B-shaped linears at M=1 of {what}: quantise X + FP64 GEMM "
+                        f"from packed bytes, {sec:.1f} s, single thread",
+              "seconds": round(sec, 2)}
+    if not all_cores or len(os.sched_getaffinity(0)) < 2:
+        return single
+    # whole layers are what the all-cores run gives out: time one when the
+    # single-thread sample had only part of one
+    layer_s = sec / layers if rows >= max(lin.n for lin in synthetic.LINEARS_8B) else \
+        sec * sum(lin.n * lin.k for lin in synthetic.LINEARS_8B) / \
+        sum(min(rows, lin.n) * lin.k for lin in synthetic.LINEARS_8B)
+    line = cpu_baseline_all_cores(layer_s, budget_s)
+    line["single_thread"] = single
+    return line
+
+
+def _oracle_worker(layers: int, first_layer: int, barrier, out) -> None:
+    """One host process of the all-cores baseline: build its whole layers of
+    the sample (untimed), wait for the others, time one oracle pass."""
+    items = oracle_sample(max(lin.n for lin in synthetic.LINEARS_8B), layers=layers,
+                          first_layer=first_layer)
+    barrier.wait(timeout=900)
+    t0 = time.perf_counter()
+    oracle_pass(items)
+    t1 = time.perf_counter()
+    out.put((t0, t1, sample_bytes(items)))
+
+
+def cpu_baseline_all_cores(layer_seconds: float, budget_s: float = 12.0) -> dict:
+    """The same oracle on every core of this process's affinity mask: one
+    single-threaded process per core (started with spawn), each with its own
+    whole layers of the step (at most the step's 36 in total, about
+    ``budget_s`` seconds each), all timed together: the wall time from the
+    first start to the last finish."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    per_worker = max(1, int(budget_s / max(layer_seconds, 1e-3)))
+    total = min(synthetic.DECODE_LAYERS_8B, per_worker * cores)
+    workers = min(cores, total)
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(workers)
+    out = ctx.Queue()
+    procs, first = [], 0
+    for i in range(workers):
+        n = total // workers + (1 if i < total % workers else 0)
+        procs.append(ctx.Process(target=_oracle_worker, args=(n, first, barrier, out)))
+        first += n
+    for p in procs:
+        p.start()
+    res, deadline = [], time.time() + 1800
+    while len(res) < len(procs):
+        try:
+            res.append(out.get(timeout=2))
+        except queue.Empty:
+            if time.time() > deadline or any(p.exitcode not in (None, 0) for p in procs):
+                for p in procs:      # the processes started here, by handle
+                    p.terminate()
+                raise RuntimeError("an all-cores oracle process failed or ran out of time")
+    for p in procs:
+        p.join()
+    wall = max(r[1] for r in res) - min(r[0] for r in res)
+    v = sum(r[2] for r in res) / wall / 1e9
+    return {"value": round(v, 4), "unit": UNIT, "cores": workers, "kind": "oracle",
+            "sample": f"{total} whole layers of the step (the four 8B-shaped linears at M=1, all "
+                      f"output rows), spread over {workers} single-threaded processes: quantise X "
+                      f"+ FP64 GEMM from packed bytes, {wall:.1f} s wall",
+            "seconds": round(wall, 2)}
 
 
 KERNELS = {"auto": lambda nv: nv.KERNEL_AUTO, "generic": lambda nv: nv.KERNEL_GENERIC,
