@@ -385,12 +385,54 @@ def auto_choice(nv, m, lin) -> int:
                           nv.gemm_workspace_size(m, lin.n, lin.k))
 
 
+def tiny_latency(nv, torch, kernels: dict, pdl: bool, calls: int = 50) -> dict:
+    """The single 256 x 512 GEMV at M = 1 (75 KB: latency, not bandwidth):
+    µs per call of a CUDA graph of `calls` back-to-back calls on the same
+    seeded operands (L2-resident), for the library's choice and every kernel
+    that takes the shape, GEMM alone and quantise + GEMM (nvfp4_linear)."""
+    lin = synthetic.TINY
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    w = torch.randn((lin.n, lin.k), generator=gen, device="cuda") * synthetic.WEIGHT_STD_8B
+    wq, ws, wg = nv.pack_weight(w)
+    x = torch.from_numpy(synthetic.activations(1, lin.k, seed=0, outliers=False)).cuda()
+    xg = nv.global_scale(x)
+    xq, xs = nv.quantize_act(x, xg)
+    y = torch.empty((1, lin.n), device="cuda")
+
+    def timed(fn):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(calls):
+                fn()
+        return round(min(time_graph(torch, g, reps=5) for _ in range(3)) * 1e3 / calls, 3)
+
+    res = {"n": lin.n, "k": lin.k, "m": 1,
+           "kernel": nv.KERNEL_NAMES.get(auto_choice(nv, 1, lin))}
+    for name, kid in kernels.items():
+        if not takes(nv, 1, lin, kid):
+            continue
+        wsp = nv.workspace(1, lin.n, lin.k, kid)
+        res[name] = {
+            "gemm_us_per_call": timed(lambda: nv.gemm_smallm(xq, xs, xg, wq, ws, wg, out=y,
+                                                             kernel=kid, pdl=pdl, workspace=wsp)),
+            "quantize_plus_gemm_us_per_call": timed(
+                lambda: nv.linear(x, xg, wq, ws, wg, out=y, x_out=(xq, xs), kernel=kid, pdl=pdl,
+                                  workspace=wsp))}
+    return res
+
+
 def sweep(nv, torch, stack, peaks, args) -> dict:
     """µs/call and GB/s of every linear shape for every M of the sweep, with
     the library's kernel choice and with each kernel that takes the shape."""
     kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA,
                "splitk": nv.KERNEL_SPLITK, "generic": nv.KERNEL_GENERIC}
-    out = {"8B": {}, "32B": {}}
+    out = {"8B": {}, "32B": {}, "C1": tiny_latency(nv, torch, kernels, stack.pdl)}
     reps = 5
     w8 = {j: [stack.w[l][j] for l in range(stack.layers)] for j in range(4)}
     for m in synthetic.M_SWEEP_8B:

@@ -51,6 +51,26 @@ namespace {
 #endif
 constexpr int kCtasPerSm = NVFP4_GEMV_CTAS_PER_SM;
 
+// Registers per SM the M = 1 variants with up to 512 threads (the decode
+// shapes) leave free: room for one CTA of the activation quantiser (128
+// threads at up to 32 registers) beside a full complement of these CTAs, so
+// that under programmatic dependent launch the next linear's quantiser is
+// resident, and its prefetch of X issued, before this kernel ends.  The
+// per-thread cap follows: (65536 - reserve) / (threads x CTAs per SM), in the
+// allocation unit of 8.  The other variants keep the whole register file
+// (tighter caps spill there).
+#ifndef NVFP4_GEMV_REG_RESERVE
+#define NVFP4_GEMV_REG_RESERVE 4096
+#endif
+__host__ __device__ constexpr int gemv_reg_cap(int m, int maxt, int minb)
+{
+    return (65536 - (m == 1 && maxt <= 512 ? NVFP4_GEMV_REG_RESERVE : 0)) / (maxt * minb) / 8 *
+                       8 > 255
+               ? 255
+               : (65536 - (m == 1 && maxt <= 512 ? NVFP4_GEMV_REG_RESERVE : 0)) /
+                     (maxt * minb) / 8 * 8;
+}
+
 struct GemvParams {
     const uint8_t* xq;     // quantised activations (unfused) ...
     const uint8_t* xs;
@@ -95,7 +115,8 @@ __device__ __forceinline__ float rs_step(float a, float b, int bit, bool upper)
 }
 
 template <int M, int STAGES, int MAXT, int MINB, bool PDL, bool FUSED>
-__global__ void __launch_bounds__(MAXT, MINB) gemv_kernel(const GemvParams prm)
+__global__ void __launch_bounds__(MAXT) __maxnreg__(gemv_reg_cap(M, MAXT, MINB))
+    gemv_kernel(const GemvParams prm)
 {
     static_assert(STAGES == 8 || STAGES == 4, "reduce-scatter is written for 8 or 4 stages");
     extern __shared__ __align__(16) float red[];  // [2][P][STAGES][M][G/32] warp sums,

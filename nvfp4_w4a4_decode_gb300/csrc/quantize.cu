@@ -43,28 +43,49 @@ __global__ void finalize_scale_kernel(float* g)
     *g = __fdiv_rn(amax, 2688.0f);
 }
 
+// Threads per quantiser CTA.  128 threads at 26 registers take 4096
+// registers, which a GEMM CTA pair that leaves that many free (the CUDA-core
+// stream's register cap) has room for, so the quantiser of the next linear
+// becomes resident while the current GEMM still runs.
+#ifndef NVFP4_QUANT_THREADS
+#define NVFP4_QUANT_THREADS 128
+#endif
+// Prefetch X into L2 before waiting on its producer (1) or not (0).
+#ifndef NVFP4_QUANT_PREFETCH
+#define NVFP4_QUANT_PREFETCH 1
+#endif
+constexpr int kQuantThreads = NVFP4_QUANT_THREADS;
+
 // Four threads per 16-element block (each holds 4 consecutive elements):
 // block amax by a quad shuffle, the E4M3 block scale relative to the tensor
 // scale, then each thread's 4 E2M1 codes; the quad gathers its 16 codes into
 // two 32-bit words.  Blocks are numbered row-major, so a warp reads 512
 // contiguous bytes of t and writes 64 contiguous code bytes.  With
 // programmatic dependent launch the kernel lets the next kernel (the GEMM)
-// launch at once, then waits for the producer of t.  BF16 input is widened
-// to FP32 exactly (a BF16 value is the top half of its FP32 bits).
+// launch at once, asks L2 for its slice of t (a hint: L2 is where global
+// memory is coherent, so lines fetched before the producer's writes land are
+// updated by them, and the loads below come after the wait), then waits for
+// the producer of t.  BF16 input is widened to FP32 exactly (a BF16 value is
+// the top half of its FP32 bits).
 template <bool PDL, bool BF16>
-__global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ t, int64_t nblocks,
-                                                       const float* __restrict__ g_ptr,
-                                                       uint8_t* __restrict__ q,
-                                                       uint8_t* __restrict__ s)
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const void* __restrict__ t,
+                                                                 int64_t nblocks,
+                                                                 const float* __restrict__ g_ptr,
+                                                                 uint8_t* __restrict__ q,
+                                                                 uint8_t* __restrict__ s)
 {
-    if constexpr (PDL) {
-        asm volatile("griddepcontrol.launch_dependents;");
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-    }
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t b = tid >> 2;
     const int sub = (int)(tid & 3);
     const bool valid = b < nblocks;
+    if constexpr (PDL) {
+        asm volatile("griddepcontrol.launch_dependents;");
+        // one prefetch per 128-byte line of t: 8 threads (FP32) or 16 (BF16)
+        if (NVFP4_QUANT_PREFETCH && valid && (tid & (BF16 ? 15 : 7)) == 0)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(t) +
+                                                           tid * (BF16 ? 8 : 16)));
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
 
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
@@ -122,14 +143,15 @@ template <bool BF16>
 cudaError_t launch_quantize_t(const void* t, int64_t nblocks, const float* g, uint8_t* q,
                               uint8_t* s, cudaStream_t stream, bool pdl)
 {
-    const int64_t grid = (4 * nblocks + 255) / 256;
+    const int64_t grid = (4 * nblocks + kQuantThreads - 1) / kQuantThreads;
     if (!pdl) {
-        quantize_kernel<false, BF16><<<(unsigned)grid, 256, 0, stream>>>(t, nblocks, g, q, s);
+        quantize_kernel<false, BF16><<<(unsigned)grid, kQuantThreads, 0, stream>>>(t, nblocks, g,
+                                                                                   q, s);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
