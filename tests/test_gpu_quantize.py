@@ -216,3 +216,33 @@ def test_quantize_act_bf16_input_bit_exact(nv, m, k):
     xq, xs = nv.quantize_act(bf16_tensor(bits), dev(np.array([gx], np.float32)))
     np.testing.assert_array_equal(host(xq), oq)
     np.testing.assert_array_equal(host(xs), os_)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("m,k", [(1, 16), (3, 16 * 37), (1, 4096), (8, 12288), (2, 25600)])
+def test_quantize_act_pdl_chain_bit_exact(nv, m, k, bf16):
+    """The programmatic-dependent-launch form (it prefetches X into L2 before
+    waiting on X's producer), launched right after a kernel that writes X:
+    the codes are those of the X that kernel wrote, equal to the oracle's."""
+    x = synthetic.activations(m, k, seed=3000 + m + k)
+    stale = np.full_like(x, 1e4)           # what X holds before the producer runs
+    if bf16:
+        bits = oracle.f32_to_bf16(x)
+        xv = oracle.bf16_to_f32(bits)
+        xd = bf16_tensor(oracle.f32_to_bf16(stale))
+        src = bf16_tensor(bits)
+    else:
+        xv = x
+        xd = dev(stale)
+        src = dev(x)
+    gx = oracle.global_scale(xv)
+    oq, os_ = oracle.quantize(xv, gx)
+    g = dev(np.array([gx], np.float32))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        xd.zero_()
+        xd.add_(src)                        # the producer of X: a kernel on the same stream
+        xq, xs = nv.quantize_act(xd, g, pdl=True)
+        np.testing.assert_array_equal(host(xq), oq)
+        np.testing.assert_array_equal(host(xs), os_)
+        xd.fill_(1e4)
