@@ -309,7 +309,7 @@ int nvfp4_linear_ws(const void* x, int64_t m, int64_t n, int64_t k, const float*
 /*
  * Read-only streaming probe, a measurement aid with no counterpart in the
  * method: the DRAM read rate a plain stream of 128-bit loads reaches on this
- * device, the ceiling next to which the GEMM's weight stream is judged.
+ * device, the ceiling the GEMM's weight stream is compared with.
  *   buf    device, `bytes` bytes (16-byte aligned; read-only, not owned)
  *   bytes  a multiple of 16 (0: only the sink is written)
  *   sink   device uint64_t[1] (8-byte aligned), OUTPUT: zeroed on the stream,
