@@ -169,6 +169,9 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       streams w_q/w_s before waiting.  Set it only when the
  *                       work queued just before the call does not write the
  *                       weights (true in decode, where weights are constant).
+ *                       (The activation quantiser also asks L2 to prefetch x
+ *                       before waiting; a prefetch reads nothing into the
+ *                       kernel, and x itself is loaded after the wait.)
  */
 #define NVFP4_KERNEL_AUTO 0u
 #define NVFP4_KERNEL_GENERIC 1u
