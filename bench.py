@@ -748,7 +748,11 @@ def cpu_baseline(budget_s: float = 12.0, all_cores: bool = True) -> dict:
     layer_s = sec / layers if rows >= max(lin.n for lin in synthetic.LINEARS_8B) else \
         sec * sum(lin.n * lin.k for lin in synthetic.LINEARS_8B) / \
         sum(min(rows, lin.n) * lin.k for lin in synthetic.LINEARS_8B)
-    line = cpu_baseline_all_cores(layer_s, budget_s)
+    try:
+        line = cpu_baseline_all_cores(layer_s, budget_s)
+    except Exception as e:  # the single-thread line still stands
+        single["all_cores_error"] = f"{type(e).__name__}: {e}"[:200]
+        return single
     line["single_thread"] = single
     return line
 
