@@ -551,7 +551,7 @@ def run_ours(args) -> dict:
     probe_gbs = read_probe_gbs(nv, torch)
 
     # ---- end to end: pinned host X in, host Y out, through the public API
-    e2e = run_e2e(torch, stack, step_graph, args)
+    e2e = run_e2e(torch, stack, step_graph, args, world)
     sweep_detail = None if args.no_sweep else sweep(nv, torch, stack, peaks, args)
 
     # the committed capture is of the default step (M = 1, FP32 I/O, two launches)
@@ -591,16 +591,17 @@ def run_ours(args) -> dict:
                    "step_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                    "sweep": sweep_detail},
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # rank 0 at N = 1 only
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     return line if rank == 0 else None
 
 
-def run_e2e(torch, stack, step_graph, args) -> dict:
+def run_e2e(torch, stack, step_graph, args, world: int = 1) -> dict:
     """End to end through the public API: every step copies all of its
     activations from pinned host memory to the device, replays the step (the
     same graph of C-ABI calls) and reads all of its outputs back to pinned host
-    memory -- both copies inside the timed region."""
+    memory -- both copies inside the timed region.  With several ranks: a
+    barrier on both sides, the slowest rank's time, all ranks' bytes."""
     x_host = stack.x_flat.cpu().pin_memory()
     y_host = torch.empty(stack.y_flat.shape, dtype=stack.y_flat.dtype).pin_memory()
     h2d = x_host.numel() * x_host.element_size()
@@ -615,13 +616,16 @@ def run_e2e(torch, stack, step_graph, args) -> dict:
         one_step()
     torch.cuda.synchronize()
     reps = max(10, args.steps // 3)
+    barrier(world)
     t0 = time.perf_counter()
     for _ in range(reps):
         one_step()
     torch.cuda.synchronize()
     sec = (time.perf_counter() - t0) / reps
+    barrier(world)
+    sec = reduce_max(sec, world)
     b = stack.bytes_per_step()
-    v = (b["gemm"] + b["quant"]) / sec / 1e9
+    v = world * (b["gemm"] + b["quant"]) / sec / 1e9
     return {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3),
             "path": "per step: pinned H2D of all activations, the step's CUDA graph of "
