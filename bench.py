@@ -174,10 +174,20 @@ def job_throughput(bytes_per_rank_step: float, ms_step_max: float, world: int) -
 
 class DecodeStack:
     """36 layers x 4 linears of packed weights resident in HBM, per-call
-    activation buffers, and the graphs that replay them."""
+    activation buffers, and the graphs that replay them.
+
+    Two ways to run a step:
+    * ``launches``: every linear is its own nvfp4_linear call (quantiser +
+      GEMM, programmatic dependent launch between them), one (x_q, x_s) pair
+      per linear shape shared by all layers and one workspace shared by all
+      calls -- the form a model whose linears depend on each other needs;
+    * ``chain``: the step's 144 independent linears as one nvfp4_linear_chain
+      call (one quantiser launch for all of them, one persistent GEMM launch),
+      each linear with its own (x_q, x_s) -- the synthetic step's inputs are
+      all known when it starts.  M of 1 or 2."""
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
-                 fused: bool = True, kernel: int = 0, bf16: bool = False):
+                 fused: bool = True, kernel: int = 0, bf16: bool = False, mode: str = "launches"):
         self.nv, self.torch = nv, torch
         self.m = m
         self.bf16 = bf16   # BF16 activations in and BF16 outputs out
@@ -186,19 +196,23 @@ class DecodeStack:
         self.fused = fused
         self.kernel = kernel
         self.layers = layers
+        self.seed = seed
         self.lins = synthetic.LINEARS_8B
+        if mode not in ("launches", "chain"):
+            raise ValueError(f"unknown mode {mode}")
+        self.has_chain = all(nv.chain_supported(m, lin.n, lin.k) for lin in self.lins)
+        if mode == "chain" and not self.has_chain:
+            raise ValueError(f"the chain does not take M = {m}")
+        self.mode = mode
         # one workspace for every call of the step (calls run one after another)
         wsz = max(nv.gemm_workspace_size(m, lin.n, lin.k, kernel) for lin in self.lins)
         self.workspace = (torch.zeros(wsz, dtype=torch.uint8, device="cuda") if wsz else None)
         dev = torch.device("cuda")
-        gen = torch.Generator(device=dev)
         self.w = []          # [layer][j] -> (wq, ws, wg)
         for l in range(layers):
             row = []
             for j, lin in enumerate(self.lins):
-                gen.manual_seed(synthetic.weight_seed(seed, l, j))
-                wf = torch.randn((lin.n, lin.k), generator=gen, device=dev, dtype=torch.float32)
-                wf.mul_(synthetic.WEIGHT_STD_8B)
+                wf = self.weight_fp32(l, j)
                 row.append(nv.pack_weight(wf))
                 del wf
             self.w.append(row)
@@ -227,16 +241,64 @@ class DecodeStack:
             self.x.append(xr)
             self.xg.append(gr)
             self.y.append(yr)
+        # launches: one activation-code buffer pair per linear shape, shared by
+        # the layers
         self.xq = [(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
                     torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev)) for lin in self.lins]
+        self.chain = None
+        if self.has_chain:
+            # chain: one pair per linear (every linear of the step is in flight)
+            self.xq_item = [[(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
+                              torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev))
+                             for lin in self.lins] for _ in range(layers)]
+            self.chain = nv.Chain([self._chain_entry(l, j) for l in range(layers)
+                                   for j in range(4)])
+            self.chain_j = [nv.Chain([self._chain_entry(l, j) for l in range(layers)])
+                            for j in range(4)]
         torch.cuda.synchronize()
+
+    def _chain_entry(self, l: int, j: int):
+        return (self.x[l][j], self.xg[l][j], self.xq_item[l][j], self.w[l][j], self.y[l][j])
+
+    def weight_fp32(self, l: int, j: int):
+        """FP32 weights of linear j of layer l, drawn on the device: N(0, 0.02^2),
+        torch's generator seeded per linear (the packed copy is made from
+        exactly this tensor)."""
+        torch = self.torch
+        lin = self.lins[j]
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(synthetic.weight_seed(self.seed, l, j))
+        wf = torch.randn((lin.n, lin.k), generator=gen, device="cuda", dtype=torch.float32)
+        wf.mul_(synthetic.WEIGHT_STD_8B)
+        return wf
+
+    def codes(self, l: int, j: int):
+        """The (x_q, x_s) buffers the step's linear j of layer l writes."""
+        return self.xq_item[l][j] if self.mode == "chain" else self.xq[j]
 
     def chosen(self, lin) -> int:
         """Kernel id the step's calls of this linear run."""
+        if self.mode == "chain":
+            return self.nv.KERNEL_GEMV
         wsz = self.workspace.numel() if self.workspace is not None else 0
         return self.nv.gemm_select(self.m, lin.n, lin.k, self.kernel, wsz)
 
+    def launches_per_step(self) -> int:
+        if self.mode == "chain":
+            pieces = -(-4 * self.layers // self.nv.CHAIN_MAX_LINEARS)
+            return 2 * pieces
+        return sum(1 if (self.fused and self.chosen(lin) == self.nv.KERNEL_GEMV) else 2
+                   for lin in self.lins) * self.layers
+
+    def gemm_launches_per_step(self) -> int:
+        if self.mode == "chain":
+            return -(-4 * self.layers // self.nv.CHAIN_MAX_LINEARS)
+        return 4 * self.layers
+
     def step(self):
+        if self.mode == "chain":
+            self.chain.run(pdl=self.pdl)
+            return
         nv = self.nv
         for l in range(self.layers):
             for j in range(4):
@@ -247,6 +309,9 @@ class DecodeStack:
 
     def linear_only(self, j: int):
         """The step's calls of linear j only (quantise + GEMM each)."""
+        if self.mode == "chain":
+            self.chain_j[j].run(pdl=self.pdl)
+            return
         nv = self.nv
         for l in range(self.layers):
             wq, ws, wg = self.w[l][j]
@@ -257,14 +322,18 @@ class DecodeStack:
     def quantize_only(self, j: int):
         """The step's activation quantisations of linear j only."""
         for l in range(self.layers):
-            self.nv.quantize_act(self.x[l][j], self.xg[l][j], out=self.xq[j], pdl=self.pdl)
+            self.nv.quantize_act(self.x[l][j], self.xg[l][j], out=self.codes(l, j), pdl=self.pdl)
 
     def quantize_all(self):
-        """Fill the per-shape activation buffers (before GEMM-only timing)."""
-        for j in range(4):
-            self.nv.quantize_act(self.x[-1][j], self.xg[-1][j], out=self.xq[j])
+        """Fill the activation-code buffers (before GEMM-only timing)."""
+        for l in range(self.layers):
+            for j in range(4):
+                self.nv.quantize_act(self.x[l][j], self.xg[l][j], out=self.codes(l, j))
 
     def gemm_only(self, j=None):
+        if self.mode == "chain":
+            (self.chain if j is None else self.chain_j[j]).gemm_only(pdl=self.pdl)
+            return
         nv = self.nv
         for l in range(self.layers):
             for jj in (range(4) if j is None else (j,)):
@@ -483,8 +552,14 @@ def run_ours(args) -> dict:
     nv.library()
     peaks = load_peaks()
 
+    mode = args.mode
+    if mode == "auto":
+        chain_ok = args.m <= 2 and not args.fused and args.kernel == "auto" and all(
+            nv.chain_supported(args.m, lin.n, lin.k) for lin in synthetic.LINEARS_8B)
+        mode = "chain" if chain_ok else "launches"
     stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
-                        fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16)
+                        fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16,
+                        mode=mode)
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -492,8 +567,7 @@ def run_ours(args) -> dict:
             step_graph.replay()
         torch.cuda.synchronize()
         return None
-    launches_per_step = sum(1 if (stack.fused and stack.chosen(lin) == nv.KERNEL_GEMV) else 2
-                            for lin in stack.lins) * stack.layers
+    launches_per_step = stack.launches_per_step()
     bytes_step = stack.bytes_per_step()
     alg_step = bytes_step["gemm"] + bytes_step["quant"]
 
@@ -524,17 +598,18 @@ def run_ours(args) -> dict:
     stack.quantize_all()
     gemm_graph = stack.capture(stack.gemm_only)
     ms_gemm = time_graph(torch, gemm_graph, reps=max(3, args.steps // 2))
-    gemm_launches = 4 * stack.layers
+    del gemm_graph
+    gemm_launches = stack.gemm_launches_per_step()
     gemm_avg_us = ms_gemm * 1e3 / gemm_launches
     gemm_bytes_per_launch = bytes_step["gemm"] / gemm_launches
     achieved = gemm_bytes_per_launch / (gemm_avg_us * 1e-6) / 1e9
 
     per_linear = {}
+    io = 2 if stack.bf16 else 4
     for j, lin in enumerate(stack.lins):
         g = stack.capture(lambda j=j: stack.gemm_only(j))
         ms = time_graph(torch, g, reps=max(3, args.steps // 2))
         us = ms * 1e3 / stack.layers
-        io = 2 if stack.bf16 else 4
         b = algorithmic_bytes(args.m, lin.n, lin.k, io, io)["gemm"]
         gbs = b / (us * 1e-6) / 1e9
         gq = stack.capture(lambda j=j: stack.quantize_only(j))
@@ -548,15 +623,32 @@ def run_ours(args) -> dict:
                                 "quantize_us_per_call": round(us_q, 3),
                                 "quantize_plus_gemm_us_per_call": round(us_p, 3)}
         del g, gq, gp
+    # the other way of running the same step, on the same weights
+    other = None
+    alt = "launches" if mode == "chain" else ("chain" if stack.has_chain else None)
+    if alt is not None:
+        stack.mode = alt
+        g_alt = stack.capture(stack.step)
+        ms_alt = time_graph(torch, g_alt, reps=max(3, args.steps // 2))
+        stack.quantize_all()
+        g_alt_gemm = stack.capture(stack.gemm_only)
+        ms_alt_gemm = time_graph(torch, g_alt_gemm, reps=max(3, args.steps // 2))
+        other = {"mode": alt, "ms_per_step": round(ms_alt, 4),
+                 "GBps": round(alg_step / (ms_alt * 1e-3) / 1e9, 1),
+                 "gemm_only_ms_per_step": round(ms_alt_gemm, 4),
+                 "launches_per_step": stack.launches_per_step()}
+        del g_alt, g_alt_gemm
+        stack.mode = mode
     probe_gbs = read_probe_gbs(nv, torch)
 
     # ---- end to end: pinned host X in, host Y out, through the public API
     e2e = run_e2e(torch, stack, step_graph, args, world)
     sweep_detail = None if args.no_sweep else sweep(nv, torch, stack, peaks, args)
 
-    # the committed capture is of the default step (M = 1, FP32 I/O, two launches)
+    # the committed traffic capture is of the default step's GEMM kernel
     default_step = args.m == 1 and not args.bf16 and not args.fused and args.kernel == "auto"
-    traffic = profile_traffic("gemm_smallm") if default_step else None
+    traffic_name = "gemm_chain" if mode == "chain" else "gemm_smallm"
+    traffic = profile_traffic(traffic_name) if default_step else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4),
@@ -569,16 +661,19 @@ def run_ours(args) -> dict:
                    "l2": "inputs larger than L2: 3.9 GB of packed weights per step",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "graph": "one CUDA graph per step",
+                   "mode": mode,
                    "pdl": not args.no_pdl,
                    "fused_quantize": args.fused,
                    "io": "bf16 X in, bf16 Y out" if args.bf16 else "fp32 X in, fp32 Y out"},
-        "roofline": {"bound": "hbm", "kernel": "nvfp4_gemm_smallm",
+        "roofline": {"bound": "hbm",
+                     "kernel": "nvfp4_gemm_chain" if mode == "chain" else "nvfp4_gemm_smallm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": traffic,
                      "bytes_per_launch": round(gemm_bytes_per_launch),
                      "avg_launch_us": round(gemm_avg_us, 3),
+                     "launches_per_step": gemm_launches,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                      "read_probe_gbs": round(probe_gbs, 1),
                      "frac_of_read_probe": round(achieved / probe_gbs, 4)},
@@ -586,13 +681,20 @@ def run_ours(args) -> dict:
         "clocks": clocks.summary(),
         "e2e": e2e,
         "wall_s_timed": round(wall, 4),
-        "detail": {"per_linear_m1": per_linear,
+        "detail": {"per_linear_m1" if args.m == 1 else f"per_linear_m{args.m}": per_linear,
                    "step_frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
                    "step_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+                   "other_mode": other,
                    "sweep": sweep_detail},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # rank 0 at N = 1 only
+        # the oracle on the host: the timed baseline, then a check of sampled
+        # outputs of the timed step against it (outside every timed region)
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+        line["parity"] = step_parity(stack)
+        if not line["parity"]["ok"]:
+            print(json.dumps(line), flush=True)
+            raise SystemExit("the decode step's outputs disagree with the oracle")
     return line if rank == 0 else None
 
 
@@ -668,6 +770,59 @@ def kernel_source_hash() -> str:
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
+
+def step_parity(stack, layers=None, rows: int = 16, seed: int = 5) -> dict:
+    """Sampled outputs of the decode step the GPU just ran, against the oracle
+    (host side, after every timed region): for the first and last layer, all
+    four linears -- the oracle's tensor scales and activation codes compared
+    bit for bit with the GPU's (the step's x_q / x_s buffers), and ``rows``
+    output rows of every Y (rows 0 and n - 1 among them) with the FP64 result
+    the oracle computes from its own quantisation of X and of those weight
+    rows.  Error metric: max |y - ref| / max(|ref|, rms of the row of ref)."""
+    import oracle
+    torch = stack.torch
+    torch.cuda.synchronize()
+    if layers is None:
+        layers = sorted({0, stack.layers - 1})
+    rng = np.random.default_rng(seed)
+    tol = 1e-3 + (2.0 ** -8) * (1 + 1e-3) if stack.bf16 else 1e-3
+    worst, codes_ok, checked = 0.0, True, 0
+
+    def host_f32(t):
+        if t.dtype == torch.bfloat16:
+            return oracle.bf16_to_f32(t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+        return t.cpu().numpy()
+
+    for l in layers:
+        for j, lin in enumerate(stack.lins):
+            x = host_f32(stack.x[l][j])
+            gx = oracle.global_scale(x)
+            codes_ok &= bool(np.float32(stack.xg[l][j].cpu().numpy()[0]) == gx)
+            oxq, oxs = oracle.quantize(x, gx)
+            if stack.mode == "chain" or l == stack.layers - 1:   # shared buffers: last layer's
+                xq, xs = stack.codes(l, j)
+                codes_ok &= bool(np.array_equal(xq.cpu().numpy(), oxq) and
+                                 np.array_equal(xs.cpu().numpy(), oxs))
+            wf = stack.weight_fp32(l, j)
+            w = wf.cpu().numpy()
+            del wf
+            gw = oracle.global_scale(w)
+            codes_ok &= bool(np.float32(stack.w[l][j][2].cpu().numpy()[0]) == gw)
+            sel = np.unique(np.concatenate([[0, lin.n - 1], rng.integers(0, lin.n, rows - 2)]))
+            owq, ows = oracle.quantize(w[sel], gw)
+            del w
+            ref = oracle.gemm(oxq, oxs, gx, owq, ows, gw)
+            y = host_f32(stack.y[l][j])[:, sel].astype(np.float64)
+            rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+            den = np.maximum(np.abs(ref), rms)
+            den = np.where(den > 0, den, 1.0)
+            worst = max(worst, float(np.max(np.abs(y - ref) / den)))
+            checked += 1
+    return {"ok": bool(codes_ok and worst <= tol), "max_err": worst, "tol": tol,
+            "codes_bit_exact": codes_ok, "layers": layers, "rows_per_linear": rows,
+            "linears_checked": checked, "mode": stack.mode,
+            "metric": "max |y - ref| / max(|ref|, row rms of ref), ref = oracle FP64"}
+
 
 def oracle_sample(rows_per_linear: int, seed: int = 99, layers: int = 1, first_layer: int = 0):
     """Packed operands for a bounded sample of the workload: the four linears
@@ -968,6 +1123,9 @@ def main():
                     help="also time the shape-general kernel in the sweep")
     ap.add_argument("--single", type=int, nargs=3, metavar=("M", "N", "K"),
                     help="time one linear shape (for kernel-level profiling) and exit")
+    ap.add_argument("--mode", default="auto", choices=["auto", "chain", "launches"],
+                    help="the step as one multi-linear call (chain, M <= 2) or one call per "
+                         "linear (launches); auto: chain where it applies")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNELS),
                     help="GEMM kernel for the decode step (and for --single)")
     ap.add_argument("--reps", type=int, default=3)

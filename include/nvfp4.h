@@ -310,6 +310,80 @@ int nvfp4_linear_ws(const void* x, int64_t m, int64_t n, int64_t k, const float*
                     size_t workspace_bytes, void* stream);
 
 /*
+ * Many decode linears in one persistent launch.  The decode step of the
+ * ReSET README ("Core components" item 2; its trace figure decodes at batch 1
+ * under CUDA graphs) is a long sequence of small-M linears.  Launched one by
+ * one, each pays a launch, a ramp-up of its weight stream and a tail in which
+ * its last CTAs finish alone: a few microseconds per linear, comparable to
+ * the DRAM time of an 8B-shaped layer.  These entry points take a list of
+ * INDEPENDENT linears -- no linear reads another's output, all activations
+ * are ready when the call's work starts (the projections that share one
+ * input, the linears of several layers whose inputs are known, experts of a
+ * mixture) -- and stream all their weights in one persistent launch of the
+ * CUDA-core kernel, whose weight loads do not pause between linears.  Each
+ * output equals, bit for bit, that of the single-linear CUDA-core kernel
+ * (NVFP4_KERNEL_GEMV) for the same linear: the same per-output reduction
+ * order.  Linears that depend on each other need one call per linear
+ * (nvfp4_linear with NVFP4_FLAG_PDL).
+ *
+ *   x      activations [m][k]: FP32, or BF16 with NVFP4_FLAG_X_BF16
+ *          (nvfp4_linear_chain quantises them; nvfp4_gemm_chain ignores x)
+ *   x_g    activation tensor scale [1]
+ *   x_q    codes [m][k/2] and x_s block scales [m][k/16]: OUTPUTS of
+ *          nvfp4_linear_chain, INPUTS of nvfp4_gemm_chain
+ *   w_q, w_s, w_g   packed weights as for nvfp4_gemm_smallm
+ *   y      output [m][n]: FP32, or BF16 with NVFP4_FLAG_Y_BF16
+ *   n, k   n >= 0 (a linear with n == 0 is skipped); k a multiple of 1024,
+ *          at most 32768
+ * Every pointer is device memory; x_q and w_q 32-byte aligned, x_s and w_s
+ * 4-byte, x 16-byte (8 for BF16), y 4-byte (2 for BF16).  The y, x_q and x_s
+ * buffers of different linears must not overlap each other or any input of
+ * the call (all linears are in flight at once).
+ */
+typedef struct {
+    const void* x;
+    const float* x_g;
+    uint8_t* x_q;
+    uint8_t* x_s;
+    const uint8_t* w_q;
+    const uint8_t* w_s;
+    const float* w_g;
+    void* y;
+    int64_t n;
+    int64_t k;
+} nvfp4_chain_linear;
+
+/* Linears per launch: longer lists are cut into launches of this many. */
+#define NVFP4_CHAIN_MAX_LINEARS 256
+
+/*
+ * Quantise every linear's activations (one launch: the recipe of
+ * nvfp4_quantize_act, same bytes) and compute every Y (one persistent
+ * launch, which starts streaming weights before the codes are written and
+ * reads them once they are).  `linears` is a HOST array of `count`
+ * descriptions, read during the call only.  m must be 1 or 2 (the CUDA-core
+ * weight stream); other m in 3..8 return NVFP4_ERR_UNSUPPORTED, m > 8 too.
+ * options: NVFP4_FLAG_PDL (the first launch may start before the previous
+ * kernel on the stream ends; the weights must not be written by it),
+ * NVFP4_FLAG_X_BF16, NVFP4_FLAG_Y_BF16.  Every description is checked before
+ * anything is launched: NVFP4_ERR_INVALID_ARG for a null or misaligned
+ * pointer or a bad size, NVFP4_ERR_UNSUPPORTED for a shape the kernel does
+ * not take.  Asynchronous on `stream`; nothing allocated.
+ */
+int nvfp4_linear_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                       uint32_t options, void* stream);
+
+/* The GEMM half of nvfp4_linear_chain: x_q / x_s are inputs (quantised
+ * beforehand), x is not read; one launch per NVFP4_CHAIN_MAX_LINEARS
+ * linears.  options: NVFP4_FLAG_PDL, NVFP4_FLAG_Y_BF16. */
+int nvfp4_gemm_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                     uint32_t options, void* stream);
+
+/* 1 when a linear of shape (m, n, k) can be part of a chain, else 0.  Host
+ * only. */
+int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k);
+
+/*
  * Read-only streaming probe, a measurement aid with no counterpart in the
  * method: the DRAM read rate a plain stream of 128-bit loads reaches on this
  * device, the ceiling the GEMM's weight stream is compared with.

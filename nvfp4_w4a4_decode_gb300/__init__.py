@@ -26,6 +26,7 @@ __all__ = [
     "quantize_act", "gemm_smallm", "nvfp4_linear", "linear", "MAX_M",
     "nvfp4_gemm_workspace_size", "nvfp4_workspace", "gemm_workspace_size", "workspace",
     "nvfp4_gemm_smallm_static", "gemm_smallm_static", "nvfp4_read_probe", "read_probe",
+    "ChainLinear", "Chain", "CHAIN_MAX_LINEARS", "nvfp4_chain_supported", "chain_supported",
 ]
 
 MAX_M = 8
@@ -62,6 +63,9 @@ SIGNATURES = {
     "nvfp4_linear_ws": ([_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, ctypes.c_uint32, _p,
                          ctypes.c_size_t, _p], ctypes.c_int),
     "nvfp4_read_probe": ([_p, _i64, _p, _p], ctypes.c_int),
+    "nvfp4_linear_chain": ([_p, _i64, _i64, ctypes.c_uint32, _p], ctypes.c_int),
+    "nvfp4_gemm_chain": ([_p, _i64, _i64, ctypes.c_uint32, _p], ctypes.c_int),
+    "nvfp4_chain_supported": ([_i64, _i64, _i64], ctypes.c_int),
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA, KERNEL_SPLITK = 0, 1, 2, 3, 4, 5
@@ -338,6 +342,91 @@ def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=
 
 
 linear = nvfp4_linear
+
+
+# ---- many independent linears in one persistent launch ----------------------
+
+CHAIN_MAX_LINEARS = 256
+
+
+class ChainLinear(ctypes.Structure):
+    """``nvfp4_chain_linear`` of include/nvfp4.h (device pointers, sizes)."""
+    _fields_ = [("x", _p), ("x_g", _p), ("x_q", _p), ("x_s", _p), ("w_q", _p), ("w_s", _p),
+                ("w_g", _p), ("y", _p), ("n", _i64), ("k", _i64)]
+
+
+def nvfp4_chain_supported(m: int, n: int, k: int) -> bool:
+    """Whether a linear of this shape can be part of a chain."""
+    return bool(library().nvfp4_chain_supported(m, n, k))
+
+
+class Chain:
+    """A fixed list of independent linears run as one multi-linear call
+    (``nvfp4_linear_chain`` / ``nvfp4_gemm_chain``).
+
+    ``linears`` is a sequence of ``(x, xg, (xq, xs), (wq, ws, wg), y)``: x
+    [m, k] float32 or bfloat16 (the same dtype for every linear), xg [1]
+    float32, xq [m, k/2] / xs [m, k/16] uint8 (written by ``run``, read by
+    ``gemm_only``), the packed weights, and y [m, n] float32 or bfloat16 (the
+    same dtype for every linear).  The descriptions are built once; the
+    tensors must stay alive and in place while the chain is used."""
+
+    def __init__(self, linears):
+        if not linears:
+            raise ValueError("a chain needs at least one linear")
+        descs = []
+        self._keep = []
+        xdt = ydt = None
+        m = None
+        for x, xg, (xq, xs), (wq, ws, wg), y in linears:
+            if x.dtype not in (torch.float32, torch.bfloat16):
+                raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
+            _dev(x, x.dtype, "x")
+            _dev(xg, torch.float32, "xg")
+            for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
+                _dev(t, torch.uint8, name)
+            _dev(wg, torch.float32, "wg")
+            if y.dtype not in (torch.float32, torch.bfloat16):
+                raise ValueError(f"y must be float32 or bfloat16, got {y.dtype}")
+            _dev(y, y.dtype, "y")
+            mm, k = x.shape
+            n = wq.shape[0]
+            if (xq.shape != (mm, k // 2) or xs.shape != (mm, k // 16) or wq.shape != (n, k // 2)
+                    or ws.shape != (n, k // 16) or y.shape != (mm, n)):
+                raise ValueError("operand shapes disagree")
+            if m is None:
+                m, xdt, ydt = mm, x.dtype, y.dtype
+            elif mm != m or x.dtype != xdt or y.dtype != ydt:
+                raise ValueError("every linear of a chain has the same m and dtypes")
+            descs.append(ChainLinear(x.data_ptr(), xg.data_ptr(), xq.data_ptr(), xs.data_ptr(),
+                                     wq.data_ptr(), ws.data_ptr(), wg.data_ptr(), y.data_ptr(),
+                                     n, k))
+            self._keep.append((x, xg, xq, xs, wq, ws, wg, y))
+        self.m = m
+        self.count = len(descs)
+        self._arr = (ChainLinear * self.count)(*descs)
+        self._flags = (FLAG_X_BF16 if xdt == torch.bfloat16 else 0) | \
+                      (FLAG_Y_BF16 if ydt == torch.bfloat16 else 0)
+        self.device = linears[0][0].device
+
+    def run(self, pdl: bool = False):
+        """Quantise every linear's X and compute every Y (two launches per
+        CHAIN_MAX_LINEARS linears) on the current stream."""
+        _check("nvfp4_linear_chain", library().nvfp4_linear_chain(
+            ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
+            self._flags | (FLAG_PDL if pdl else 0),
+            torch.cuda.current_stream(self.device).cuda_stream))
+
+    def gemm_only(self, pdl: bool = False):
+        """Every Y from the codes already in each xq / xs (one launch per
+        CHAIN_MAX_LINEARS linears)."""
+        _check("nvfp4_gemm_chain", library().nvfp4_gemm_chain(
+            ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
+            (self._flags & FLAG_Y_BF16) | (FLAG_PDL if pdl else 0),
+            torch.cuda.current_stream(self.device).cuda_stream))
+
+
+chain_supported = nvfp4_chain_supported
 
 
 global_scale = nvfp4_global_scale

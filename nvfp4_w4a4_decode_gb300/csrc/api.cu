@@ -341,6 +341,93 @@ int64_t nvfp4_gemm_static_scratch_bytes(void)
     return nvfp4::splitk_static_scratch_bytes();
 }
 
+namespace {
+
+// Checks of a multi-linear call; on success the host descriptions of its
+// linears with n >= 1 (linears with n == 0 compute nothing and are dropped).
+int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t options,
+                bool quantize, nvfp4::ChainLinear* out, int64_t* kept)
+{
+    const bool x_bf16 = (options & NVFP4_FLAG_X_BF16) != 0;
+    const bool y_bf16 = (options & NVFP4_FLAG_Y_BF16) != 0;
+    *kept = 0;
+    for (int64_t i = 0; i < count; ++i) {
+        const nvfp4_chain_linear& L = linears[i];
+        if (L.n < 0 || L.k < 0 || (L.k % 16) != 0)
+            return NVFP4_ERR_INVALID_ARG;
+        if (L.n == 0)
+            continue;
+        if (!nvfp4::chain_shape_ok(m, L.n, L.k))
+            return NVFP4_ERR_UNSUPPORTED;
+        if (L.x_q == nullptr || L.x_s == nullptr || L.x_g == nullptr || L.w_q == nullptr ||
+            L.w_s == nullptr || L.w_g == nullptr || L.y == nullptr ||
+            (quantize && L.x == nullptr))
+            return NVFP4_ERR_INVALID_ARG;
+        if (!aligned(L.x_q, 32) || !aligned(L.w_q, 32) || !aligned(L.x_s, 4) ||
+            !aligned(L.w_s, 4) || !aligned(L.x_g, 4) || !aligned(L.w_g, 4) ||
+            !aligned(L.y, y_bf16 ? 2 : 4) || (quantize && !aligned(L.x, x_bf16 ? 8 : 16)))
+            return NVFP4_ERR_INVALID_ARG;
+        out[*kept] = {L.x, L.x_g, L.x_q, L.x_s, L.w_q, L.w_s, L.w_g, L.y, L.n, L.k};
+        ++*kept;
+    }
+    return NVFP4_OK;
+}
+
+int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t options,
+          void* stream, bool quantize)
+{
+    const uint32_t allowed = NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 | (quantize ? NVFP4_FLAG_X_BF16 : 0u);
+    if (count < 0 || m < 0 || (count > 0 && linears == nullptr) || (options & ~allowed) != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (m > 8)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (count == 0 || m == 0)
+        return NVFP4_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
+    // one launch (or launch pair) per kChainMaxItems linears, checked first
+    nvfp4::ChainLinear part[nvfp4::kChainMaxItems];
+    for (int64_t i0 = 0; i0 < count; i0 += nvfp4::kChainMaxItems) {
+        const int64_t cnt = count - i0 < nvfp4::kChainMaxItems ? count - i0 : nvfp4::kChainMaxItems;
+        int64_t kept = 0;
+        const int st = check_chain(linears + i0, cnt, m, options, quantize, part, &kept);
+        if (st != NVFP4_OK)
+            return st;
+    }
+    for (int64_t i0 = 0; i0 < count; i0 += nvfp4::kChainMaxItems) {
+        const int64_t cnt = count - i0 < nvfp4::kChainMaxItems ? count - i0 : nvfp4::kChainMaxItems;
+        int64_t kept = 0;
+        check_chain(linears + i0, cnt, m, options, quantize, part, &kept);
+        if (kept == 0)
+            continue;
+        const cudaError_t e = nvfp4::launch_linear_chain(
+            part, (int)kept, (int)m, quantize, (options & NVFP4_FLAG_X_BF16) != 0,
+            (options & NVFP4_FLAG_Y_BF16) != 0, s, pdl || i0 > 0);
+        if (e != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+int nvfp4_linear_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                       uint32_t options, void* stream)
+{
+    return chain(linears, count, m, options, stream, true);
+}
+
+int nvfp4_gemm_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                     uint32_t options, void* stream)
+{
+    return chain(linears, count, m, options, stream, false);
+}
+
+int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k)
+{
+    return nvfp4::chain_shape_ok(m, n, k) ? 1 : 0;
+}
+
 int nvfp4_read_probe(const void* buf, int64_t bytes, uint64_t* sink, void* stream)
 {
     if (bytes < 0 || bytes % 16 != 0 || sink == nullptr || !aligned(sink, 8) ||

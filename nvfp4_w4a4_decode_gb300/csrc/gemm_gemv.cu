@@ -37,6 +37,7 @@
 #include "formats.cuh"
 #include "kernels.cuh"
 #include "launch_cache.cuh"
+#include "stream_core.cuh"
 
 namespace nvfp4 {
 
@@ -87,32 +88,6 @@ struct GemvParams {
     int G;  // threads per row
     int P;  // rows per group
 };
-
-__device__ __forceinline__ uint32_t ld_u16_nc(const uint8_t* p)
-{
-    unsigned short v;
-    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return v;
-}
-
-// Two E4M3 bytes (low 16 bits) -> two floats, exact.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two)
-{
-    uint32_t h;
-    asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
-        : "=r"(h)
-        : "r"(two));
-    return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
-
-// One step of a butterfly reduce-scatter over lanes: lanes with `upper`
-// clear keep a (adding the partner's a), lanes with it set keep b.
-__device__ __forceinline__ float rs_step(float a, float b, int bit, bool upper)
-{
-    const float send = upper ? a : b;
-    const float keep = upper ? b : a;
-    return keep + __shfl_xor_sync(0xFFFFFFFFu, send, bit);
-}
 
 template <int M, int STAGES, int MAXT, int MINB, bool PDL, bool FUSED>
 __global__ void __launch_bounds__(MAXT) __maxnreg__(gemv_reg_cap(M, MAXT, MINB))

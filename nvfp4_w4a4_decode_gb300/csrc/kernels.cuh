@@ -94,6 +94,39 @@ int64_t splitk_static_scratch_bytes();
 bool splitk_static_fits(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_gemm_splitk_static(const GemmArgs& a, bool pdl);
 
+// One linear of a multi-linear launch (host-side description; every pointer
+// is device memory).  x is FP32 or BF16 (launch-wide flag); xq / xs are the
+// quantised activations (written by the launch's quantiser, or inputs when it
+// has none); y is FP32 or BF16 (launch-wide flag).
+struct ChainLinear {
+    const void* x;
+    const float* xg;
+    uint8_t* xq;
+    uint8_t* xs;
+    const uint8_t* wq;
+    const uint8_t* ws;
+    const float* wg;
+    void* y;
+    int64_t n;
+    int64_t k;
+};
+
+// Linears per launch of the multi-linear kernels (their descriptions travel
+// in the kernel parameters).
+constexpr int kChainMaxItems = 256;
+
+// Whether a linear of this shape can be part of a multi-linear launch: M of
+// 1 or 2, K a multiple of 1024 up to 32768, N below 2^30.
+bool chain_shape_ok(int64_t m, int64_t n, int64_t k);
+
+// 1 <= count <= kChainMaxItems linears (each with n >= 1) in one persistent
+// CUDA-core weight-streaming launch, preceded (quantize) by one launch that
+// quantises every linear's activations.  Operands aligned as for the
+// single-linear CUDA-core kernel; the y, xq and xs buffers of different
+// linears must not overlap.
+cudaError_t launch_linear_chain(const ChainLinear* items, int count, int m, bool quantize,
+                                bool x_bf16, bool y_bf16, cudaStream_t stream, bool pdl);
+
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
 
 // Read-only streaming probe: zeroes *sink on the stream, then loads every
