@@ -743,24 +743,28 @@ def profile_traffic(kernel: str):
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("source_hash") != kernel_source_hash():
+        if d.get("source_hash") != kernel_source_hash(kernel):
             return None
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None
 
 
-# the sources the M = 1 step's kernels (activation quantiser, CUDA-core
-# stream) and their launch path are built from
-TRAFFIC_SOURCES = ("api.cu", "formats.cuh", "gemm_gemv.cu", "kernels.cuh", "launch_cache.cuh",
-                   "quantize.cu")
+# the sources each measured kernel (with the activation quantiser before it)
+# and its launch path are built from
+TRAFFIC_SOURCES = {
+    "gemm_smallm": ("api.cu", "formats.cuh", "gemm_gemv.cu", "kernels.cuh", "launch_cache.cuh",
+                    "quantize.cu", "stream_core.cuh"),
+    "gemm_chain": ("api.cu", "formats.cuh", "gemm_chain.cu", "kernels.cuh", "launch_cache.cuh",
+                   "stream_core.cuh"),
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "gemm_smallm") -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_w4a4_decode_gb300", "csrc")
-    for name in TRAFFIC_SOURCES:
+    for name in TRAFFIC_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
