@@ -187,7 +187,8 @@ class DecodeStack:
       all known when it starts.  M of 1 or 2."""
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
-                 fused: bool = True, kernel: int = 0, bf16: bool = False, mode: str = "launches"):
+                 fused: bool = True, kernel: int = 0, bf16: bool = False, mode: str = "launches",
+                 chain_kernel: int = 0):
         self.nv, self.torch = nv, torch
         self.m = m
         self.bf16 = bf16   # BF16 activations in and BF16 outputs out
@@ -197,6 +198,7 @@ class DecodeStack:
         self.kernel = kernel
         self.layers = layers
         self.seed = seed
+        self.chain_kernel = chain_kernel   # the chain's engine (0: the library's choice)
         self.lins = synthetic.LINEARS_8B
         if mode not in ("launches", "chain"):
             raise ValueError(f"unknown mode {mode}")
@@ -252,9 +254,9 @@ class DecodeStack:
                               torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev))
                              for lin in self.lins] for _ in range(layers)]
             self.chain = nv.Chain([self._chain_entry(l, j) for l in range(layers)
-                                   for j in range(4)])
-            self.chain_j = [nv.Chain([self._chain_entry(l, j) for l in range(layers)])
-                            for j in range(4)]
+                                   for j in range(4)], kernel=chain_kernel)
+            self.chain_j = [nv.Chain([self._chain_entry(l, j) for l in range(layers)],
+                                     kernel=chain_kernel) for j in range(4)]
         torch.cuda.synchronize()
 
     def _chain_entry(self, l: int, j: int):
@@ -279,20 +281,19 @@ class DecodeStack:
     def chosen(self, lin) -> int:
         """Kernel id the step's calls of this linear run."""
         if self.mode == "chain":
-            return self.nv.KERNEL_GEMV
+            return self.chain.engine
         wsz = self.workspace.numel() if self.workspace is not None else 0
         return self.nv.gemm_select(self.m, lin.n, lin.k, self.kernel, wsz)
 
     def launches_per_step(self) -> int:
         if self.mode == "chain":
-            pieces = -(-4 * self.layers // self.nv.CHAIN_MAX_LINEARS)
-            return 2 * pieces
+            return self.chain.launches()
         return sum(1 if (self.fused and self.chosen(lin) == self.nv.KERNEL_GEMV) else 2
                    for lin in self.lins) * self.layers
 
     def gemm_launches_per_step(self) -> int:
         if self.mode == "chain":
-            return -(-4 * self.layers // self.nv.CHAIN_MAX_LINEARS)
+            return self.chain.launches(quantize=False)
         return 4 * self.layers
 
     def step(self):
@@ -554,12 +555,12 @@ def run_ours(args) -> dict:
 
     mode = args.mode
     if mode == "auto":
-        chain_ok = args.m <= 2 and not args.fused and args.kernel == "auto" and all(
+        chain_ok = not args.fused and args.kernel == "auto" and all(
             nv.chain_supported(args.m, lin.n, lin.k) for lin in synthetic.LINEARS_8B)
         mode = "chain" if chain_ok else "launches"
     stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
                         fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16,
-                        mode=mode)
+                        mode=mode, chain_kernel=KERNELS[args.chain_kernel](nv))
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -647,7 +648,8 @@ def run_ours(args) -> dict:
 
     # the committed traffic capture is of the default step's GEMM kernel
     default_step = args.m == 1 and not args.bf16 and not args.fused and args.kernel == "auto"
-    traffic_name = "gemm_chain" if mode == "chain" else "gemm_smallm"
+    traffic_name = ("gemm_chain" if stack.chosen(stack.lins[0]) == nv.KERNEL_GEMV else "gemm_tc") \
+        if mode == "chain" else "gemm_smallm"
     traffic = profile_traffic(traffic_name) if default_step else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -666,7 +668,8 @@ def run_ours(args) -> dict:
                    "fused_quantize": args.fused,
                    "io": "bf16 X in, bf16 Y out" if args.bf16 else "fp32 X in, fp32 Y out"},
         "roofline": {"bound": "hbm",
-                     "kernel": "nvfp4_gemm_chain" if mode == "chain" else "nvfp4_gemm_smallm",
+                     "kernel": (f"nvfp4_gemm_chain ({nv.KERNEL_NAMES[stack.chain.engine]})"
+                                if mode == "chain" else "nvfp4_gemm_smallm"),
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -757,6 +760,7 @@ TRAFFIC_SOURCES = {
                     "quantize.cu", "stream_core.cuh"),
     "gemm_chain": ("api.cu", "formats.cuh", "gemm_chain.cu", "kernels.cuh", "launch_cache.cuh",
                    "stream_core.cuh"),
+    "gemm_tc": ("api.cu", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh"),
 }
 
 
@@ -975,7 +979,8 @@ def cpu_baseline_all_cores(layer_seconds: float, budget_s: float = 12.0) -> dict
 
 KERNELS = {"auto": lambda nv: nv.KERNEL_AUTO, "generic": lambda nv: nv.KERNEL_GENERIC,
            "gemv": lambda nv: nv.KERNEL_GEMV, "mma": lambda nv: nv.KERNEL_MMA,
-           "tma": lambda nv: nv.KERNEL_TMA, "splitk": lambda nv: nv.KERNEL_SPLITK}
+           "tma": lambda nv: nv.KERNEL_TMA, "splitk": lambda nv: nv.KERNEL_SPLITK,
+           "tc": lambda nv: nv.KERNEL_TC}
 
 
 def run_single(args) -> None:
@@ -1130,6 +1135,9 @@ def main():
     ap.add_argument("--mode", default="auto", choices=["auto", "chain", "launches"],
                     help="the step as one multi-linear call (chain, M <= 2) or one call per "
                          "linear (launches); auto: chain where it applies")
+    ap.add_argument("--chain-kernel", default="auto", choices=["auto", "gemv", "tc"],
+                    help="engine of the chain step (auto: CUDA-core stream at M <= 2, "
+                         "tensor cores above)")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNELS),
                     help="GEMM kernel for the decode step (and for --single)")
     ap.add_argument("--reps", type=int, default=3)

@@ -147,9 +147,21 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       _ws entry points), so without one it takes only
  *                       K <= 4096.  The last partial of a tile to arrive sums
  *                       them in chunk order: results do not depend on timing.
+ * NVFP4_KERNEL_TC      the fifth-generation tensor-core kernel: tcgen05.mma
+ *                       kind::mxf4nvf4 (the FP4 codes and UE4M3 block scales
+ *                       go to the tensor core as they are; FP32 accumulation
+ *                       in tensor memory) with the operands swapped -- 128
+ *                       weight rows per MMA tile, the activation rows padded
+ *                       to 16 or 32 -- weights streamed by TMA through an
+ *                       8-stage shared-memory ring, one persistent CTA per SM.
+ *                       M up to 32 (this kernel only; M above 8 has to be
+ *                       requested by name), K a multiple of 256; one tile of
+ *                       128 rows x K per work unit, so a lone call occupies
+ *                       ceil(N / 128) SMs.  Results are exact sums up to FP32
+ *                       rounding in the tensor core's own order.
  *   The GEMV, MMA and SPLITK kernels need x_q/w_q 32-byte and x_s/w_s 4-byte
- *   aligned, the TMA kernel all four 32-byte aligned; a request a kernel
- *   cannot take returns NVFP4_ERR_UNSUPPORTED.
+ *   aligned, the TMA and TC kernels all four 32-byte aligned; a request a
+ *   kernel cannot take returns NVFP4_ERR_UNSUPPORTED.
  * NVFP4_FLAG_TEST_WAIT_TIMEOUT  test hook of the TMA kernel: the first stage
  *                       waits for 16 bytes that never come, so its bounded
  *                       wait runs out (after a few microseconds) and the
@@ -179,6 +191,7 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_KERNEL_MMA 3u
 #define NVFP4_KERNEL_TMA 4u
 #define NVFP4_KERNEL_SPLITK 5u
+#define NVFP4_KERNEL_TC 6u
 #define NVFP4_KERNEL_MASK 0xFFu
 #define NVFP4_FLAG_PDL 0x100u
 #define NVFP4_FLAG_FUSED_QUANTIZE 0x200u
@@ -319,12 +332,12 @@ int nvfp4_linear_ws(const void* x, int64_t m, int64_t n, int64_t k, const float*
  * INDEPENDENT linears -- no linear reads another's output, all activations
  * are ready when the call's work starts (the projections that share one
  * input, the linears of several layers whose inputs are known, experts of a
- * mixture) -- and stream all their weights in one persistent launch of the
- * CUDA-core kernel, whose weight loads do not pause between linears.  Each
- * output equals, bit for bit, that of the single-linear CUDA-core kernel
- * (NVFP4_KERNEL_GEMV) for the same linear: the same per-output reduction
- * order.  Linears that depend on each other need one call per linear
- * (nvfp4_linear with NVFP4_FLAG_PDL).
+ * mixture) -- and stream all their weights in one persistent launch (the
+ * CUDA-core stream or the tensor-core kernel), whose weight loads do not
+ * pause between linears.  On the CUDA-core stream each output equals, bit for
+ * bit, that of the single-linear NVFP4_KERNEL_GEMV for the same linear (the
+ * same per-output reduction order).  Linears that depend on each other need
+ * one call per linear (nvfp4_linear with NVFP4_FLAG_PDL).
  *
  *   x      activations [m][k]: FP32, or BF16 with NVFP4_FLAG_X_BF16
  *          (nvfp4_linear_chain quantises them; nvfp4_gemm_chain ignores x)
@@ -353,34 +366,48 @@ typedef struct {
     int64_t k;
 } nvfp4_chain_linear;
 
-/* Linears per launch: longer lists are cut into launches of this many. */
+/* Linears per launch: longer lists are cut into launches of this many
+ * (CUDA-core stream; tensor-core kernel). */
 #define NVFP4_CHAIN_MAX_LINEARS 256
+#define NVFP4_TC_MAX_LINEARS 160
 
 /*
  * Quantise every linear's activations (one launch: the recipe of
  * nvfp4_quantize_act, same bytes) and compute every Y (one persistent
  * launch, which starts streaming weights before the codes are written and
  * reads them once they are).  `linears` is a HOST array of `count`
- * descriptions, read during the call only.  m must be 1 or 2 (the CUDA-core
- * weight stream); other m in 3..8 return NVFP4_ERR_UNSUPPORTED, m > 8 too.
- * options: NVFP4_FLAG_PDL (the first launch may start before the previous
- * kernel on the stream ends; the weights must not be written by it),
- * NVFP4_FLAG_X_BF16, NVFP4_FLAG_Y_BF16.  Every description is checked before
- * anything is launched: NVFP4_ERR_INVALID_ARG for a null or misaligned
- * pointer or a bad size, NVFP4_ERR_UNSUPPORTED for a shape the kernel does
- * not take.  Asynchronous on `stream`; nothing allocated.
+ * descriptions, read during the call only.  options: a kernel choice in the
+ * low byte --
+ *   NVFP4_KERNEL_AUTO   the CUDA-core stream at m <= 2, the tensor-core
+ *                       kernel above;
+ *   NVFP4_KERNEL_GEMV   the CUDA-core stream: m of 1 or 2, k a multiple of
+ *                       1024 up to 32768 (each output bit-exact with the
+ *                       single-linear NVFP4_KERNEL_GEMV);
+ *   NVFP4_KERNEL_TC     the tensor-core kernel (NVFP4_KERNEL_TC above): m up
+ *                       to 32, k a multiple of 256, x_s and w_s 16-byte
+ *                       aligned; NVFP4_TC_MAX_LINEARS linears per launch
+ * -- OR-ed with NVFP4_FLAG_PDL (the first launch may start before the
+ * previous kernel on the stream ends; the weights must not be written by
+ * it), NVFP4_FLAG_X_BF16, NVFP4_FLAG_Y_BF16.  Every description is checked
+ * before anything is launched: NVFP4_ERR_INVALID_ARG for a null or
+ * misaligned pointer or a bad size, NVFP4_ERR_UNSUPPORTED for an m or shape
+ * the chosen kernel does not take.  Asynchronous on `stream`; nothing
+ * allocated.  The tensor-core kernel's waits are bounded: one that runs out
+ * (nothing in a correct call makes that happen) sets
+ * NVFP4_DEVICE_WAIT_TIMEOUT (nvfp4_device_status) and leaves Y unspecified.
  */
 int nvfp4_linear_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
                        uint32_t options, void* stream);
 
 /* The GEMM half of nvfp4_linear_chain: x_q / x_s are inputs (quantised
- * beforehand), x is not read; one launch per NVFP4_CHAIN_MAX_LINEARS
- * linears.  options: NVFP4_FLAG_PDL, NVFP4_FLAG_Y_BF16. */
+ * beforehand), x is not read; one launch per NVFP4_CHAIN_MAX_LINEARS (or
+ * NVFP4_TC_MAX_LINEARS) linears.  options: a kernel choice as above,
+ * NVFP4_FLAG_PDL, NVFP4_FLAG_Y_BF16. */
 int nvfp4_gemm_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
                      uint32_t options, void* stream);
 
-/* 1 when a linear of shape (m, n, k) can be part of a chain, else 0.  Host
- * only. */
+/* 1 when a linear of shape (m, n, k) can be part of a chain (on either
+ * kernel), else 0.  Host only. */
 int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k);
 
 /*

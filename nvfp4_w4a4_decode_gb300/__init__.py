@@ -69,8 +69,9 @@ SIGNATURES = {
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA, KERNEL_SPLITK = 0, 1, 2, 3, 4, 5
+KERNEL_TC = 6
 KERNEL_NAMES = {KERNEL_GENERIC: "generic", KERNEL_GEMV: "gemv", KERNEL_MMA: "mma",
-                KERNEL_TMA: "tma", KERNEL_SPLITK: "splitk"}
+                KERNEL_TMA: "tma", KERNEL_SPLITK: "splitk", KERNEL_TC: "tc"}
 FLAG_PDL = 0x100
 FLAG_FUSED_QUANTIZE = 0x200
 FLAG_X_BF16 = 0x400
@@ -347,6 +348,7 @@ linear = nvfp4_linear
 # ---- many independent linears in one persistent launch ----------------------
 
 CHAIN_MAX_LINEARS = 256
+TC_MAX_LINEARS = 160
 
 
 class ChainLinear(ctypes.Structure):
@@ -371,7 +373,7 @@ class Chain:
     same dtype for every linear).  The descriptions are built once; the
     tensors must stay alive and in place while the chain is used."""
 
-    def __init__(self, linears):
+    def __init__(self, linears, kernel: int = KERNEL_AUTO):
         if not linears:
             raise ValueError("a chain needs at least one linear")
         descs = []
@@ -408,21 +410,31 @@ class Chain:
         self._flags = (FLAG_X_BF16 if xdt == torch.bfloat16 else 0) | \
                       (FLAG_Y_BF16 if ydt == torch.bfloat16 else 0)
         self.device = linears[0][0].device
+        self.kernel = int(kernel)
+        if self.kernel == KERNEL_AUTO:
+            self.engine = KERNEL_GEMV if m <= 2 else KERNEL_TC
+        else:
+            self.engine = self.kernel
 
     def run(self, pdl: bool = False):
         """Quantise every linear's X and compute every Y (two launches per
         CHAIN_MAX_LINEARS linears) on the current stream."""
         _check("nvfp4_linear_chain", library().nvfp4_linear_chain(
             ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
-            self._flags | (FLAG_PDL if pdl else 0),
+            self.kernel | self._flags | (FLAG_PDL if pdl else 0),
             torch.cuda.current_stream(self.device).cuda_stream))
+
+    def launches(self, quantize: bool = True) -> int:
+        """Kernel launches of one call."""
+        per = TC_MAX_LINEARS if self.engine == KERNEL_TC else CHAIN_MAX_LINEARS
+        return -(-self.count // per) * (2 if quantize else 1)
 
     def gemm_only(self, pdl: bool = False):
         """Every Y from the codes already in each xq / xs (one launch per
-        CHAIN_MAX_LINEARS linears)."""
+        CHAIN_MAX_LINEARS, or TC_MAX_LINEARS, linears)."""
         _check("nvfp4_gemm_chain", library().nvfp4_gemm_chain(
             ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
-            (self._flags & FLAG_Y_BF16) | (FLAG_PDL if pdl else 0),
+            self.kernel | (self._flags & FLAG_Y_BF16) | (FLAG_PDL if pdl else 0),
             torch.cuda.current_stream(self.device).cuda_stream))
 
 

@@ -138,6 +138,9 @@ int select_kernel(int64_t m, int64_t n, int64_t k, uint32_t options, bool ptrs_o
                        nvfp4::splitk_plan_ok(m, n, k, ws_bytes)
                    ? (int)NVFP4_KERNEL_SPLITK
                    : -(int)NVFP4_ERR_UNSUPPORTED;
+    case NVFP4_KERNEL_TC:
+        return nvfp4::tc_shape_ok(m, n, k) && ptrs_ok_tma ? (int)NVFP4_KERNEL_TC
+                                                          : -(int)NVFP4_ERR_UNSUPPORTED;
     default: return -(int)NVFP4_ERR_UNSUPPORTED;
     }
 }
@@ -152,7 +155,8 @@ int check_gemm_args(int64_t m, int64_t n, int64_t k, uint32_t options)
         return NVFP4_ERR_INVALID_ARG;
     if ((options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) && (options & NVFP4_KERNEL_MASK) != NVFP4_KERNEL_TMA)
         return NVFP4_ERR_INVALID_ARG;
-    if (m > 8)
+    // M above 8 only on the tensor-core kernel, by request
+    if (m > ((options & NVFP4_KERNEL_MASK) == NVFP4_KERNEL_TC ? 32 : 8))
         return NVFP4_ERR_UNSUPPORTED;
     return NVFP4_OK;
 }
@@ -198,6 +202,8 @@ int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t
         return from_cuda(nvfp4::launch_gemm_tma(a, pdl, (options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) != 0));
     case NVFP4_KERNEL_SPLITK:
         return from_cuda(nvfp4::launch_gemm_splitk(a, pdl, workspace, ws_bytes));
+    case NVFP4_KERNEL_TC:
+        return from_cuda(nvfp4::launch_gemm_tc(a, pdl));
     default:
         return from_cuda(nvfp4::launch_gemm_generic(a));
     }
@@ -210,7 +216,7 @@ int nvfp4_gemm_select_ws(int64_t m, int64_t n, int64_t k, uint32_t options,
 {
     if (m < 1 || n < 1 || k < 16 || (k % 16) != 0)
         return -NVFP4_ERR_INVALID_ARG;
-    if (m > 8)
+    if (m > ((options & NVFP4_KERNEL_MASK) == NVFP4_KERNEL_TC ? 32 : 8))
         return -NVFP4_ERR_UNSUPPORTED;
     return select_kernel(m, n, k, options, true, true, (int64_t)workspace_bytes);
 }
@@ -224,7 +230,7 @@ int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t opti
 {
     if (m < 1 || n < 1 || k < 16 || (k % 16) != 0)
         return -NVFP4_ERR_INVALID_ARG;
-    if (m > 8)
+    if (m > ((options & NVFP4_KERNEL_MASK) == NVFP4_KERNEL_TC ? 32 : 8))
         return -NVFP4_ERR_UNSUPPORTED;
     const int kern = select_kernel(m, n, k, options, true, true, INT64_MAX);
     if (kern < 0)
@@ -343,13 +349,26 @@ int64_t nvfp4_gemm_static_scratch_bytes(void)
 
 namespace {
 
+// Engine of a multi-linear call: the CUDA-core stream (M of 1 or 2) or the
+// tensor-core kernel (M up to 32); AUTO takes the CUDA-core stream at M <= 2.
+int chain_engine(int64_t m, uint32_t options)
+{
+    const uint32_t req = options & NVFP4_KERNEL_MASK;
+    if (req == NVFP4_KERNEL_AUTO)
+        return m <= 2 ? (int)NVFP4_KERNEL_GEMV : (int)NVFP4_KERNEL_TC;
+    if (req == NVFP4_KERNEL_GEMV || req == NVFP4_KERNEL_TC)
+        return (int)req;
+    return -1;
+}
+
 // Checks of a multi-linear call; on success the host descriptions of its
 // linears with n >= 1 (linears with n == 0 compute nothing and are dropped).
 int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t options,
-                bool quantize, nvfp4::ChainLinear* out, int64_t* kept)
+                bool quantize, int engine, nvfp4::ChainLinear* out, int64_t* kept)
 {
     const bool x_bf16 = (options & NVFP4_FLAG_X_BF16) != 0;
     const bool y_bf16 = (options & NVFP4_FLAG_Y_BF16) != 0;
+    const bool tc = engine == (int)NVFP4_KERNEL_TC;
     *kept = 0;
     for (int64_t i = 0; i < count; ++i) {
         const nvfp4_chain_linear& L = linears[i];
@@ -357,14 +376,15 @@ int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uin
             return NVFP4_ERR_INVALID_ARG;
         if (L.n == 0)
             continue;
-        if (!nvfp4::chain_shape_ok(m, L.n, L.k))
+        if (!(tc ? nvfp4::tc_shape_ok(m, L.n, L.k) : nvfp4::chain_shape_ok(m, L.n, L.k)))
             return NVFP4_ERR_UNSUPPORTED;
         if (L.x_q == nullptr || L.x_s == nullptr || L.x_g == nullptr || L.w_q == nullptr ||
             L.w_s == nullptr || L.w_g == nullptr || L.y == nullptr ||
             (quantize && L.x == nullptr))
             return NVFP4_ERR_INVALID_ARG;
-        if (!aligned(L.x_q, 32) || !aligned(L.w_q, 32) || !aligned(L.x_s, 4) ||
-            !aligned(L.w_s, 4) || !aligned(L.x_g, 4) || !aligned(L.w_g, 4) ||
+        const uintptr_t sal = tc ? 16 : 4;  // the tensor-core kernel loads scales 16 bytes at a time
+        if (!aligned(L.x_q, 32) || !aligned(L.w_q, 32) || !aligned(L.x_s, sal) ||
+            !aligned(L.w_s, sal) || !aligned(L.x_g, 4) || !aligned(L.w_g, 4) ||
             !aligned(L.y, y_bf16 ? 2 : 4) || (quantize && !aligned(L.x, x_bf16 ? 8 : 16)))
             return NVFP4_ERR_INVALID_ARG;
         out[*kept] = {L.x, L.x_g, L.x_q, L.x_s, L.w_q, L.w_s, L.w_g, L.y, L.n, L.k};
@@ -376,33 +396,41 @@ int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uin
 int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t options,
           void* stream, bool quantize)
 {
-    const uint32_t allowed = NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 | (quantize ? NVFP4_FLAG_X_BF16 : 0u);
+    const uint32_t allowed = NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 |
+                             (quantize ? NVFP4_FLAG_X_BF16 : 0u);
     if (count < 0 || m < 0 || (count > 0 && linears == nullptr) || (options & ~allowed) != 0)
         return NVFP4_ERR_INVALID_ARG;
-    if (m > 8)
+    const int engine = chain_engine(m, options);
+    if (engine < 0)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (m > (engine == (int)NVFP4_KERNEL_TC ? 32 : 2))
         return NVFP4_ERR_UNSUPPORTED;
     if (count == 0 || m == 0)
         return NVFP4_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
-    // one launch (or launch pair) per kChainMaxItems linears, checked first
+    const int64_t per = engine == (int)NVFP4_KERNEL_TC ? nvfp4::kTcMaxItems : nvfp4::kChainMaxItems;
+    // one launch (or launch pair) per `per` linears, all checked first
     nvfp4::ChainLinear part[nvfp4::kChainMaxItems];
-    for (int64_t i0 = 0; i0 < count; i0 += nvfp4::kChainMaxItems) {
-        const int64_t cnt = count - i0 < nvfp4::kChainMaxItems ? count - i0 : nvfp4::kChainMaxItems;
+    for (int64_t i0 = 0; i0 < count; i0 += per) {
+        const int64_t cnt = count - i0 < per ? count - i0 : per;
         int64_t kept = 0;
-        const int st = check_chain(linears + i0, cnt, m, options, quantize, part, &kept);
+        const int st = check_chain(linears + i0, cnt, m, options, quantize, engine, part, &kept);
         if (st != NVFP4_OK)
             return st;
     }
-    for (int64_t i0 = 0; i0 < count; i0 += nvfp4::kChainMaxItems) {
-        const int64_t cnt = count - i0 < nvfp4::kChainMaxItems ? count - i0 : nvfp4::kChainMaxItems;
+    for (int64_t i0 = 0; i0 < count; i0 += per) {
+        const int64_t cnt = count - i0 < per ? count - i0 : per;
         int64_t kept = 0;
-        check_chain(linears + i0, cnt, m, options, quantize, part, &kept);
+        check_chain(linears + i0, cnt, m, options, quantize, engine, part, &kept);
         if (kept == 0)
             continue;
-        const cudaError_t e = nvfp4::launch_linear_chain(
-            part, (int)kept, (int)m, quantize, (options & NVFP4_FLAG_X_BF16) != 0,
-            (options & NVFP4_FLAG_Y_BF16) != 0, s, pdl || i0 > 0);
+        const bool xb = (options & NVFP4_FLAG_X_BF16) != 0, yb = (options & NVFP4_FLAG_Y_BF16) != 0;
+        const cudaError_t e =
+            engine == (int)NVFP4_KERNEL_TC
+                ? nvfp4::launch_tc_chain(part, (int)kept, (int)m, quantize, xb, yb, s, pdl || i0 > 0)
+                : nvfp4::launch_linear_chain(part, (int)kept, (int)m, quantize, xb, yb, s,
+                                             pdl || i0 > 0);
         if (e != cudaSuccess)
             return NVFP4_ERR_CUDA;
     }
@@ -425,7 +453,7 @@ int nvfp4_gemm_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m
 
 int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k)
 {
-    return nvfp4::chain_shape_ok(m, n, k) ? 1 : 0;
+    return nvfp4::chain_shape_ok(m, n, k) || nvfp4::tc_shape_ok(m, n, k) ? 1 : 0;
 }
 
 int nvfp4_read_probe(const void* buf, int64_t bytes, uint64_t* sink, void* stream)

@@ -430,6 +430,8 @@ cudaError_t launch_chain_gemm_m(ChainGemmParams& prm, const Variant& v, int T, i
     return launch_chain_gemm_t<M, 4, 1024, 1>(prm, T, total, gb, s, pdl);
 }
 
+}  // namespace
+
 cudaError_t launch_chain_quant(const ChainLinear* items, int count, int m, bool x_bf16,
                                cudaStream_t stream, bool pdl)
 {
@@ -459,8 +461,6 @@ cudaError_t launch_chain_quant(const ChainLinear* items, int count, int m, bool 
     return x_bf16 ? cudaLaunchKernelEx(&cfg, quantize_chain_kernel<true>, prm)
                   : cudaLaunchKernelEx(&cfg, quantize_chain_kernel<false>, prm);
 }
-
-}  // namespace
 
 bool chain_shape_ok(int64_t m, int64_t n, int64_t k)
 {

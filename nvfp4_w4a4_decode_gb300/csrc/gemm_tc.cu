@@ -1,0 +1,667 @@
+// gemm_tc.cu -- small-M W4A4 linears on the fifth-generation tensor cores:
+// tcgen05.mma kind::mxf4nvf4 (E2M1 x E2M1 with one UE4M3 scale per 16
+// elements of K on each side, FP32 accumulation in tensor memory), for M up
+// to 32.  The ReSET README ("Core components" item 2) leaves the tensor cores
+// aside at M <= 8 because a 128-row MMA tile would be at most 8/128 occupied;
+// here the operands are swapped -- 128 WEIGHT rows fill the MMA's M side and
+// the M activation rows are its N side (16 or 32, rows past M unused) -- so
+// the tile is full and the MMA consumes FP4 weights and their scales directly:
+// no decode, no scale fold and no FMA per weight element on the CUDA cores.
+//
+// One persistent CTA per SM streams a contiguous range of the 128-row weight
+// tiles of a list of independent linears (one linear is a list of one), K
+// whole per tile, through an 8-stage shared-memory ring.  Warp roles:
+//   warp 0      one thread issues the TMA loads (cp.async.bulk.tensor, 128-byte
+//               swizzle) of each stage's 128 x 256 weight codes;
+//   warp 1      allocates tensor memory; one thread issues the MMAs: four
+//               K = 64 MMAs per stage into the tile's accumulator (two
+//               accumulators alternate, so the epilogue of one tile overlaps
+//               the next), tcgen05.commit frees the stage and, after the last
+//               stage, hands the accumulator to the epilogue;
+//   warps 2..5  per stage: the weight rows' and activation rows' block scales
+//               into tensor memory (tcgen05.st) and the activation codes into
+//               the stage's shared-memory slot (same swizzled layout as TMA
+//               writes), loaded from global memory kPrefetch stages ahead;
+//   warps 6..9  epilogue: the accumulator out of tensor memory (tcgen05.ld),
+//               Y[m][row] = acc * gX * gW (FP32 or BF16).
+// Every wait is on an mbarrier with a clock budget: running out records
+// NVFP4_DEVICE_WAIT_TIMEOUT in the library's status word, every role stops,
+// the copies and MMAs already issued are drained (again bounded) and tensor
+// memory is freed before the CTA exits.
+//
+// Layouts, measured on GB300 with in-bounds probes before this kernel was
+// written: operand descriptors for K-major 128-byte-swizzled tiles (8-row
+// atoms of 1024 bytes, the start address advanced by 32 bytes per K = 64
+// step inside the atom); scale factors of A row r at tensor-memory lane r,
+// column sfa + r / 32; those of B column n at lane 32 q + n of column sfb for
+// every lane quarter q; byte j of a 32-bit cell is the j-th 16-element block
+// of the MMA's K = 64.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/nvfp4.h"
+#include "kernels.cuh"
+#include "launch_cache.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kStages = 8;                 // shared-memory ring
+constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
+constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
+constexpr int kABytes = kRows * 128;       // weight codes of a stage
+constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
+constexpr int kPrefetch = 4;               // stages the scale / activation warps load ahead
+constexpr int kThreads = 320;              // 10 warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColSfa = 64;           // 16 columns per ring slot
+constexpr uint32_t kColSfb = 192;          // 16 columns per ring slot
+constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
+constexpr size_t kSmem = (size_t)kStages * (kABytes + kBBytes) + 1024;  // + alignment slack
+
+struct TcItem {
+    const uint8_t* xq;
+    const uint8_t* xs;
+    const float* xg;
+    const uint8_t* ws;
+    const float* wg;
+    void* y;
+    int32_t n, k;
+    int32_t tiles;  // ceil(n / 128)
+    int32_t t0;     // first tile of this linear in the launch's tile list
+};
+static_assert(sizeof(TcItem) == 64, "TcItem is one 64-byte line");
+
+struct TcParams {
+    CUtensorMap wmap[kTcMaxItems];  // weight codes [n][k/2]: boxes of 128 bytes x 128 rows,
+                                    // 128-byte swizzle
+    TcItem item[kTcMaxItems];
+    int32_t start[kTcMaxCtas + 1];  // first tile of each CTA; start[grid] = all tiles
+    unsigned* status;               // the library's device status word
+    int32_t count;
+    int32_t m;
+    int32_t y_bf16;
+};
+static_assert(sizeof(TcParams) <= 32764, "kernel parameters are limited to 32764 bytes");
+
+// ---- small PTX wrappers --------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(done)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, within the clock budget and
+// while no other role has given up; false when it did not.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status)
+{
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+        if (*abort_flag)
+            return false;
+        if (clock64() - t0 > kWaitBudget) {
+            *abort_flag = 1;
+            atomicOr(status, (unsigned)NVFP4_DEVICE_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// K-major operand tile with 128-byte swizzle: 8-row atoms of 1024 bytes.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (not used by this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: one 8-row atom
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B, K-major both,
+// UE4M3 scales, M = 128, N = nmma.
+__host__ __device__ constexpr uint32_t instr_desc(int nmma)
+{
+    return (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+}
+
+__device__ __forceinline__ uint4 ld_nc_u4(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+// Position in a CTA's sequence of (linear, tile, stage).
+struct Cursor {
+    int item;
+    int32_t tile;  // tile index within the linear
+    int32_t st;    // stage within the tile
+    int32_t nst;   // stages per tile of this linear (k / 256)
+    int32_t tend;  // one past this CTA's last tile of this linear
+};
+
+__device__ __forceinline__ void cursor_set(Cursor& c, const TcParams& p, int i, int32_t lo,
+                                           int32_t hi)
+{
+    c.item = i;
+    c.tile = lo > p.item[i].t0 ? lo - p.item[i].t0 : 0;
+    c.st = 0;
+    c.nst = p.item[i].k / kStageK;
+    const int32_t e = hi - p.item[i].t0;
+    c.tend = e < p.item[i].tiles ? e : p.item[i].tiles;
+}
+
+__device__ __forceinline__ void cursor_next_tile(Cursor& c, const TcParams& p, int32_t lo,
+                                                 int32_t hi)
+{
+    c.st = 0;
+    if (++c.tile >= c.tend && c.item + 1 < p.count)
+        cursor_set(c, p, c.item + 1, lo, hi);
+}
+
+__device__ __forceinline__ void cursor_next_stage(Cursor& c, const TcParams& p, int32_t lo,
+                                                  int32_t hi)
+{
+    if (++c.st >= c.nst)
+        cursor_next_tile(c, p, lo, hi);
+}
+
+// What a scale / activation thread loads for one stage.
+struct AuxLoad {
+    uint4 sa;  // block scales of this thread's weight row (4 MMA K-steps)
+    uint4 sb;  // block scales of activation row `lane` (lanes < M)
+    uint4 b0;  // activation codes, chunk u
+    uint4 b1;  // activation codes, chunk u + 128 (M > 16)
+};
+
+template <int NMMA>
+__device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cursor& c, int r,
+                                         int lane, int u)
+{
+    const TcItem& it = p.item[c.item];
+    const int32_t kb = it.k / 16, kh = it.k / 2;
+    const int64_t row = (int64_t)c.tile * kRows + r;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    a.sa = row < it.n ? ld_nc_u4(it.ws + row * kb + c.st * 16) : z;
+    a.sb = lane < p.m ? __ldg(reinterpret_cast<const uint4*>(it.xs + lane * kb + c.st * 16)) : z;
+    a.b0 = u < p.m * 8
+               ? __ldg(reinterpret_cast<const uint4*>(it.xq + (u >> 3) * kh + c.st * 128 +
+                                                      (u & 7) * 16))
+               : z;
+    if constexpr (NMMA > 16)
+        a.b1 = u + 128 < p.m * 8
+                   ? __ldg(reinterpret_cast<const uint4*>(it.xq + ((u + 128) >> 3) * kh +
+                                                          c.st * 128 + ((u + 128) & 7) * 16))
+                   : z;
+}
+
+template <int NMMA>
+__global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages], aux_bar[kStages], empty_bar[kStages];
+    __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t lo = p.start[blockIdx.x], hi = p.start[blockIdx.x + 1];
+    // tile-aligned (1024-byte) ring: weight slots, then activation slots
+    const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes;
+    uint8_t* sB_gen = smem_raw + (sB0 - smem_u32(smem_raw));
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&tmem_base_s)), "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&aux_bar[s]), 4);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accf_bar[b]), 1);
+            mbar_init(smem_u32(&acce_bar[b]), 4);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = tmem_base_s;
+    volatile int* abort_flag = &abort_s;
+
+    // this CTA's stages
+    int first = 0;
+    int32_t total = 0;
+    if (lo < hi) {
+        int b = p.count - 1;
+        while (first < b) {
+            const int mid = (first + b + 1) >> 1;
+            if (p.item[mid].t0 <= lo)
+                first = mid;
+            else
+                b = mid - 1;
+        }
+        for (int i = first; i < p.count && p.item[i].t0 < hi; ++i) {
+            const int32_t a = lo > p.item[i].t0 ? lo - p.item[i].t0 : 0;
+            const int32_t e = hi - p.item[i].t0 < p.item[i].tiles ? hi - p.item[i].t0
+                                                                   : p.item[i].tiles;
+            if (e > a)
+                total += (e - a) * (p.item[i].k / kStageK);
+        }
+    }
+
+    if (warp == 0) {
+        // ---- TMA producer: weight codes of every stage ----------------------------
+        if (lane == 0 && total > 0) {
+            Cursor c;
+            cursor_set(c, p, first, lo, hi);
+            int32_t issued = 0;
+            for (int32_t g = 0; g < total; ++g) {
+                const int slot = g % kStages;
+                if (g >= kStages &&
+                    !mbar_wait(smem_u32(&empty_bar[slot]), ((g / kStages) - 1) & 1, abort_flag,
+                               p.status))
+                    break;
+                const uint32_t fb = smem_u32(&full_bar[slot]);
+                mbar_expect_tx(fb, kABytes);
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+                    "[%0], [%1, {%2, %3}], [%4];" ::"r"(sA0 + slot * kABytes),
+                    "l"(&p.wmap[c.item]), "r"(c.st * 128), "r"(c.tile * kRows), "r"(fb)
+                    : "memory");
+                issued = g + 1;
+                cursor_next_stage(c, p, lo, hi);
+            }
+            // drain: every copy issued has landed before the CTA can exit
+            for (int32_t g = issued > kStages ? issued - kStages : 0; g < issued; ++g) {
+                const long long t0 = clock64();
+                while (!mbar_test(smem_u32(&full_bar[g % kStages]), (g / kStages) & 1) &&
+                       clock64() - t0 < kWaitBudget) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----------------------------------------------------------------
+        if (lane == 0 && total > 0) {
+            Cursor c;
+            cursor_set(c, p, first, lo, hi);
+            const uint32_t idesc = instr_desc(NMMA);
+            int32_t g = 0, tcount = 0;
+            bool ok = true;
+            while (ok && g < total) {
+                const int buf = tcount & 1;
+                if (tcount >= 2 && !mbar_wait(smem_u32(&acce_bar[buf]), ((tcount >> 1) - 1) & 1,
+                                              abort_flag, p.status))
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t dcol = tmem + (uint32_t)(buf * 32);
+                for (int32_t st = 0; st < c.nst; ++st, ++g) {
+                    const int slot = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1;
+                    if (!mbar_wait(smem_u32(&full_bar[slot]), ph, abort_flag, p.status) ||
+                        !mbar_wait(smem_u32(&aux_bar[slot]), ph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;");
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t ad = operand_desc(sA0 + slot * kABytes + 32 * j);
+                        const uint64_t bd = operand_desc(sB0 + slot * kBBytes + 32 * j);
+                        const uint32_t sfa = tmem + kColSfa + slot * 16 + 4 * j;
+                        const uint32_t sfb = tmem + kColSfb + slot * 16 + 4 * j;
+                        asm volatile(
+                            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+                            "[%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(dcol),
+                            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(st | j)
+                            : "memory");
+                    }
+                    asm volatile(
+                        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+                        "[%0];" ::"r"(smem_u32(&empty_bar[slot]))
+                        : "memory");
+                }
+                if (!ok)
+                    break;
+                asm volatile(
+                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                    ::"r"(smem_u32(&accf_bar[buf]))
+                    : "memory");
+                ++tcount;
+                cursor_next_tile(c, p, lo, hi);
+            }
+            // drain: every MMA issued has completed before tensor memory is freed
+            asm volatile(
+                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                ::"r"(smem_u32(&drain_bar))
+                : "memory");
+            const long long t0 = clock64();
+            while (!mbar_test(smem_u32(&drain_bar), 0) && clock64() - t0 < kWaitBudget) {
+            }
+        }
+    } else if (warp < 6) {
+        // ---- block scales and activation codes of every stage --------------------------
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // x_q / x_s come from the producer
+        const int q = warp & 3;               // tensor-memory lane quarter of this warp
+        const int r = 32 * q + lane;          // weight row within the tile
+        const int u = (warp - 2) * 32 + lane;  // activation code chunk (row u / 8, 16 bytes u % 8)
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        if (total > 0) {
+            Cursor pf;
+            cursor_set(pf, p, first, lo, hi);
+            AuxLoad ring[kPrefetch];
+#pragma unroll
+            for (int d = 0; d < kPrefetch; ++d) {
+                if (d < total) {
+                    aux_load<NMMA>(ring[d], p, pf, r, lane, u);
+                    cursor_next_stage(pf, p, lo, hi);
+                }
+            }
+            bool ok = true;
+            for (int32_t g0 = 0; ok && g0 < total; g0 += kPrefetch) {
+#pragma unroll
+                for (int d = 0; d < kPrefetch; ++d) {
+                    const int32_t g = g0 + d;
+                    if (g >= total)
+                        break;
+                    const int slot = g % kStages;
+                    // warp-uniform decision: the tcgen05 stores below are .sync.aligned
+                    if (g >= kStages &&
+                        !__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[slot]),
+                                                           ((g / kStages) - 1) & 1, abort_flag,
+                                                           p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;");
+                    const uint32_t sa[4] = {ring[d].sa.x, ring[d].sa.y, ring[d].sa.z, ring[d].sa.w};
+                    const uint32_t sb[4] = {ring[d].sb.x, ring[d].sb.y, ring[d].sb.z, ring[d].sb.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        tmem_st1(lane_base + kColSfa + slot * 16 + 4 * j + q, sa[j]);
+                        tmem_st1(lane_base + kColSfb + slot * 16 + 4 * j, sb[j]);
+                    }
+                    // activation codes in the swizzled layout TMA would write
+                    uint8_t* bs = sB_gen + slot * kBBytes;
+                    if (u < p.m * 8) {
+                        const int n = u >> 3, ch = u & 7;
+                        *reinterpret_cast<uint4*>(bs + n * 128 + ((ch ^ (n & 7)) << 4)) = ring[d].b0;
+                    }
+                    if constexpr (NMMA > 16) {
+                        if (u + 128 < p.m * 8) {
+                            const int n = (u + 128) >> 3, ch = (u + 128) & 7;
+                            *reinterpret_cast<uint4*>(bs + n * 128 + ((ch ^ (n & 7)) << 4)) =
+                                ring[d].b1;
+                        }
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("tcgen05.fence::before_thread_sync;");
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&aux_bar[slot]));
+                    if (g + kPrefetch < total) {
+                        aux_load<NMMA>(ring[d], p, pf, r, lane, u);
+                        cursor_next_stage(pf, p, lo, hi);
+                    }
+                }
+            }
+        }
+    } else {
+        // ---- epilogue ----------------------------------------------------------------------
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // Y may still be read before
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        if (total > 0) {
+            Cursor c;
+            cursor_set(c, p, first, lo, hi);
+            int32_t g = 0, tcount = 0;
+            while (g < total) {
+                const int buf = tcount & 1;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&accf_bar[buf]), (tcount >> 1) & 1,
+                                                       abort_flag, p.status)))
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                uint32_t v[NMMA];
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 32);
+                if constexpr (NMMA == 16) {
+                    asm volatile(
+                        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,"
+                        "%10,%11,%12,%13,%14,%15}, [%16];"
+                        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                          "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                          "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                        : "r"(taddr));
+                } else {
+                    asm volatile(
+                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,"
+                        "%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+                        "%28,%29,%30,%31}, [%32];"
+                        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                          "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                          "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+                          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]),
+                          "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                        : "r"(taddr));
+                }
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&acce_bar[buf]));
+                const TcItem& it = p.item[c.item];
+                const int64_t row = (int64_t)c.tile * kRows + r;
+                if (row < it.n) {
+                    const float gxw = __fmul_rn(__ldg(it.xg), __ldg(it.wg));
+                    const OutY y = {it.y, p.y_bf16};
+#pragma unroll
+                    for (int n = 0; n < NMMA; ++n)
+                        if (n < p.m)
+                            store_y(y, (int64_t)n * it.n + row, __uint_as_float(v[n]) * gxw);
+                }
+                g += c.nst;
+                ++tcount;
+                cursor_next_tile(c, p, lo, hi);
+            }
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Weight codes [n][k/2] as a 2-D tensor of bytes: boxes of 128 bytes x 128
+// rows with 128-byte swizzle (rows past n read as zeros).
+bool weight_map(CUtensorMap* m, const uint8_t* wq, int64_t n, int64_t k)
+{
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+    const cuuint32_t box[2] = {128, kRows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wq), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int NMMA>
+cudaError_t launch_tc_t(TcParams& prm, int grid, cudaStream_t stream, bool pdl)
+{
+    auto kern = tc_chain_kernel<NMMA>;
+    const int dev = current_device();
+    cudaError_t e = ensure_smem_limit(kern, kSmem, dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+}  // namespace
+
+bool tc_shape_ok(int64_t m, int64_t n, int64_t k)
+{
+    return m >= 1 && m <= 32 && n >= 1 && n < (int64_t(1) << 30) && k >= kStageK &&
+           k % kStageK == 0 && k < (int64_t(1) << 30);
+}
+
+cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool quantize, bool x_bf16,
+                            bool y_bf16, cudaStream_t stream, bool pdl)
+{
+    if (count < 1 || count > kTcMaxItems || m < 1 || m > 32)
+        return cudaErrorInvalidValue;
+    static thread_local TcParams prm;  // 31 KB: kept off the stack
+    prm.count = count;
+    prm.m = m;
+    prm.y_bf16 = y_bf16 ? 1 : 0;
+    cudaError_t e = device_status_address(&prm.status);
+    if (e != cudaSuccess)
+        return e;
+    int64_t tb[kTcMaxItems];  // weight bytes of one tile
+    int64_t total = 0, tiles = 0;
+    for (int i = 0; i < count; ++i) {
+        const ChainLinear& L = items[i];
+        TcItem& it = prm.item[i];
+        if (!weight_map(&prm.wmap[i], L.wq, L.n, L.k))
+            return cudaErrorInvalidValue;
+        it.xq = L.xq;
+        it.xs = L.xs;
+        it.xg = L.xg;
+        it.ws = L.ws;
+        it.wg = L.wg;
+        it.y = L.y;
+        it.n = (int32_t)L.n;
+        it.k = (int32_t)L.k;
+        it.tiles = (int32_t)((L.n + kRows - 1) / kRows);
+        it.t0 = (int32_t)tiles;
+        tb[i] = (int64_t)kRows * L.k * 9 / 16;
+        total += it.tiles * tb[i];
+        tiles += it.tiles;
+    }
+    if (tiles >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;
+    const int dev = current_device();
+    int grid = device_sm_count(dev);
+    if (grid > kTcMaxCtas)
+        grid = kTcMaxCtas;
+    if (grid > tiles)
+        grid = (int)tiles;
+    // contiguous tile ranges of (nearly) equal weight bytes
+    int i = 0;
+    int64_t before = 0;
+    for (int b = 0; b <= grid; ++b) {
+        const int64_t target = total * b / grid;
+        while (i < count - 1 && before + prm.item[i].tiles * tb[i] <= target) {
+            before += prm.item[i].tiles * tb[i];
+            ++i;
+        }
+        int64_t t = prm.item[i].t0 + (target - before + tb[i] - 1) / tb[i];
+        prm.start[b] = (int32_t)(t < tiles ? t : tiles);
+    }
+    prm.start[0] = 0;
+    prm.start[grid] = (int32_t)tiles;
+    for (int b = 1; b <= grid; ++b)
+        if (prm.start[b] < prm.start[b - 1])
+            prm.start[b] = prm.start[b - 1];
+
+    bool tc_pdl = pdl;
+    if (quantize) {
+        e = launch_chain_quant(items, count, m, x_bf16, stream, pdl);
+        if (e != cudaSuccess)
+            return e;
+        tc_pdl = true;  // the weight loads do not depend on the quantiser
+    }
+    return m <= 16 ? launch_tc_t<16>(prm, grid, stream, tc_pdl)
+                   : launch_tc_t<32>(prm, grid, stream, tc_pdl);
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl)
+{
+    const ChainLinear one = {nullptr, a.xg, const_cast<uint8_t*>(a.xq), const_cast<uint8_t*>(a.xs),
+                             a.wq, a.ws, a.wg, a.y.p, a.n, a.k};
+    return launch_tc_chain(&one, 1, a.m, false, false, a.y.bf16 != 0, a.stream, pdl);
+}
+
+}  // namespace nvfp4

@@ -27,6 +27,9 @@
 // of its work; the host reads the word with nvfp4_device_status().
 #include <cooperative_groups.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "../../include/nvfp4.h"
 #include "formats.cuh"
 #include "kernels.cuh"
@@ -471,6 +474,28 @@ cudaError_t launch_gemm_tma(const GemmArgs& a, bool pdl, bool test_timeout)
     case 4: return pdl ? launch_tma_t<4, true>(a, p, budget, skew) : launch_tma_t<4, false>(a, p, budget, skew);
     default: return pdl ? launch_tma_t<8, true>(a, p, budget, skew) : launch_tma_t<8, false>(a, p, budget, skew);
     }
+}
+
+cudaError_t device_status_address(unsigned** out)
+{
+    // looked up once per device (the address of a module variable is fixed
+    // for the life of the context)
+    static std::mutex mu;
+    static std::unordered_map<int, unsigned*> addr;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess)
+        return e;
+    addr[dev] = static_cast<unsigned*>(p);
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear)

@@ -127,7 +127,29 @@ bool chain_shape_ok(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_linear_chain(const ChainLinear* items, int count, int m, bool quantize,
                                 bool x_bf16, bool y_bf16, cudaStream_t stream, bool pdl);
 
+// The activation quantisation of up to kChainMaxItems linears in one launch
+// (four threads per 16-element block, the stand-alone quantiser's recipe).
+// With pdl it may start before the previous kernel on the stream ends (it
+// waits before reading x).
+cudaError_t launch_chain_quant(const ChainLinear* items, int count, int m, bool x_bf16,
+                               cudaStream_t stream, bool pdl);
+
+// Tensor-core (tcgen05, kind::mxf4nvf4) persistent kernel over up to
+// kTcMaxItems independent linears: m in 1..32, k a multiple of 256, n below
+// 2^30; w_q 16-byte, x_q / x_s / w_s 16-byte aligned.  With quantize, one
+// launch of launch_chain_quant comes first.
+constexpr int kTcMaxItems = 160;
+constexpr int kTcMaxCtas = 256;
+bool tc_shape_ok(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool quantize, bool x_bf16,
+                            bool y_bf16, cudaStream_t stream, bool pdl);
+// One linear through the tensor-core kernel (m up to 32).
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl);
+
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
+// Device address of the status word on the current device (for kernels of
+// other translation units that record bounded-wait timeouts in it).
+cudaError_t device_status_address(unsigned** out);
 
 // Read-only streaming probe: zeroes *sink on the stream, then loads every
 // 16-byte word of buf once and XORs all its 8-byte words into *sink.  buf

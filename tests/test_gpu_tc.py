@@ -1,0 +1,240 @@
+"""GPU parity of the fifth-generation tensor-core kernel (NVFP4_KERNEL_TC:
+tcgen05.mma kind::mxf4nvf4, swap-AB, TMA weight stream) against the oracle.
+
+Single linears through nvfp4_gemm_smallm_ex for M from 1 to 32 (both MMA
+widths, 16 and 32, and their edges), row counts below one 128-row tile,
+exactly one, one plus one row and ragged; K from one 256-element stage to
+25600; lists of linears through nvfp4_linear_chain with this kernel
+(activation codes bit-exact with the oracle's, Y within GEMM_TOL of its FP64
+result), BF16 in and out, decades of block scales, replay in a CUDA graph,
+and the refusals.  Marked gpu."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from helpers import GEMM_TOL, gemm_error
+
+pytestmark = pytest.mark.gpu
+
+GEMM_TOL_BF16 = GEMM_TOL + 2.0 ** -8 * (1 + GEMM_TOL)
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_w4a4_decode_gb300 as nvmod
+    from nvfp4_w4a4_decode_gb300 import build as nvbuild
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    nvbuild.build()
+    oracle.build()
+    nvmod.library()
+    return nvmod
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def bf16_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_y(x, w):
+    gx = oracle.global_scale(x)
+    oxq, oxs = oracle.quantize(x, gx)
+    owq, ows, ogw = oracle.pack_weight(w)
+    return oracle.gemm(oxq, oxs, gx, owq, ows, ogw), (oxq, oxs, gx)
+
+
+def gpu_operands(nv, x, w):
+    xd = dev(x)
+    xg = nv.global_scale(xd)
+    xq, xs = nv.quantize_act(xd, xg)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    return xq, xs, xg, wq, ws, wg
+
+
+M_VALUES = [1, 2, 3, 5, 8, 9, 12, 15, 16, 17, 24, 31, 32]
+
+
+@pytest.mark.parametrize("m", M_VALUES)
+def test_tc_every_m_class(nv, m):
+    """Several tiles and a ragged last one, K of 17 stages."""
+    n, k = 128 * 3 + 37, 256 * 17
+    x = synthetic.activations(m, k, seed=11 * m)
+    w = synthetic.weights(n, k, 0.02, seed=7 + m)
+    ref, _ = oracle_y(x, w)
+    y = nv.gemm_smallm(*gpu_operands(nv, x, w), kernel=nv.KERNEL_TC)
+    torch.cuda.synchronize()
+    assert gemm_error(y.cpu().numpy(), ref) <= GEMM_TOL
+
+
+TC_SHAPES = [(1, 1, 256), (3, 127, 512), (8, 128, 4096), (16, 129, 1024), (32, 1, 256),
+             (4, 4096, 4096), (8, 300, 12288), (2, 77, 25600), (32, 255, 8192), (20, 640, 5120)]
+
+
+@pytest.mark.parametrize("m,n,k", TC_SHAPES)
+@pytest.mark.parametrize("pdl", [False, True])
+def test_tc_shapes(nv, m, n, k, pdl):
+    x = synthetic.activations(m, k, seed=m + k)
+    w = synthetic.weights(n, k, 0.02, seed=n + 3 * k)
+    ref, _ = oracle_y(x, w)
+    ops = gpu_operands(nv, x, w)
+    y = nv.gemm_smallm(*ops, kernel=nv.KERNEL_TC, pdl=pdl)
+    torch.cuda.synchronize()
+    assert gemm_error(y.cpu().numpy(), ref) <= GEMM_TOL
+    y2 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_TC)          # deterministic
+    np.testing.assert_array_equal(y2.cpu().numpy(), y.cpu().numpy())
+
+
+def test_tc_decades_of_scales(nv):
+    """Block scales over many decades (E4M3 subnormal to saturated) on both
+    sides: the tensor core applies them as given."""
+    m, n, k = 8, 200, 2048
+    x = synthetic.log_uniform_blocks(m, k, seed=21)
+    w = synthetic.log_uniform_blocks(n, k, seed=22)
+    ref, _ = oracle_y(x, w)
+    y = nv.gemm_smallm(*gpu_operands(nv, x, w), kernel=nv.KERNEL_TC)
+    torch.cuda.synchronize()
+    assert gemm_error(y.cpu().numpy(), ref) <= GEMM_TOL
+
+
+def test_tc_bf16_output(nv):
+    m, n, k = 12, 333, 4096
+    x = synthetic.activations(m, k, seed=31)
+    w = synthetic.weights(n, k, 0.02, seed=32)
+    ref, _ = oracle_y(x, w)
+    ops = gpu_operands(nv, x, w)
+    y32 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_TC)
+    y16 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_TC, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bf16_bits(y16), oracle.f32_to_bf16(y32.cpu().numpy()))
+    assert gemm_error(oracle.bf16_to_f32(bf16_bits(y16)), ref) <= GEMM_TOL_BF16
+
+
+def make_chain(nv, m, shapes, seed, x_bf16=False, y_bf16=False):
+    lins = []
+    for i, (n, k) in enumerate(shapes):
+        x32 = synthetic.activations(m, k, seed=seed + 2 * i)
+        w = synthetic.weights(n, k, 0.02, seed=seed + 2 * i + 1)
+        if x_bf16:
+            bits = oracle.f32_to_bf16(x32)
+            xh = oracle.bf16_to_f32(bits)
+            xd = torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+        else:
+            xh, xd = x32, dev(x32)
+        xg = nv.global_scale(dev(xh))
+        codes = (torch.full((m, k // 2), 0xAB, dtype=torch.uint8, device="cuda"),
+                 torch.full((m, k // 16), 0xAB, dtype=torch.uint8, device="cuda"))
+        y = torch.full((m, n), float("nan"), device="cuda",
+                       dtype=torch.bfloat16 if y_bf16 else torch.float32)
+        lins.append({"xh": xh, "w": w, "entry": (xd, xg, codes, nv.pack_weight(dev(w)), y)})
+    return lins
+
+
+def check_chain(lins, y_bf16=False):
+    for L in lins:
+        ref, (oxq, oxs, gx) = oracle_y(L["xh"], L["w"])
+        xd, xg, (xq, xs), _, y = L["entry"]
+        assert np.float32(xg.item()) == gx
+        np.testing.assert_array_equal(xq.cpu().numpy(), oxq)
+        np.testing.assert_array_equal(xs.cpu().numpy(), oxs)
+        yy = oracle.bf16_to_f32(bf16_bits(y)) if y_bf16 else y.cpu().numpy()
+        assert gemm_error(yy, ref) <= (GEMM_TOL_BF16 if y_bf16 else GEMM_TOL)
+
+
+CHAIN_SHAPES = [(300, 4096), (1, 256), (129, 12288), (1000, 1024), (128, 5120), (70, 2048)]
+
+
+@pytest.mark.parametrize("m", [1, 4, 8, 13, 32])
+def test_tc_chain_matches_oracle(nv, m):
+    lins = make_chain(nv, m, CHAIN_SHAPES, seed=40 + m)
+    ch = nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC)
+    ch.run(pdl=True)
+    torch.cuda.synchronize()
+    check_chain(lins)
+
+
+def test_tc_chain_bf16_in_and_out(nv):
+    lins = make_chain(nv, 8, CHAIN_SHAPES, seed=77, x_bf16=True, y_bf16=True)
+    nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC).run()
+    torch.cuda.synchronize()
+    check_chain(lins, y_bf16=True)
+
+
+def test_tc_chain_more_than_one_launch(nv):
+    """200 small linears: two launch pairs of at most 160."""
+    shapes = [(1 + (i * 53) % 300, 256 * (1 + i % 5)) for i in range(200)]
+    lins = make_chain(nv, 3, shapes, seed=500)
+    nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC).run(pdl=True)
+    torch.cuda.synchronize()
+    check_chain(lins)
+
+
+def test_tc_chain_graph_replay_and_status(nv):
+    lins = make_chain(nv, 8, CHAIN_SHAPES, seed=90)
+    ch = nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC)
+    nv.device_status(clear=True)
+    ch.run()
+    torch.cuda.synchronize()
+    eager = [L["entry"][4].cpu().numpy().copy() for L in lins]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ch.run(pdl=True)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ch.run(pdl=True)
+    for L in lins:
+        L["entry"][4].fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for L, e in zip(lins, eager):
+        np.testing.assert_array_equal(L["entry"][4].cpu().numpy(), e)
+    assert nv.device_status(clear=True) == 0          # no wait ran out
+
+
+def test_tc_full_size_8b_layer_m8(nv):
+    """The four 8B-shaped linears at M = 8, full size, one chain: sampled rows
+    against the oracle."""
+    m = 8
+    lins = make_chain(nv, m, [(l.n, l.k) for l in synthetic.LINEARS_8B], seed=123)
+    nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC).run(pdl=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    for L in lins:
+        gx = oracle.global_scale(L["xh"])
+        oxq, oxs = oracle.quantize(L["xh"], gx)
+        np.testing.assert_array_equal(L["entry"][2][0].cpu().numpy(), oxq)
+        n = L["w"].shape[0]
+        rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 62)]))
+        gw = oracle.global_scale(L["w"])
+        owq, ows = oracle.quantize(L["w"][rows], gw)
+        ref = oracle.gemm(oxq, oxs, gx, owq, ows, gw)
+        y = L["entry"][4].cpu().numpy()[:, rows]
+        assert gemm_error(y, ref) <= GEMM_TOL
+
+
+def test_tc_refusals(nv):
+    g = torch.ones(1, device="cuda")
+    z = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    y = torch.full((40, 4), 7.0, device="cuda")
+    lib = nv.library()
+    st = torch.cuda.current_stream().cuda_stream
+
+    def call(m, n, k, opts):
+        return lib.nvfp4_gemm_smallm_ex(z.data_ptr(), z.data_ptr(), g.data_ptr(), z.data_ptr(),
+                                        z.data_ptr(), g.data_ptr(), y.data_ptr(), m, n, k, opts, st)
+    assert call(9, 4, 256, nv.KERNEL_AUTO) == 2       # M > 8 only on request
+    assert call(33, 4, 256, nv.KERNEL_TC) == 2        # the kernel's limit
+    assert call(4, 4, 128, nv.KERNEL_TC) == 2         # K below one stage
+    assert call(4, 4, 272, nv.KERNEL_TC) == 2         # K not a multiple of 256
+    assert nv.gemm_select(9, 4, 256, nv.KERNEL_TC) == nv.KERNEL_TC
+    assert nv.gemm_select(9, 4, 256, nv.KERNEL_AUTO) == -2
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy() == 7.0).all()              # nothing launched
