@@ -207,7 +207,8 @@ class DecodeStack:
             raise ValueError(f"the chain does not take M = {m}")
         self.mode = mode
         # one workspace for every call of the step (calls run one after another)
-        wsz = max(nv.gemm_workspace_size(m, lin.n, lin.k, kernel) for lin in self.lins)
+        wsz = max(nv.gemm_workspace_size(m, lin.n, lin.k, kernel) for lin in self.lins) \
+            if m <= 8 else 0
         self.workspace = (torch.zeros(wsz, dtype=torch.uint8, device="cuda") if wsz else None)
         dev = torch.device("cuda")
         self.w = []          # [layer][j] -> (wq, ws, wg)
@@ -497,43 +498,70 @@ def tiny_latency(nv, torch, kernels: dict, pdl: bool, calls: int = 50) -> dict:
     return res
 
 
+def time_chain_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
+    """µs per linear of one shape when len(weights) distinct copies of it run
+    as one multi-linear GEMM call (nvfp4_gemm_chain on pre-quantised codes):
+    the rate of the shape inside a long chain, graph-replayed."""
+    xa = synthetic.activations(m, lin.k, seed=seed)
+    xd = torch.from_numpy(xa).cuda()
+    xg = nv.global_scale(xd)
+    entries = []
+    for wq, ws, wg in weights:
+        codes = nv.quantize_act(xd, xg)
+        entries.append((xd, xg, codes, (wq, ws, wg),
+                        torch.empty((m, lin.n), device="cuda")))
+    ch = nv.Chain(entries, kernel=kernel)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ch.gemm_only(pdl=pdl)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ch.gemm_only(pdl=pdl)
+    ms = time_graph(torch, g, reps=reps)
+    us = ms * 1e3 / len(weights)
+    b = algorithmic_bytes(m, lin.n, lin.k)["gemm"]
+    return {"us_per_call": round(us, 3), "GBps": round(b / (us * 1e-6) / 1e9, 1)}
+
+
 def sweep(nv, torch, stack, peaks, args) -> dict:
-    """µs/call and GB/s of every linear shape for every M of the sweep, with
-    the library's kernel choice and with each kernel that takes the shape."""
+    """µs/call and GB/s of every linear shape for every M of the sweep: each
+    kernel that takes the shape as a lone call (graph of calls over rotating
+    weight copies, L2-cold), the library's choice marked, and the shape
+    inside a multi-linear call on the tensor cores (``tc_chain``).  Beyond
+    M = 8 (tensor-core kernel only) the 8B shapes at M = 12..32."""
     kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA,
-               "splitk": nv.KERNEL_SPLITK, "generic": nv.KERNEL_GENERIC}
+               "splitk": nv.KERNEL_SPLITK, "tc": nv.KERNEL_TC, "generic": nv.KERNEL_GENERIC}
     out = {"8B": {}, "32B": {}, "C1": tiny_latency(nv, torch, kernels, stack.pdl)}
     reps = 5
+
+    def entry(m, lin, ws):
+        auto = auto_choice(nv, m, lin) if m <= 8 else nv.KERNEL_TC
+        ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
+        for name, kid in kernels.items():
+            if name == "generic" and not args.sweep_generic:
+                continue
+            if m > 8 and kid != nv.KERNEL_TC:
+                continue
+            if not takes(nv, m, lin, kid):
+                continue
+            ent[name] = time_linear(nv, torch, ws, lin, m, kid, stack.pdl, reps)
+        ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
+        ent["tc_chain"] = time_chain_linear(nv, torch, ws, lin, m, nv.KERNEL_TC, stack.pdl, reps)
+        ent["tc_chain"]["frac_of_peak"] = round(ent["tc_chain"]["GBps"] / peaks["hbm_gbs"], 4)
+        return ent
+
     w8 = {j: [stack.w[l][j] for l in range(stack.layers)] for j in range(4)}
-    for m in synthetic.M_SWEEP_8B:
-        row = {}
-        for j, lin in enumerate(synthetic.LINEARS_8B):
-            auto = auto_choice(nv, m, lin)
-            ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
-            for name, kid in kernels.items():
-                if name == "generic" and not args.sweep_generic:
-                    continue
-                if not takes(nv, m, lin, kid):
-                    continue
-                ent[name] = time_linear(nv, torch, w8[j], lin, m, kid, stack.pdl, reps)
-            ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
-            row[lin.name] = ent
-        out["8B"][f"M={m}"] = row
+    for m in tuple(synthetic.M_SWEEP_8B) + tuple(synthetic.M_SWEEP_WIDE):
+        out["8B"][f"M={m}"] = {lin.name: entry(m, lin, w8[j])
+                               for j, lin in enumerate(synthetic.LINEARS_8B)}
     for j, lin in enumerate(synthetic.LINEARS_32B):
         per_copy = lin.n * lin.k * 9 // 16
         copies = max(3, -(-400_000_000 // per_copy))
         ws = make_weights(nv, torch, lin, synthetic.WEIGHT_STD_32B, copies, seed=4000 + 100 * j)
         for m in synthetic.M_SWEEP_32B:
-            auto = auto_choice(nv, m, lin)
-            ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
-            for name, kid in kernels.items():
-                if name == "generic" and not args.sweep_generic:
-                    continue
-                if not takes(nv, m, lin, kid):
-                    continue
-                ent[name] = time_linear(nv, torch, ws, lin, m, kid, stack.pdl, reps)
-            ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
-            out["32B"].setdefault(f"M={m}", {})[lin.name] = ent
+            out["32B"].setdefault(f"M={m}", {})[lin.name] = entry(m, lin, ws)
         del ws
         torch.cuda.empty_cache()
     return out

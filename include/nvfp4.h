@@ -378,8 +378,8 @@ typedef struct {
  * reads them once they are).  `linears` is a HOST array of `count`
  * descriptions, read during the call only.  options: a kernel choice in the
  * low byte --
- *   NVFP4_KERNEL_AUTO   the CUDA-core stream at m <= 2, the tensor-core
- *                       kernel above;
+ *   NVFP4_KERNEL_AUTO   the tensor-core kernel (measured faster than the
+ *                       CUDA-core stream on the decode step at every m);
  *   NVFP4_KERNEL_GEMV   the CUDA-core stream: m of 1 or 2, k a multiple of
  *                       1024 up to 32768 (each output bit-exact with the
  *                       single-linear NVFP4_KERNEL_GEMV);

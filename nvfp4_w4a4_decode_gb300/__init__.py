@@ -412,7 +412,7 @@ class Chain:
         self.device = linears[0][0].device
         self.kernel = int(kernel)
         if self.kernel == KERNEL_AUTO:
-            self.engine = KERNEL_GEMV if m <= 2 else KERNEL_TC
+            self.engine = KERNEL_TC          # the library's choice at every m
         else:
             self.engine = self.kernel
 

@@ -57,6 +57,9 @@ DECODE_LAYERS_8B = 36
 
 M_SWEEP_8B = (1, 2, 4, 8)
 M_SWEEP_32B = (1, 4)
+# batch sizes past the small-M range (tensor-core kernel only): the GEMV /
+# tensor-core crossover study of the README's `gemv_max_m` knob
+M_SWEEP_WIDE = (12, 16, 24, 32)
 
 
 def weight_seed(base: int, layer: int, j: int) -> int:

@@ -1,5 +1,7 @@
 """GPU parity of the multi-linear entry points (nvfp4_linear_chain,
-nvfp4_gemm_chain): every linear's activation codes bit-exact with the
+nvfp4_gemm_chain) on the CUDA-core stream (NVFP4_KERNEL_GEMV; the
+tensor-core engine is covered in test_gpu_tc.py): every linear's activation
+codes bit-exact with the
 oracle's, every Y equal bit for bit to the single-linear CUDA-core kernel
 (NVFP4_KERNEL_GEMV) on the same codes and within GEMM_TOL of the oracle's FP64
 result.  Lists cover every compiled CTA width (rows of K <= 8192 / 12288 /
@@ -66,7 +68,9 @@ def make_linears(nv, m, shapes, seed, x_bf16=False, y_bf16=False):
 
 
 def chain_of(nv, lins):
-    return nv.Chain([(L["xd"], L["xg"], L["codes"], L["packed"], L["y"]) for L in lins])
+    """The chain on the CUDA-core stream (the engine these tests cover)."""
+    return nv.Chain([(L["xd"], L["xg"], L["codes"], L["packed"], L["y"]) for L in lins],
+                    kernel=nv.KERNEL_GEMV)
 
 
 def check_against_oracle_and_gemv(nv, lins, m, y_bf16=False):
@@ -206,7 +210,8 @@ def test_linear_chain_full_size_8b_layer(nv):
 def _raw_chain(nv, descs, m, options=0):
     arr = (nv.ChainLinear * len(descs))(*descs)
     return nv.library().nvfp4_linear_chain(ctypes.cast(arr, ctypes.c_void_p), len(descs), m,
-                                           options, torch.cuda.current_stream().cuda_stream)
+                                           options | nv.KERNEL_GEMV,
+                                           torch.cuda.current_stream().cuda_stream)
 
 
 def test_linear_chain_refusals_launch_nothing(nv):
@@ -230,6 +235,9 @@ def test_linear_chain_refusals_launch_nothing(nv):
     bad.y = 0                                                # null output
     assert _raw_chain(nv, [descs[0], bad], 1) == 1
     assert _raw_chain(nv, descs, 1, options=0x10000) == 1    # unknown option
+    assert nv.library().nvfp4_linear_chain(                   # a kernel no chain runs on
+        ctypes.cast((nv.ChainLinear * 2)(*descs), ctypes.c_void_p), 2, 1, nv.KERNEL_SPLITK,
+        torch.cuda.current_stream().cuda_stream) == 2
     torch.cuda.synchronize()
     for L in lins:                                           # nothing was launched
         assert np.isnan(L["y"].cpu().numpy()).all()
