@@ -406,6 +406,33 @@ int nvfp4_linear_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t
 int nvfp4_gemm_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
                      uint32_t options, void* stream);
 
+/*
+ * The chain entry points with a workspace: the tensor-core kernel then
+ * gives every CTA an equal share of the weight stream, cutting 128-row tiles
+ * between CTAs where the shares end, and the CTAs that share a tile add
+ * their partial sums through the workspace in a fixed order (the last to
+ * finish sums them; results do not depend on timing).  Without a workspace
+ * the shares end on tile boundaries, which leaves SMs idle when a call has
+ * few or large tiles (a lone linear of a few thousand rows, K = 25600).
+ *   workspace        caller-owned device memory, 16-byte aligned, ZERO before
+ *                    its first use; every completed call leaves it so, and it
+ *                    may serve any number of calls that do not overlap in time
+ *                    (overlapping calls need separate workspaces)
+ *   workspace_bytes  at least nvfp4_chain_workspace_size() (less: no
+ *                    workspace is used); NULL with 0 for none
+ * The CUDA-core stream takes no workspace (it is ignored).
+ */
+int nvfp4_linear_chain_ws(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                          uint32_t options, void* workspace, size_t workspace_bytes, void* stream);
+int nvfp4_gemm_chain_ws(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                        uint32_t options, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes the chain entry points use with this m and options on the
+ * current device (0 for the CUDA-core stream), or minus a status code.  The
+ * tensor-core kernel also uses this size through the _ws GEMM entry points
+ * (nvfp4_gemm_workspace_size reports it for NVFP4_KERNEL_TC).  Host only. */
+int64_t nvfp4_chain_workspace_size(int64_t m, uint32_t options);
+
 /* 1 when a linear of shape (m, n, k) can be part of a chain (on either
  * kernel), else 0.  Host only. */
 int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k);

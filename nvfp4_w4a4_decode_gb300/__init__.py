@@ -66,6 +66,11 @@ SIGNATURES = {
     "nvfp4_linear_chain": ([_p, _i64, _i64, ctypes.c_uint32, _p], ctypes.c_int),
     "nvfp4_gemm_chain": ([_p, _i64, _i64, ctypes.c_uint32, _p], ctypes.c_int),
     "nvfp4_chain_supported": ([_i64, _i64, _i64], ctypes.c_int),
+    "nvfp4_linear_chain_ws": ([_p, _i64, _i64, ctypes.c_uint32, _p, ctypes.c_size_t, _p],
+                              ctypes.c_int),
+    "nvfp4_gemm_chain_ws": ([_p, _i64, _i64, ctypes.c_uint32, _p, ctypes.c_size_t, _p],
+                            ctypes.c_int),
+    "nvfp4_chain_workspace_size": ([_i64, ctypes.c_uint32], _i64),
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA, KERNEL_SPLITK = 0, 1, 2, 3, 4, 5
@@ -364,16 +369,18 @@ def nvfp4_chain_supported(m: int, n: int, k: int) -> bool:
 
 class Chain:
     """A fixed list of independent linears run as one multi-linear call
-    (``nvfp4_linear_chain`` / ``nvfp4_gemm_chain``).
+    (``nvfp4_linear_chain_ws`` / ``nvfp4_gemm_chain_ws``).
 
     ``linears`` is a sequence of ``(x, xg, (xq, xs), (wq, ws, wg), y)``: x
     [m, k] float32 or bfloat16 (the same dtype for every linear), xg [1]
     float32, xq [m, k/2] / xs [m, k/16] uint8 (written by ``run``, read by
     ``gemm_only``), the packed weights, and y [m, n] float32 or bfloat16 (the
     same dtype for every linear).  The descriptions are built once; the
-    tensors must stay alive and in place while the chain is used."""
+    tensors must stay alive and in place while the chain is used.  With
+    ``workspace`` (default) the tensor-core kernel gets a zeroed workspace of
+    its own, so calls of one Chain must not overlap in time."""
 
-    def __init__(self, linears, kernel: int = KERNEL_AUTO):
+    def __init__(self, linears, kernel: int = KERNEL_AUTO, workspace: bool = True):
         if not linears:
             raise ValueError("a chain needs at least one linear")
         descs = []
@@ -415,13 +422,27 @@ class Chain:
             self.engine = KERNEL_TC          # the library's choice at every m
         else:
             self.engine = self.kernel
+        # the tensor-core kernel balances its CTAs through a zeroed workspace
+        self.workspace = None
+        if workspace:
+            size = int(library().nvfp4_chain_workspace_size(m, self.kernel))
+            if size < 0:
+                raise Nvfp4Error("nvfp4_chain_workspace_size", -size)
+            if size:
+                self.workspace = torch.zeros(size, dtype=torch.uint8, device=self.device)
+
+    def _ws(self):
+        if self.workspace is None:
+            return None, 0
+        return self.workspace.data_ptr(), self.workspace.numel()
 
     def run(self, pdl: bool = False):
         """Quantise every linear's X and compute every Y (two launches per
         CHAIN_MAX_LINEARS linears) on the current stream."""
-        _check("nvfp4_linear_chain", library().nvfp4_linear_chain(
+        wp, wn = self._ws()
+        _check("nvfp4_linear_chain", library().nvfp4_linear_chain_ws(
             ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
-            self.kernel | self._flags | (FLAG_PDL if pdl else 0),
+            self.kernel | self._flags | (FLAG_PDL if pdl else 0), wp, wn,
             torch.cuda.current_stream(self.device).cuda_stream))
 
     def launches(self, quantize: bool = True) -> int:
@@ -432,9 +453,10 @@ class Chain:
     def gemm_only(self, pdl: bool = False):
         """Every Y from the codes already in each xq / xs (one launch per
         CHAIN_MAX_LINEARS, or TC_MAX_LINEARS, linears)."""
-        _check("nvfp4_gemm_chain", library().nvfp4_gemm_chain(
+        wp, wn = self._ws()
+        _check("nvfp4_gemm_chain", library().nvfp4_gemm_chain_ws(
             ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
-            self.kernel | (self._flags & FLAG_Y_BF16) | (FLAG_PDL if pdl else 0),
+            self.kernel | (self._flags & FLAG_Y_BF16) | (FLAG_PDL if pdl else 0), wp, wn,
             torch.cuda.current_stream(self.device).cuda_stream))
 
 

@@ -203,7 +203,7 @@ int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t
     case NVFP4_KERNEL_SPLITK:
         return from_cuda(nvfp4::launch_gemm_splitk(a, pdl, workspace, ws_bytes));
     case NVFP4_KERNEL_TC:
-        return from_cuda(nvfp4::launch_gemm_tc(a, pdl));
+        return from_cuda(nvfp4::launch_gemm_tc(a, pdl, workspace, ws_bytes));
     default:
         return from_cuda(nvfp4::launch_gemm_generic(a));
     }
@@ -235,6 +235,8 @@ int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t opti
     const int kern = select_kernel(m, n, k, options, true, true, INT64_MAX);
     if (kern < 0)
         return kern;
+    if (kern == (int)NVFP4_KERNEL_TC)
+        return nvfp4::tc_workspace_bytes();
     return kern == (int)NVFP4_KERNEL_SPLITK ? nvfp4::splitk_workspace_bytes(m, n, k) : 0;
 }
 
@@ -397,8 +399,10 @@ int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uin
 }
 
 int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t options,
-          void* stream, bool quantize)
+          void* workspace, size_t workspace_bytes, void* stream, bool quantize)
 {
+    if (workspace == nullptr ? workspace_bytes != 0 : !aligned(workspace, 16))
+        return NVFP4_ERR_INVALID_ARG;
     const uint32_t allowed = NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 |
                              (quantize ? NVFP4_FLAG_X_BF16 : 0u);
     if (count < 0 || m < 0 || (count > 0 && linears == nullptr) || (options & ~allowed) != 0)
@@ -431,7 +435,8 @@ int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t 
         const bool xb = (options & NVFP4_FLAG_X_BF16) != 0, yb = (options & NVFP4_FLAG_Y_BF16) != 0;
         const cudaError_t e =
             engine == (int)NVFP4_KERNEL_TC
-                ? nvfp4::launch_tc_chain(part, (int)kept, (int)m, quantize, xb, yb, s, pdl || i0 > 0)
+                ? nvfp4::launch_tc_chain(part, (int)kept, (int)m, quantize, xb, yb, s, pdl || i0 > 0,
+                                         workspace, (int64_t)workspace_bytes)
                 : nvfp4::launch_linear_chain(part, (int)kept, (int)m, quantize, xb, yb, s,
                                              pdl || i0 > 0);
         if (e != cudaSuccess)
@@ -445,13 +450,36 @@ int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t 
 int nvfp4_linear_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
                        uint32_t options, void* stream)
 {
-    return chain(linears, count, m, options, stream, true);
+    return chain(linears, count, m, options, nullptr, 0, stream, true);
 }
 
 int nvfp4_gemm_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
                      uint32_t options, void* stream)
 {
-    return chain(linears, count, m, options, stream, false);
+    return chain(linears, count, m, options, nullptr, 0, stream, false);
+}
+
+int nvfp4_linear_chain_ws(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                          uint32_t options, void* workspace, size_t workspace_bytes, void* stream)
+{
+    return chain(linears, count, m, options, workspace, workspace_bytes, stream, true);
+}
+
+int nvfp4_gemm_chain_ws(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
+                        uint32_t options, void* workspace, size_t workspace_bytes, void* stream)
+{
+    return chain(linears, count, m, options, workspace, workspace_bytes, stream, false);
+}
+
+int64_t nvfp4_chain_workspace_size(int64_t m, uint32_t options)
+{
+    if (m < 1 || (options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_X_BF16 |
+                                        NVFP4_FLAG_Y_BF16)) != 0)
+        return -NVFP4_ERR_INVALID_ARG;
+    const int engine = chain_engine(m, options);
+    if (engine < 0 || m > (engine == (int)NVFP4_KERNEL_TC ? 32 : 2))
+        return -NVFP4_ERR_UNSUPPORTED;
+    return engine == (int)NVFP4_KERNEL_TC ? nvfp4::tc_workspace_bytes() : 0;
 }
 
 int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k)

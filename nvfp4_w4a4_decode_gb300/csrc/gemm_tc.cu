@@ -54,7 +54,7 @@ constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
 constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
-constexpr int kPrefetch = 4;               // stages the scale / activation warps load ahead
+constexpr int kPrefetch = 6;               // stages the scale / activation warps load ahead
 constexpr int kThreads = 320;              // 10 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSfa = 64;           // 16 columns per ring slot
@@ -70,8 +70,8 @@ struct TcItem {
     const float* wg;
     void* y;
     int32_t n, k;
-    int32_t tiles;  // ceil(n / 128)
-    int32_t t0;     // first tile of this linear in the launch's tile list
+    int32_t s0;  // first stage of this linear in the launch's stage list
+    int32_t pad;
 };
 static_assert(sizeof(TcItem) == 64, "TcItem is one 64-byte line");
 
@@ -79,11 +79,14 @@ struct TcParams {
     CUtensorMap wmap[kTcMaxItems];  // weight codes [n][k/2]: boxes of 128 bytes x 128 rows,
                                     // 128-byte swizzle
     TcItem item[kTcMaxItems];
-    int32_t start[kTcMaxCtas + 1];  // first tile of each CTA; start[grid] = all tiles
+    int32_t start[kTcMaxCtas + 1];  // first stage of each CTA; start[grid] = all stages
     unsigned* status;               // the library's device status word
-    int32_t count;
+    float* part;      // [2 grid][32][128] partial tiles of tiles split between CTAs (or null)
+    unsigned* count;  // [grid] arrival counters of split tiles (zero between calls)
+    int32_t count_items;
     int32_t m;
     int32_t y_bf16;
+    int32_t grid;
 };
 static_assert(sizeof(TcParams) <= 32764, "kernel parameters are limited to 32764 bytes");
 
@@ -157,10 +160,12 @@ __host__ __device__ constexpr uint32_t instr_desc(int nmma)
     return (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 }
 
+// 16 bytes of a weight row's block scales; the L2 fetches the surrounding
+// 256 bytes (the next stages' scales of the row) with the same DRAM access.
 __device__ __forceinline__ uint4 ld_nc_u4(const void* p)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -174,36 +179,65 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
 // Position in a CTA's sequence of (linear, tile, stage).
 struct Cursor {
     int item;
-    int32_t tile;  // tile index within the linear
-    int32_t st;    // stage within the tile
-    int32_t nst;   // stages per tile of this linear (k / 256)
-    int32_t tend;  // one past this CTA's last tile of this linear
+    int32_t tile;   // tile index within the linear
+    int32_t st;     // stage within the tile
+    int32_t nst;    // stages per tile of this linear (k / 256)
+    int32_t tiles;  // tiles of this linear
 };
 
-__device__ __forceinline__ void cursor_set(Cursor& c, const TcParams& p, int i, int32_t lo,
-                                           int32_t hi)
+__device__ __forceinline__ int item_of_stage(const TcParams& p, int32_t g)
 {
-    c.item = i;
-    c.tile = lo > p.item[i].t0 ? lo - p.item[i].t0 : 0;
-    c.st = 0;
-    c.nst = p.item[i].k / kStageK;
-    const int32_t e = hi - p.item[i].t0;
-    c.tend = e < p.item[i].tiles ? e : p.item[i].tiles;
+    int i = 0, b = p.count_items - 1;
+    while (i < b) {
+        const int mid = (i + b + 1) >> 1;
+        if (p.item[mid].s0 <= g)
+            i = mid;
+        else
+            b = mid - 1;
+    }
+    return i;
 }
 
-__device__ __forceinline__ void cursor_next_tile(Cursor& c, const TcParams& p, int32_t lo,
-                                                 int32_t hi)
+__device__ __forceinline__ void cursor_at(Cursor& c, const TcParams& p, int32_t g)
 {
-    c.st = 0;
-    if (++c.tile >= c.tend && c.item + 1 < p.count)
-        cursor_set(c, p, c.item + 1, lo, hi);
+    c.item = item_of_stage(p, g);
+    const TcItem& it = p.item[c.item];
+    c.nst = it.k / kStageK;
+    c.tiles = (it.n + kRows - 1) / kRows;
+    const int32_t local = g - it.s0;
+    c.tile = local / c.nst;
+    c.st = local - c.tile * c.nst;
 }
 
-__device__ __forceinline__ void cursor_next_stage(Cursor& c, const TcParams& p, int32_t lo,
-                                                  int32_t hi)
+__device__ __forceinline__ void cursor_next_tile(Cursor& c, const TcParams& p)
+{
+    c.st = 0;
+    if (++c.tile >= c.tiles && c.item + 1 < p.count_items) {
+        ++c.item;
+        c.tile = 0;
+        c.nst = p.item[c.item].k / kStageK;
+        c.tiles = (p.item[c.item].n + kRows - 1) / kRows;
+    }
+}
+
+__device__ __forceinline__ void cursor_next_stage(Cursor& c, const TcParams& p)
 {
     if (++c.st >= c.nst)
-        cursor_next_tile(c, p, lo, hi);
+        cursor_next_tile(c, p);
+}
+
+// The CTA whose stage range holds stage g.
+__device__ __forceinline__ int cta_of_stage(const TcParams& p, int32_t g)
+{
+    int c = 0, b = p.grid - 1;
+    while (c < b) {
+        const int mid = (c + b + 1) >> 1;
+        if (p.start[mid] <= g)
+            c = mid;
+        else
+            b = mid - 1;
+    }
+    return c;
 }
 
 // What a scale / activation thread loads for one stage.
@@ -243,10 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
+    __shared__ int last_s;
 
     asm volatile("griddepcontrol.launch_dependents;");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t lo = p.start[blockIdx.x], hi = p.start[blockIdx.x + 1];
+    const int32_t total = hi - lo;  // this CTA's stages
     // tile-aligned (1024-byte) ring: weight slots, then activation slots
     const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes;
@@ -277,37 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     const uint32_t tmem = tmem_base_s;
     volatile int* abort_flag = &abort_s;
 
-    // this CTA's stages
-    int first = 0;
-    int32_t total = 0;
-    if (lo < hi) {
-        int b = p.count - 1;
-        while (first < b) {
-            const int mid = (first + b + 1) >> 1;
-            if (p.item[mid].t0 <= lo)
-                first = mid;
-            else
-                b = mid - 1;
-        }
-        for (int i = first; i < p.count && p.item[i].t0 < hi; ++i) {
-            const int32_t a = lo > p.item[i].t0 ? lo - p.item[i].t0 : 0;
-            const int32_t e = hi - p.item[i].t0 < p.item[i].tiles ? hi - p.item[i].t0
-                                                                   : p.item[i].tiles;
-            if (e > a)
-                total += (e - a) * (p.item[i].k / kStageK);
-        }
-    }
-
     if (warp == 0) {
         // ---- TMA producer: weight codes of every stage ----------------------------
         if (lane == 0 && total > 0) {
             Cursor c;
-            cursor_set(c, p, first, lo, hi);
+            cursor_at(c, p, lo);
             int32_t issued = 0;
-            for (int32_t g = 0; g < total; ++g) {
-                const int slot = g % kStages;
-                if (g >= kStages &&
-                    !mbar_wait(smem_u32(&empty_bar[slot]), ((g / kStages) - 1) & 1, abort_flag,
+            for (int32_t i = 0; i < total; ++i) {
+                const int slot = i % kStages;
+                if (i >= kStages &&
+                    !mbar_wait(smem_u32(&empty_bar[slot]), ((i / kStages) - 1) & 1, abort_flag,
                                p.status))
                     break;
                 const uint32_t fb = smem_u32(&full_bar[slot]);
@@ -317,35 +332,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     "[%0], [%1, {%2, %3}], [%4];" ::"r"(sA0 + slot * kABytes),
                     "l"(&p.wmap[c.item]), "r"(c.st * 128), "r"(c.tile * kRows), "r"(fb)
                     : "memory");
-                issued = g + 1;
-                cursor_next_stage(c, p, lo, hi);
+                issued = i + 1;
+                cursor_next_stage(c, p);
             }
             // drain: every copy issued has landed before the CTA can exit
-            for (int32_t g = issued > kStages ? issued - kStages : 0; g < issued; ++g) {
+            for (int32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
                 const long long t0 = clock64();
-                while (!mbar_test(smem_u32(&full_bar[g % kStages]), (g / kStages) & 1) &&
+                while (!mbar_test(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1) &&
                        clock64() - t0 < kWaitBudget) {
                 }
             }
         }
     } else if (warp == 1) {
-        // ---- MMA issuer ----------------------------------------------------------------
+        // ---- MMA issuer: one accumulator per tile segment --------------------------------
         if (lane == 0 && total > 0) {
             Cursor c;
-            cursor_set(c, p, first, lo, hi);
+            cursor_at(c, p, lo);
             const uint32_t idesc = instr_desc(NMMA);
-            int32_t g = 0, tcount = 0;
+            int32_t i = 0, tcount = 0;
             bool ok = true;
-            while (ok && g < total) {
+            while (ok && i < total) {
                 const int buf = tcount & 1;
                 if (tcount >= 2 && !mbar_wait(smem_u32(&acce_bar[buf]), ((tcount >> 1) - 1) & 1,
                                               abort_flag, p.status))
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t dcol = tmem + (uint32_t)(buf * 32);
-                for (int32_t st = 0; st < c.nst; ++st, ++g) {
-                    const int slot = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1;
+                const int32_t len = c.nst - c.st < total - i ? c.nst - c.st : total - i;
+                for (int32_t s = 0; s < len; ++s, ++i) {
+                    const int slot = i % kStages;
+                    const uint32_t ph = (i / kStages) & 1;
                     if (!mbar_wait(smem_u32(&full_bar[slot]), ph, abort_flag, p.status) ||
                         !mbar_wait(smem_u32(&aux_bar[slot]), ph, abort_flag, p.status)) {
                         ok = false;
@@ -362,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                             "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %6, 0;\n\t"
                             "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
                             "[%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(dcol),
-                            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(st | j)
+                            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(s | j)
                             : "memory");
                     }
                     asm volatile(
@@ -377,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     ::"r"(smem_u32(&accf_bar[buf]))
                     : "memory");
                 ++tcount;
-                cursor_next_tile(c, p, lo, hi);
+                cursor_next_tile(c, p);
             }
             // drain: every MMA issued has completed before tensor memory is freed
             asm volatile(
@@ -397,27 +413,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         if (total > 0) {
             Cursor pf;
-            cursor_set(pf, p, first, lo, hi);
+            cursor_at(pf, p, lo);
             AuxLoad ring[kPrefetch];
 #pragma unroll
             for (int d = 0; d < kPrefetch; ++d) {
                 if (d < total) {
                     aux_load<NMMA>(ring[d], p, pf, r, lane, u);
-                    cursor_next_stage(pf, p, lo, hi);
+                    cursor_next_stage(pf, p);
                 }
             }
             bool ok = true;
-            for (int32_t g0 = 0; ok && g0 < total; g0 += kPrefetch) {
+            for (int32_t i0 = 0; ok && i0 < total; i0 += kPrefetch) {
 #pragma unroll
                 for (int d = 0; d < kPrefetch; ++d) {
-                    const int32_t g = g0 + d;
-                    if (g >= total)
+                    const int32_t i = i0 + d;
+                    if (i >= total)
                         break;
-                    const int slot = g % kStages;
+                    const int slot = i % kStages;
                     // warp-uniform decision: the tcgen05 stores below are .sync.aligned
-                    if (g >= kStages &&
+                    if (i >= kStages &&
                         !__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty_bar[slot]),
-                                                           ((g / kStages) - 1) & 1, abort_flag,
+                                                           ((i / kStages) - 1) & 1, abort_flag,
                                                            p.status))) {
                         ok = false;
                         break;
@@ -449,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(smem_u32(&aux_bar[slot]));
-                    if (g + kPrefetch < total) {
+                    if (i + kPrefetch < total) {
                         aux_load<NMMA>(ring[d], p, pf, r, lane, u);
-                        cursor_next_stage(pf, p, lo, hi);
+                        cursor_next_stage(pf, p);
                     }
                 }
             }
@@ -461,12 +477,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         asm volatile("griddepcontrol.wait;" ::: "memory");  // Y may still be read before
         const int q = warp & 3;
         const int r = 32 * q + lane;
+        const int et = threadIdx.x - 6 * 32;  // 0..127 among the epilogue threads
         if (total > 0) {
             Cursor c;
-            cursor_set(c, p, first, lo, hi);
-            int32_t g = 0, tcount = 0;
-            while (g < total) {
+            cursor_at(c, p, lo);
+            int32_t i = 0, tcount = 0;
+            while (i < total) {
                 const int buf = tcount & 1;
+                const int32_t st_a = c.st;
+                const int32_t len = c.nst - c.st < total - i ? c.nst - c.st : total - i;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&accf_bar[buf]), (tcount >> 1) & 1,
                                                        abort_flag, p.status)))
                     break;
@@ -501,17 +520,61 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     mbar_arrive(smem_u32(&acce_bar[buf]));
                 const TcItem& it = p.item[c.item];
                 const int64_t row = (int64_t)c.tile * kRows + r;
-                if (row < it.n) {
-                    const float gxw = __fmul_rn(__ldg(it.xg), __ldg(it.wg));
-                    const OutY y = {it.y, p.y_bf16};
+                const float gxw = __fmul_rn(__ldg(it.xg), __ldg(it.wg));
+                const OutY y = {it.y, p.y_bf16};
+                if (st_a == 0 && len == c.nst) {
+                    // the whole tile's K in this accumulator
+                    if (row < it.n) {
+#pragma unroll
+                        for (int n = 0; n < NMMA; ++n)
+                            if (n < p.m)
+                                store_y(y, (int64_t)n * it.n + row, __uint_as_float(v[n]) * gxw);
+                    }
+                } else {
+                    // a tile split between CTAs: this CTA's partial into its slot (0: the
+                    // tile its range starts in, 1: the tile it ends in), then the last of
+                    // the tile's CTAs to arrive sums every partial in stage order
+                    const int32_t T0 = it.s0 + c.tile * c.nst;  // the tile's first stage
+                    float* mine = p.part + ((size_t)(2 * blockIdx.x + (lo >= T0 ? 0 : 1)) * 32) * kRows;
 #pragma unroll
                     for (int n = 0; n < NMMA; ++n)
                         if (n < p.m)
-                            store_y(y, (int64_t)n * it.n + row, __uint_as_float(v[n]) * gxw);
+                            __stcg(mine + n * kRows + r, __uint_as_float(v[n]));
+                    __threadfence();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    const int bf = cta_of_stage(p, T0), bl = cta_of_stage(p, T0 + c.nst - 1);
+                    if (et == 0) {
+                        const unsigned prev = atomicAdd(p.count + bf, 1u);
+                        last_s = prev == (unsigned)(bl - bf);
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (last_s) {
+                        __threadfence();
+                        float acc[NMMA];
+#pragma unroll
+                        for (int n = 0; n < NMMA; ++n)
+                            acc[n] = 0.0f;
+                        for (int cc = bf; cc <= bl; ++cc) {
+                            const float* src =
+                                p.part + ((size_t)(2 * cc + (p.start[cc] >= T0 ? 0 : 1)) * 32) * kRows;
+#pragma unroll
+                            for (int n = 0; n < NMMA; ++n)
+                                if (n < p.m)
+                                    acc[n] += __ldcg(src + n * kRows + r);
+                        }
+                        if (row < it.n) {
+#pragma unroll
+                            for (int n = 0; n < NMMA; ++n)
+                                if (n < p.m)
+                                    store_y(y, (int64_t)n * it.n + row, acc[n] * gxw);
+                        }
+                        if (et == 0)
+                            atomicExch(p.count + bf, 0u);
+                    }
                 }
-                g += c.nst;
+                i += len;
                 ++tcount;
-                cursor_next_tile(c, p, lo, hi);
+                cursor_next_tile(c, p);
             }
         }
     }
@@ -587,20 +650,28 @@ bool tc_shape_ok(int64_t m, int64_t n, int64_t k)
            k % kStageK == 0 && k < (int64_t(1) << 30);
 }
 
+int64_t tc_workspace_bytes()
+{
+    int grid = device_sm_count(current_device());
+    if (grid > kTcMaxCtas)
+        grid = kTcMaxCtas;
+    return 1024 + (int64_t)2 * grid * 32 * kRows * (int64_t)sizeof(float);
+}
+
 cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool quantize, bool x_bf16,
-                            bool y_bf16, cudaStream_t stream, bool pdl)
+                            bool y_bf16, cudaStream_t stream, bool pdl, void* workspace,
+                            int64_t workspace_bytes)
 {
     if (count < 1 || count > kTcMaxItems || m < 1 || m > 32)
         return cudaErrorInvalidValue;
     static thread_local TcParams prm;  // 31 KB: kept off the stack
-    prm.count = count;
+    prm.count_items = count;
     prm.m = m;
     prm.y_bf16 = y_bf16 ? 1 : 0;
     cudaError_t e = device_status_address(&prm.status);
     if (e != cudaSuccess)
         return e;
-    int64_t tb[kTcMaxItems];  // weight bytes of one tile
-    int64_t total = 0, tiles = 0;
+    int64_t stages = 0;
     for (int i = 0; i < count; ++i) {
         const ChainLinear& L = items[i];
         TcItem& it = prm.item[i];
@@ -614,37 +685,56 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
         it.y = L.y;
         it.n = (int32_t)L.n;
         it.k = (int32_t)L.k;
-        it.tiles = (int32_t)((L.n + kRows - 1) / kRows);
-        it.t0 = (int32_t)tiles;
-        tb[i] = (int64_t)kRows * L.k * 9 / 16;
-        total += it.tiles * tb[i];
-        tiles += it.tiles;
+        it.s0 = (int32_t)stages;
+        it.pad = 0;
+        stages += ((L.n + kRows - 1) / kRows) * (L.k / kStageK);
     }
-    if (tiles >= (int64_t(1) << 31))
+    if (stages >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;
     const int dev = current_device();
     int grid = device_sm_count(dev);
     if (grid > kTcMaxCtas)
         grid = kTcMaxCtas;
-    if (grid > tiles)
-        grid = (int)tiles;
-    // contiguous tile ranges of (nearly) equal weight bytes
-    int i = 0;
-    int64_t before = 0;
-    for (int b = 0; b <= grid; ++b) {
-        const int64_t target = total * b / grid;
-        while (i < count - 1 && before + prm.item[i].tiles * tb[i] <= target) {
-            before += prm.item[i].tiles * tb[i];
-            ++i;
+    // every stage moves the same weight bytes (16 KB of codes, 2 KB of scales)
+    const bool streamk = workspace != nullptr && workspace_bytes >= tc_workspace_bytes();
+    if (streamk) {
+        // stage ranges of equal length; tiles cut at a range boundary are
+        // combined through the workspace
+        if (grid > stages)
+            grid = (int)stages;
+        for (int b = 0; b <= grid; ++b)
+            prm.start[b] = (int32_t)(stages * b / grid);
+        prm.count = static_cast<unsigned*>(workspace);
+        prm.part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + 1024);
+    } else {
+        // ranges on tile boundaries, each near an equal share of the stages
+        int64_t tiles = 0;
+        for (int i = 0; i < count; ++i)
+            tiles += (items[i].n + kRows - 1) / kRows;
+        if (grid > tiles)
+            grid = (int)tiles;
+        int i = 0;
+        for (int b = 0; b <= grid; ++b) {
+            const int64_t target = stages * b / grid;
+            // first tile boundary at or after target
+            while (i < count - 1 &&
+                   prm.item[i + 1].s0 <= target) {
+                ++i;
+            }
+            const int64_t nst = prm.item[i].k / kStageK;
+            const int64_t ti = (target - prm.item[i].s0 + nst - 1) / nst;
+            const int64_t g = prm.item[i].s0 + ti * nst;
+            prm.start[b] = (int32_t)(g < stages ? g : stages);
         }
-        int64_t t = prm.item[i].t0 + (target - before + tb[i] - 1) / tb[i];
-        prm.start[b] = (int32_t)(t < tiles ? t : tiles);
+        prm.start[0] = 0;
+        prm.start[grid] = (int32_t)stages;
+        for (int b = 1; b <= grid; ++b)
+            if (prm.start[b] < prm.start[b - 1])
+                prm.start[b] = prm.start[b - 1];
+        prm.count = nullptr;
+        prm.part = nullptr;
     }
-    prm.start[0] = 0;
-    prm.start[grid] = (int32_t)tiles;
-    for (int b = 1; b <= grid; ++b)
-        if (prm.start[b] < prm.start[b - 1])
-            prm.start[b] = prm.start[b - 1];
+    prm.grid = grid;
 
     bool tc_pdl = pdl;
     if (quantize) {
@@ -657,11 +747,12 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
                    : launch_tc_t<32>(prm, grid, stream, tc_pdl);
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl)
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl, void* workspace, int64_t workspace_bytes)
 {
     const ChainLinear one = {nullptr, a.xg, const_cast<uint8_t*>(a.xq), const_cast<uint8_t*>(a.xs),
                              a.wq, a.ws, a.wg, a.y.p, a.n, a.k};
-    return launch_tc_chain(&one, 1, a.m, false, false, a.y.bf16 != 0, a.stream, pdl);
+    return launch_tc_chain(&one, 1, a.m, false, false, a.y.bf16 != 0, a.stream, pdl, workspace,
+                           workspace_bytes);
 }
 
 }  // namespace nvfp4

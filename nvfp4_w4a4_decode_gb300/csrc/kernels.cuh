@@ -140,11 +140,17 @@ cudaError_t launch_chain_quant(const ChainLinear* items, int count, int m, bool 
 // launch of launch_chain_quant comes first.
 constexpr int kTcMaxItems = 160;
 constexpr int kTcMaxCtas = 256;
+// With a workspace of at least tc_workspace_bytes() (zero before its first
+// use; every completed launch leaves its counters zero) the CTAs get equal
+// shares of the stages and tiles cut between two CTAs are combined through
+// it in a fixed order; without one the shares end on tile boundaries.
 bool tc_shape_ok(int64_t m, int64_t n, int64_t k);
+int64_t tc_workspace_bytes();
 cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool quantize, bool x_bf16,
-                            bool y_bf16, cudaStream_t stream, bool pdl);
+                            bool y_bf16, cudaStream_t stream, bool pdl, void* workspace = nullptr,
+                            int64_t workspace_bytes = 0);
 // One linear through the tensor-core kernel (m up to 32).
-cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl);
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl, void* workspace, int64_t workspace_bytes);
 
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
 // Device address of the status word on the current device (for kernels of

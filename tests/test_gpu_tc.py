@@ -238,3 +238,58 @@ def test_tc_refusals(nv):
     assert nv.gemm_select(9, 4, 256, nv.KERNEL_AUTO) == -2
     torch.cuda.synchronize()
     assert (y.cpu().numpy() == 7.0).all()              # nothing launched
+
+
+# ---- equal stage shares through a workspace (tiles cut between CTAs) ----------
+
+@pytest.mark.parametrize("m,n,k", [(8, 300, 25600), (1, 1, 25600), (32, 130, 12288),
+                                   (4, 4096, 4096), (2, 129, 256)])
+def test_tc_split_tiles_deterministic(nv, m, n, k):
+    """Few tiles of many stages: every tile is cut between many CTAs (up to
+    about 50 partials per tile); the last to arrive sums them in stage order,
+    so repeated calls on one workspace give the same bits, and the counters
+    are left at zero (a second shape on the same workspace is right too)."""
+    x = synthetic.activations(m, k, seed=3 * m + k)
+    w = synthetic.weights(n, k, 0.02, seed=n + k)
+    ref, _ = oracle_y(x, w)
+    ops = gpu_operands(nv, x, w)
+    wsp = nv.workspace(m, n, k, nv.KERNEL_TC)
+    assert wsp is not None and wsp.numel() == nv.library().nvfp4_chain_workspace_size(m, 0)
+    y1 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_TC, workspace=wsp)
+    y2 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_TC, workspace=wsp, pdl=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y1.cpu().numpy(), y2.cpu().numpy())
+    assert gemm_error(y1.cpu().numpy(), ref) <= GEMM_TOL
+    assert not wsp[:1024].any().item()                     # counters back at zero
+    x2 = synthetic.activations(3, 1024, seed=5)
+    w2 = synthetic.weights(70, 1024, 0.02, seed=6)
+    ref2, _ = oracle_y(x2, w2)
+    y3 = nv.gemm_smallm(*gpu_operands(nv, x2, w2), kernel=nv.KERNEL_TC, workspace=wsp)
+    torch.cuda.synchronize()
+    assert gemm_error(y3.cpu().numpy(), ref2) <= GEMM_TOL
+
+
+def test_tc_without_workspace_tile_shares(nv):
+    """The C entry point without a workspace: CTA shares end on tile
+    boundaries (no partial sums); same bits as the reduction-free case of a
+    chain with a workspace is not required, only the oracle's bound."""
+    m, n, k = 8, 1000, 12288
+    x = synthetic.activations(m, k, seed=41)
+    w = synthetic.weights(n, k, 0.02, seed=42)
+    ref, _ = oracle_y(x, w)
+    xq, xs, xg, wq, ws, wg = gpu_operands(nv, x, w)
+    y = torch.full((m, n), float("nan"), device="cuda")
+    st = nv.library().nvfp4_gemm_smallm_ex(
+        xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(), wg.data_ptr(),
+        y.data_ptr(), m, n, k, nv.KERNEL_TC, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert gemm_error(y.cpu().numpy(), ref) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("m", [1, 8])
+def test_tc_chain_without_workspace(nv, m):
+    lins = make_chain(nv, m, CHAIN_SHAPES, seed=60 + m)
+    nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC, workspace=False).run(pdl=True)
+    torch.cuda.synchronize()
+    check_chain(lins)
