@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
+    __shared__ int epi_fail_s;  // an epilogue warp gave up: every epilogue warp stops
     __shared__ int last_s;
 
     asm volatile("griddepcontrol.launch_dependents;");
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         }
         mbar_init(smem_u32(&drain_bar), 1);
         abort_s = 0;
+        epi_fail_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -486,8 +488,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 const int buf = tcount & 1;
                 const int32_t st_a = c.st;
                 const int32_t len = c.nst - c.st < total - i ? c.nst - c.st : total - i;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&accf_bar[buf]), (tcount >> 1) & 1,
-                                                       abort_flag, p.status)))
+                // one decision for the four epilogue warps (they share a named
+                // barrier below, so none may leave alone)
+                const bool wok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&accf_bar[buf]),
+                                                                   (tcount >> 1) & 1, abort_flag,
+                                                                   p.status));
+                if (lane == 0 && !wok)
+                    epi_fail_s = 1;
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (*(volatile int*)&epi_fail_s)
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 uint32_t v[NMMA];
