@@ -138,7 +138,10 @@ cudaError_t launch_chain_quant(const ChainLinear* items, int count, int m, bool 
 // kTcMaxItems independent linears: m in 1..32, k a multiple of 256, n below
 // 2^30; w_q 16-byte, x_q / x_s / w_s 16-byte aligned.  With quantize, one
 // launch of launch_chain_quant comes first.
-constexpr int kTcMaxItems = 160;
+#ifndef NVFP4_TC_MAX_ITEMS
+#define NVFP4_TC_MAX_ITEMS 160
+#endif
+constexpr int kTcMaxItems = NVFP4_TC_MAX_ITEMS;
 constexpr int kTcMaxCtas = 256;
 // With a workspace of at least tc_workspace_bytes() (zero before its first
 // use; every completed launch leaves its counters zero) the CTAs get equal
