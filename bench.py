@@ -188,7 +188,7 @@ class DecodeStack:
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
                  fused: bool = True, kernel: int = 0, bf16: bool = False, mode: str = "launches",
-                 chain_kernel: int = 0):
+                 chain_kernel: int = 0, chain_workspace: bool = True):
         self.nv, self.torch = nv, torch
         self.m = m
         self.bf16 = bf16   # BF16 activations in and BF16 outputs out
@@ -255,9 +255,11 @@ class DecodeStack:
                               torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev))
                              for lin in self.lins] for _ in range(layers)]
             self.chain = nv.Chain([self._chain_entry(l, j) for l in range(layers)
-                                   for j in range(4)], kernel=chain_kernel)
+                                   for j in range(4)], kernel=chain_kernel,
+                                  workspace=chain_workspace)
             self.chain_j = [nv.Chain([self._chain_entry(l, j) for l in range(layers)],
-                                     kernel=chain_kernel) for j in range(4)]
+                                     kernel=chain_kernel, workspace=chain_workspace)
+                            for j in range(4)]
         torch.cuda.synchronize()
 
     def _chain_entry(self, l: int, j: int):
@@ -588,7 +590,8 @@ def run_ours(args) -> dict:
         mode = "chain" if chain_ok else "launches"
     stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
                         fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16,
-                        mode=mode, chain_kernel=KERNELS[args.chain_kernel](nv))
+                        mode=mode, chain_kernel=KERNELS[args.chain_kernel](nv),
+                        chain_workspace=not args.no_chain_workspace)
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -654,7 +657,9 @@ def run_ours(args) -> dict:
         del g, gq, gp
     # the other way of running the same step, on the same weights
     other = None
-    alt = "launches" if mode == "chain" else ("chain" if stack.has_chain else None)
+    # (one call per linear takes M up to 8)
+    alt = ("launches" if args.m <= 8 else None) if mode == "chain" else \
+        ("chain" if stack.has_chain else None)
     if alt is not None:
         stack.mode = alt
         g_alt = stack.capture(stack.step)
@@ -1166,6 +1171,9 @@ def main():
     ap.add_argument("--chain-kernel", default="auto", choices=["auto", "gemv", "tc"],
                     help="engine of the chain step (auto: CUDA-core stream at M <= 2, "
                          "tensor cores above)")
+    ap.add_argument("--no-chain-workspace", action="store_true",
+                    help="run the tensor-core chain without its workspace (CTA shares end on "
+                         "tile boundaries)")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNELS),
                     help="GEMM kernel for the decode step (and for --single)")
     ap.add_argument("--reps", type=int, default=3)

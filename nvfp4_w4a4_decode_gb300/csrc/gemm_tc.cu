@@ -54,7 +54,10 @@ constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
 constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
-constexpr int kPrefetch = 6;               // stages the scale / activation warps load ahead
+#ifndef NVFP4_TC_PREFETCH
+#define NVFP4_TC_PREFETCH 6
+#endif
+constexpr int kPrefetch = NVFP4_TC_PREFETCH;  // stages the scale / activation warps load ahead
 constexpr int kThreads = 320;              // 10 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSfa = 64;           // 16 columns per ring slot
@@ -162,12 +165,21 @@ __host__ __device__ constexpr uint32_t instr_desc(int nmma)
 
 // 16 bytes of a weight row's block scales; the L2 fetches the surrounding
 // 256 bytes (the next stages' scales of the row) with the same DRAM access.
+#ifndef NVFP4_TC_SCALE_L2_256
+#define NVFP4_TC_SCALE_L2_256 1
+#endif
 __device__ __forceinline__ uint4 ld_nc_u4(const void* p)
 {
     uint4 v;
+#if NVFP4_TC_SCALE_L2_256
     asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+#else
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#endif
     return v;
 }
 
