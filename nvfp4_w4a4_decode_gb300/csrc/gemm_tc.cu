@@ -54,10 +54,12 @@ constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
 constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
+// Stages the scale / activation warps load ahead (measured on the decode
+// step: 6 against 4, 0.691 against 0.703-0.746 ms at M = 8).
 #ifndef NVFP4_TC_PREFETCH
 #define NVFP4_TC_PREFETCH 6
 #endif
-constexpr int kPrefetch = NVFP4_TC_PREFETCH;  // stages the scale / activation warps load ahead
+constexpr int kPrefetch = NVFP4_TC_PREFETCH;
 constexpr int kThreads = 320;              // 10 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSfa = 64;           // 16 columns per ring slot
@@ -163,10 +165,11 @@ __host__ __device__ constexpr uint32_t instr_desc(int nmma)
     return (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 }
 
-// 16 bytes of a weight row's block scales; the L2 fetches the surrounding
-// 256 bytes (the next stages' scales of the row) with the same DRAM access.
+// 16 bytes of a weight row's block scales (one stage).  Asking L2 for the
+// surrounding 256 bytes (NVFP4_TC_SCALE_L2_256=1) measured slower on the
+// decode step (M = 8: 0.725 against 0.691 ms), so it is off.
 #ifndef NVFP4_TC_SCALE_L2_256
-#define NVFP4_TC_SCALE_L2_256 1
+#define NVFP4_TC_SCALE_L2_256 0
 #endif
 __device__ __forceinline__ uint4 ld_nc_u4(const void* p)
 {
