@@ -114,9 +114,14 @@ int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g,
  *   y               device float[m][n], overwritten
  * m must be 0..8 (NVFP4_ERR_UNSUPPORTED otherwise).  One kernel launch:
  * the CUDA-core stream at M = 1, the split-K tensor-core kernel at M >= 2
- * when its plan needs no workspace (use nvfp4_gemm_smallm_ws to offer one),
- * else a TMA-fed or cluster tensor-core kernel.  The result does not depend on the
- * launch order of CTAs: every reduction has a fixed order.
+ * when its plan needs no workspace, else a TMA-fed or cluster tensor-core
+ * kernel.  The result does not depend on the launch order of CTAs: every
+ * reduction has a fixed order.  Without a workspace the split-K kernel only
+ * takes K <= 4096 at M >= 3, and the fallbacks measured 1.6-3.6x slower on
+ * the longer-K decode layers (8B down, 32B o / down): callers that want the
+ * fast path offer a workspace (nvfp4_gemm_smallm_ws), use the allocation-free
+ * nvfp4_gemm_smallm_static, or batch independent linears into one
+ * nvfp4_linear_chain call.
  */
 int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
                       const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
@@ -271,10 +276,10 @@ int nvfp4_gemm_smallm_ws(const uint8_t* x_q, const uint8_t* x_s, const float* x_
  * least nvfp4_gemm_workspace_size() bytes -- same plan, same result bits --
  * except that the scratch is a library-owned static device array of
  * nvfp4_gemm_static_scratch_bytes() (4 MiB) per device.  Its address is
- * looked up once per device, on the first call, which also clears its
- * counter region on `stream` (the counters must start at zero; the array is
- * zero when the library loads and every completed call leaves them zero).
- * Nothing is allocated or freed.
+ * looked up once per device, on the first call (looked up again after a
+ * launch fails); the counters it holds start at zero because the array is
+ * zero when the library loads and every completed call leaves them zero.
+ * Nothing is allocated, freed or cleared.
  *   options   NVFP4_KERNEL_AUTO or NVFP4_KERNEL_SPLITK, optionally
  *             NVFP4_FLAG_PDL and NVFP4_FLAG_Y_BF16 (anything else:
  *             NVFP4_ERR_INVALID_ARG)

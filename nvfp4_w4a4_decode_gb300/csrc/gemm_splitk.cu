@@ -582,30 +582,36 @@ constexpr int64_t kStaticScratchBytes = int64_t(4) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // Device address of the static scratch on the current device, looked up
-// once per device; the first lookup also clears the counter region on
-// `stream` (the counters must start at zero; every completed call leaves
-// them at zero).
-cudaError_t static_scratch(cudaStream_t stream, void** out)
+// once per device.  Its counter region needs no clearing: the array is zero
+// when the module loads and every completed call leaves the counters zero
+// (a memset here would also race with a call still running on another
+// stream).  A launch that fails drops the cached address, so that it is
+// looked up again on the next call (after a context reset, for instance).
+std::mutex g_scratch_mu;
+std::unordered_map<int, void*> g_scratch_addr;
+
+cudaError_t static_scratch(void** out)
 {
-    static std::mutex mu;
-    static std::unordered_map<int, void*> addr;
     const int dev = current_device();
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = addr.find(dev);
-    if (it != addr.end()) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    auto it = g_scratch_addr.find(dev);
+    if (it != g_scratch_addr.end()) {
         *out = it->second;
         return cudaSuccess;
     }
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess)
         return e;
-    e = cudaMemsetAsync(p, 0, (size_t)counter_region(kStaticScratchBytes), stream);
-    if (e != cudaSuccess)
-        return e;
-    addr[dev] = p;
+    g_scratch_addr[dev] = p;
     *out = p;
     return cudaSuccess;
+}
+
+void forget_static_scratch()
+{
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    g_scratch_addr.erase(current_device());
 }
 
 }  // namespace
@@ -624,10 +630,13 @@ bool splitk_static_fits(int64_t m, int64_t n, int64_t k)
 cudaError_t launch_gemm_splitk_static(const GemmArgs& a, bool pdl)
 {
     void* scratch = nullptr;
-    const cudaError_t e = static_scratch(a.stream, &scratch);
+    const cudaError_t e = static_scratch(&scratch);
     if (e != cudaSuccess)
         return e;
-    return launch_gemm_splitk(a, pdl, scratch, kStaticScratchBytes);
+    const cudaError_t l = launch_gemm_splitk(a, pdl, scratch, kStaticScratchBytes);
+    if (l != cudaSuccess)
+        forget_static_scratch();
+    return l;
 }
 
 bool splitk_shape_ok(int64_t m, int64_t k)

@@ -10,6 +10,7 @@
 // or approximate division can change a code.
 #include "formats.cuh"
 #include "kernels.cuh"
+#include "launch_cache.cuh"
 
 namespace nvfp4 {
 
@@ -125,11 +126,13 @@ cudaError_t launch_global_scale(const float* t, int64_t count, float* g, cudaStr
     if (err != cudaSuccess)
         return err;
     if (count > 0) {
+        // enough CTAs for every SM a few times over, then a grid-stride loop
         int64_t blocks = (count / 4 + 255) / 256;
         if (blocks < 1)
             blocks = 1;
-        if (blocks > 4 * 152 * 8)
-            blocks = 4 * 152 * 8;
+        const int64_t cap = (int64_t)32 * device_sm_count(current_device());
+        if (blocks > cap)
+            blocks = cap;
         amax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(t, count, reinterpret_cast<uint32_t*>(g));
         err = cudaGetLastError();
         if (err != cudaSuccess)

@@ -23,3 +23,18 @@ def sampled_error(y_vals, ref_vals, row_rms):
     denom = np.maximum(np.abs(ref_vals), row_rms)
     denom = np.where(denom > 0, denom, 1.0)
     return float(np.max(np.abs(np.asarray(y_vals, np.float64) - ref_vals) / denom))
+
+
+def plain_rel_error(y, ref):
+    """max |y - ref| / |ref| over the outputs with |ref| >= the rms of their
+    row: the plain relative error where it is well conditioned, reported
+    beside gemm_error (which floors the denominator at the row rms)."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
+    mask = (np.abs(ref) >= rms) & (np.abs(ref) > 0)
+    if not mask.any():
+        return 0.0
+    return float(np.max(np.abs(y - ref)[mask] / np.abs(ref)[mask]))

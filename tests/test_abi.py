@@ -200,3 +200,55 @@ def test_splitk_planner_properties_host_only(lib):
             assert need == 0 or need >= 1024 * ((n + 15) // 16)   # 2+ partials of 512 B per tile
     for m, k in ((1, 4000), (9, 4096), (0, 4096)):
         assert lib.nvfp4_gemm_select_ws(m, 100, k, SPLITK, 1 << 30) < 0
+
+
+def _chain_arr(**over):
+    fields = dict(x=FAKE, x_g=FAKE, x_q=FAKE, x_s=FAKE, w_q=FAKE, w_s=FAKE, w_g=FAKE, y=FAKE,
+                  n=64, k=4096)
+    fields.update(over)
+    arr = (nv.ChainLinear * 1)(nv.ChainLinear(**fields))
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def test_chain_rejects_before_launch(lib):
+    """Every refusal of the multi-linear entry points returns before a launch."""
+    f = lib.nvfp4_linear_chain
+    p, _keep = _chain_arr()
+    assert f(p, 1, 3, nv.KERNEL_GEMV, None) == 2            # CUDA-core stream: M of 1 or 2
+    assert f(p, 1, 33, nv.KERNEL_AUTO, None) == 2           # tensor cores: M up to 32
+    assert f(p, 1, 1, nv.KERNEL_SPLITK, None) == 2          # no chain on this kernel
+    assert f(p, 1, 1, 0x10000, None) == 1                   # unknown flag
+    assert f(p, -1, 1, 0, None) == 1
+    assert f(p, 0, 1, 0, None) == 0                         # nothing to do
+    assert f(None, 0, 1, 0, None) == 0
+    assert f(p, 1, 0, 0, None) == 0
+    for over, want in ((dict(k=4100), 1),                   # K not a multiple of 16
+                       (dict(k=4112), 2),                   # nor of 256 (tensor cores)
+                       (dict(n=-1), 1),
+                       (dict(x_q=FAKE + 16), 1),            # codes 32-byte aligned
+                       (dict(w_s=FAKE + 4), 1),             # tensor cores: scales 16-byte aligned
+                       (dict(x=None), 1),                   # the quantiser reads x
+                       (dict(y=None), 1)):
+        q, _k = _chain_arr(**over)
+        assert f(q, 1, 1, 0, None) == want, over
+    q, _k = _chain_arr(k=2560)                               # K % 1024 != 0: not on the
+                                                             # CUDA-core stream
+    assert f(q, 1, 1, nv.KERNEL_GEMV, None) == 2
+    assert lib.nvfp4_linear_chain_ws(p, 1, 1, 0, FAKE + 8, 16, None) == 1   # workspace alignment
+    assert lib.nvfp4_linear_chain_ws(p, 1, 1, 0, None, 16, None) == 1       # size without memory
+
+
+def test_chain_queries(lib):
+    assert lib.nvfp4_chain_workspace_size(1, nv.KERNEL_GEMV) == 0
+    assert lib.nvfp4_chain_workspace_size(1, nv.KERNEL_AUTO) >= 1024
+    assert lib.nvfp4_chain_workspace_size(3, nv.KERNEL_GEMV) == -2
+    assert lib.nvfp4_chain_workspace_size(33, nv.KERNEL_AUTO) == -2
+    assert lib.nvfp4_chain_workspace_size(0, 0) == -1
+    assert lib.nvfp4_chain_supported(1, 4096, 4096) == 1
+    assert lib.nvfp4_chain_supported(32, 4096, 256) == 1
+    assert lib.nvfp4_chain_supported(1, 4096, 4112) == 0
+    assert lib.nvfp4_chain_supported(33, 4096, 4096) == 0
+    assert lib.nvfp4_gemm_select(9, 4, 256, nv.KERNEL_TC) == nv.KERNEL_TC
+    assert lib.nvfp4_gemm_select(9, 4, 256, nv.KERNEL_AUTO) == -2
+    assert lib.nvfp4_gemm_select(33, 4, 256, nv.KERNEL_TC) == -2
+    assert lib.nvfp4_gemm_select(4, 4, 272, nv.KERNEL_TC) == -2

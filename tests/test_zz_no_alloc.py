@@ -74,3 +74,31 @@ def test_static_refuses_scratch_beyond_its_size(nv):
     assert st == 2
     torch.cuda.synchronize()
     assert (y.cpu().numpy() == 7.0).all()
+
+
+def test_static_allocates_no_device_memory(nv):
+    """Free device memory (cudaMemGetInfo, which sees every allocation on the
+    device, not only torch's) is unchanged by repeated calls once the first
+    call has looked up the scratch address; the shape here needs the scratch
+    (its split-K plan cuts K into several chunks)."""
+    m, n, k = 4, 5120, 25600
+    assert nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) > 0
+    ops, _, _ = operands(nv, m, n, k, seed=11)
+    y = torch.empty((m, n), device="cuda")
+    lib = nv.library()
+    st = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        xq, xs, xg, wq, ws, wg = ops
+        return lib.nvfp4_gemm_smallm_static(
+            xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
+            wg.data_ptr(), y.data_ptr(), m, n, k, nv.KERNEL_SPLITK, st)
+
+    assert call() == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(20):
+        assert call() == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
