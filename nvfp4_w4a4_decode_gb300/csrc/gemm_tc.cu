@@ -49,7 +49,10 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kStages = 8;                 // shared-memory ring
+#ifndef NVFP4_TC_STAGES
+#define NVFP4_TC_STAGES 8
+#endif
+constexpr int kStages = NVFP4_TC_STAGES;   // shared-memory ring
 constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
@@ -62,8 +65,9 @@ constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 
 constexpr int kPrefetch = NVFP4_TC_PREFETCH;
 constexpr int kThreads = 320;              // 10 warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColSfa = 64;           // 16 columns per ring slot
-constexpr uint32_t kColSfb = 192;          // 16 columns per ring slot
+constexpr uint32_t kColSfa = 64;                       // 16 columns per ring slot
+constexpr uint32_t kColSfb = kColSfa + 16 * kStages;   // 16 columns per ring slot
+static_assert(kColSfb + 16 * kStages <= kTmemCols, "scale slots fit the tensor memory");
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
 constexpr size_t kSmem = (size_t)kStages * (kABytes + kBBytes) + 1024;  // + alignment slack
 
@@ -639,10 +643,12 @@ bool weight_map(CUtensorMap* m, const uint8_t* wq, int64_t n, int64_t k)
     const cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
     const cuuint32_t box[2] = {128, kRows};
     const cuuint32_t es[2] = {1, 1};
+#ifndef NVFP4_TC_L2_PROMOTION
+#define NVFP4_TC_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wq), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, NVFP4_TC_L2_PROMOTION,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int NMMA>
