@@ -188,7 +188,7 @@ class DecodeStack:
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
                  fused: bool = True, kernel: int = 0, bf16: bool = False, mode: str = "launches",
-                 chain_kernel: int = 0, chain_workspace: bool = True):
+                 chain_kernel: int = 0, chain_workspace: bool = True, tiled: bool = True):
         self.nv, self.torch = nv, torch
         self.m = m
         self.bf16 = bf16   # BF16 activations in and BF16 outputs out
@@ -249,6 +249,13 @@ class DecodeStack:
         self.xq = [(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
                     torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev)) for lin in self.lins]
         self.chain = None
+        # the tensor-core chain streams tile-major weights (an offline repack of
+        # the same bytes) unless asked for the row-major ones
+        self.tiled = bool(tiled) and self.has_chain and chain_kernel in (0, nv.KERNEL_TC)
+        self.wt = None
+        if self.tiled:
+            self.wt = [[nv.tile_weight(*self.w[l][j]) for j in range(4)] for l in range(layers)]
+            torch.cuda.synchronize()
         if self.has_chain:
             # chain: one pair per linear (every linear of the step is in flight)
             self.xq_item = [[(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
@@ -263,7 +270,8 @@ class DecodeStack:
         torch.cuda.synchronize()
 
     def _chain_entry(self, l: int, j: int):
-        return (self.x[l][j], self.xg[l][j], self.xq_item[l][j], self.w[l][j], self.y[l][j])
+        wts = self.wt[l][j] if self.tiled else self.w[l][j]
+        return (self.x[l][j], self.xg[l][j], self.xq_item[l][j], wts, self.y[l][j])
 
     def weight_fp32(self, l: int, j: int):
         """FP32 weights of linear j of layer l, drawn on the device: N(0, 0.02^2),
@@ -591,7 +599,8 @@ def run_ours(args) -> dict:
     stack = DecodeStack(nv, torch, m=args.m, layers=args.layers, pdl=not args.no_pdl,
                         fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16,
                         mode=mode, chain_kernel=KERNELS[args.chain_kernel](nv),
-                        chain_workspace=not args.no_chain_workspace)
+                        chain_workspace=not args.no_chain_workspace,
+                        tiled=not args.row_major_weights)
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -681,8 +690,9 @@ def run_ours(args) -> dict:
 
     # the committed traffic capture is of the default step's GEMM kernel
     default_step = args.m == 1 and not args.bf16 and not args.fused and args.kernel == "auto"
-    traffic_name = ("gemm_chain" if stack.chosen(stack.lins[0]) == nv.KERNEL_GEMV else "gemm_tc") \
-        if mode == "chain" else "gemm_smallm"
+    traffic_name = ("gemm_chain" if stack.chosen(stack.lins[0]) == nv.KERNEL_GEMV else
+                    ("gemm_tc_tiled" if stack.tiled else "gemm_tc")) if mode == "chain" else \
+        "gemm_smallm"
     traffic = profile_traffic(traffic_name) if default_step else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -697,6 +707,7 @@ def run_ours(args) -> dict:
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "graph": "one CUDA graph per step",
                    "mode": mode,
+                   "weights": "tile-major" if stack.tiled else "row-major",
                    "pdl": not args.no_pdl,
                    "fused_quantize": args.fused,
                    "io": "bf16 X in, bf16 Y out" if args.bf16 else "fp32 X in, fp32 Y out"},
@@ -794,6 +805,7 @@ TRAFFIC_SOURCES = {
     "gemm_chain": ("api.cu", "formats.cuh", "gemm_chain.cu", "kernels.cuh", "launch_cache.cuh",
                    "stream_core.cuh"),
     "gemm_tc": ("api.cu", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh"),
+    "gemm_tc_tiled": ("api.cu", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh"),
 }
 
 
@@ -1171,6 +1183,9 @@ def main():
     ap.add_argument("--chain-kernel", default="auto", choices=["auto", "gemv", "tc"],
                     help="engine of the chain step (auto: CUDA-core stream at M <= 2, "
                          "tensor cores above)")
+    ap.add_argument("--row-major-weights", action="store_true",
+                    help="the tensor-core chain reads the row-major packed weights (TMA with a "
+                         "tensor map) instead of the tile-major repack")
     ap.add_argument("--no-chain-workspace", action="store_true",
                     help="run the tensor-core chain without its workspace (CTA shares end on "
                          "tile boundaries)")

@@ -179,6 +179,12 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       copy of X.
  * NVFP4_FLAG_Y_BF16     (GEMM, linear) Y is BF16 (uint16 [m][n], 2-byte
  *                       aligned): the FP32 result rounded to nearest even.
+ * NVFP4_FLAG_W_TILED    (NVFP4_KERNEL_TC GEMMs and tensor-core chains only) w_q
+ *                       and w_s are in the tile-major layout written by
+ *                       nvfp4_tile_weight, 16-byte aligned, instead of
+ *                       row-major: every pipeline stage of the tensor-core
+ *                       kernel is then two contiguous bulk copies (16 KB of
+ *                       codes, 2 KB of scales) instead of 128 strided pieces.
  * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
  *                       while the previous kernel on the stream is still
  *                       running and waits for it before it touches anything
@@ -202,6 +208,7 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
 #define NVFP4_FLAG_FUSED_QUANTIZE 0x200u
 #define NVFP4_FLAG_X_BF16 0x400u
 #define NVFP4_FLAG_Y_BF16 0x800u
+#define NVFP4_FLAG_W_TILED 0x1000u
 #define NVFP4_FLAG_TEST_WAIT_TIMEOUT 0x10000u
 
 /* Bits of the device status word (nvfp4_device_status). */
@@ -374,7 +381,7 @@ typedef struct {
 /* Linears per launch: longer lists are cut into launches of this many
  * (CUDA-core stream; tensor-core kernel). */
 #define NVFP4_CHAIN_MAX_LINEARS 256
-#define NVFP4_TC_MAX_LINEARS 160
+#define NVFP4_TC_MAX_LINEARS 150
 
 /*
  * Quantise every linear's activations (one launch: the recipe of
@@ -393,7 +400,9 @@ typedef struct {
  *                       aligned; NVFP4_TC_MAX_LINEARS linears per launch
  * -- OR-ed with NVFP4_FLAG_PDL (the first launch may start before the
  * previous kernel on the stream ends; the weights must not be written by
- * it), NVFP4_FLAG_X_BF16, NVFP4_FLAG_Y_BF16.  Every description is checked
+ * it), NVFP4_FLAG_X_BF16, NVFP4_FLAG_Y_BF16, NVFP4_FLAG_W_TILED (tensor
+ * cores only: every linear's w_q / w_s in the tile-major layout of
+ * nvfp4_tile_weight, 16-byte aligned).  Every description is checked
  * before anything is launched: NVFP4_ERR_INVALID_ARG for a null or
  * misaligned pointer or a bad size, NVFP4_ERR_UNSUPPORTED for an m or shape
  * the chosen kernel does not take.  Asynchronous on `stream`; nothing
@@ -431,6 +440,28 @@ int nvfp4_linear_chain_ws(const nvfp4_chain_linear* linears, int64_t count, int6
                           uint32_t options, void* workspace, size_t workspace_bytes, void* stream);
 int nvfp4_gemm_chain_ws(const nvfp4_chain_linear* linears, int64_t count, int64_t m,
                         uint32_t options, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Tile-major weight layout of the tensor-core kernel (an offline repack of
+ * the row-major packed weights; the bytes are the same, only their order and
+ * the zero rows that pad N to a multiple of 128 differ).  For tile t (weight
+ * rows 128 t .. 128 t + 127) and stage s (K elements 256 s .. 256 s + 255):
+ *   t_q  block (t, s) of 16384 bytes at offset (t * K/256 + s) * 16384: row r
+ *        at 128 r, its 16-byte chunk c (K elements 256 s + 32 c ..) at
+ *        16 (c XOR (r mod 8)) -- the 128-byte-swizzled image the tensor core
+ *        reads from shared memory;
+ *   t_s  block (t, s) of 2048 bytes at offset (t * K/256 + s) * 2048: row r's
+ *        16 block scales of the stage at 16 r.
+ * Rows past n are zero.  nvfp4_tiled_weight_bytes returns the code bytes
+ * (ceil(n/128) * 128 * k/2) and writes the scale bytes (ceil(n/128) * 128 *
+ * k/16) to *scale_bytes (may be NULL), or minus a status code; k must be a
+ * multiple of 256.  nvfp4_tile_weight writes both from w_q [n][k/2] and
+ * w_s [n][k/16] (all four pointers 16-byte aligned, device memory; two
+ * kernels on `stream`).  Pass the results with NVFP4_FLAG_W_TILED.
+ */
+int64_t nvfp4_tiled_weight_bytes(int64_t n, int64_t k, int64_t* scale_bytes);
+int nvfp4_tile_weight(const uint8_t* w_q, const uint8_t* w_s, int64_t n, int64_t k, uint8_t* t_q,
+                      uint8_t* t_s, void* stream);
 
 /* Workspace bytes the chain entry points use with this m and options on the
  * current device (0 for the CUDA-core stream), or minus a status code.  The

@@ -27,6 +27,7 @@ __all__ = [
     "nvfp4_gemm_workspace_size", "nvfp4_workspace", "gemm_workspace_size", "workspace",
     "nvfp4_gemm_smallm_static", "gemm_smallm_static", "nvfp4_read_probe", "read_probe",
     "ChainLinear", "Chain", "CHAIN_MAX_LINEARS", "nvfp4_chain_supported", "chain_supported",
+    "TiledWeight", "nvfp4_tile_weight", "tile_weight",
 ]
 
 MAX_M = 8
@@ -71,6 +72,8 @@ SIGNATURES = {
     "nvfp4_gemm_chain_ws": ([_p, _i64, _i64, ctypes.c_uint32, _p, ctypes.c_size_t, _p],
                             ctypes.c_int),
     "nvfp4_chain_workspace_size": ([_i64, ctypes.c_uint32], _i64),
+    "nvfp4_tiled_weight_bytes": ([_i64, _i64, ctypes.POINTER(_i64)], _i64),
+    "nvfp4_tile_weight": ([_p, _p, _i64, _i64, _p, _p, _p], ctypes.c_int),
 }
 
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_GEMV, KERNEL_MMA, KERNEL_TMA, KERNEL_SPLITK = 0, 1, 2, 3, 4, 5
@@ -81,6 +84,7 @@ FLAG_PDL = 0x100
 FLAG_FUSED_QUANTIZE = 0x200
 FLAG_X_BF16 = 0x400
 FLAG_Y_BF16 = 0x800
+FLAG_W_TILED = 0x1000
 FLAG_TEST_WAIT_TIMEOUT = 0x10000
 DEVICE_WAIT_TIMEOUT = 1
 
@@ -243,18 +247,30 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
     ``nvfp4_workspace``) is made per call when the kernel needs one and none
     is given.  The output is float32, or bfloat16 (``out_dtype`` or the dtype
     of ``out``): the float32 result rounded to nearest even."""
+    tiled = isinstance(wq, TiledWeight)
+    if tiled:                        # gemm_smallm(xq, xs, xg, TiledWeight, ...)
+        tw = wq
+        if ws is not None or wg is not None:
+            raise ValueError("pass a TiledWeight in place of (wq, ws, wg), with ws = wg = None")
+        wq, ws, wg = tw.t_q, tw.t_s, tw.w_g
     for t, name in ((xq, "xq"), (xs, "xs"), (wq, "wq"), (ws, "ws")):
         _dev(t, torch.uint8, name)
     _dev(xg, torch.float32, "xg")
     _dev(wg, torch.float32, "wg")
     m, kh = xq.shape
-    n = wq.shape[0]
     k = kh * 2
-    if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
-        raise ValueError("operand shapes disagree")
+    if tiled:
+        n = tw.n
+        if tw.k != k or xs.shape != (m, k // 16):
+            raise ValueError("operand shapes disagree")
+        kernel = KERNEL_TC
+    else:
+        n = wq.shape[0]
+        if wq.shape[1] != kh or xs.shape != (m, k // 16) or ws.shape != (n, k // 16):
+            raise ValueError("operand shapes disagree")
     y, yflag = _y_out(out, m, n, out_dtype, xq.device)
     opts = int(kernel) | (FLAG_PDL if pdl else 0) | (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0)
-    opts |= yflag
+    opts |= yflag | (FLAG_W_TILED if tiled else 0)
     wp, wn, _keep = _ws_args(workspace, m, n, k, kernel, xq.device)
     _check("nvfp4_gemm_smallm", library().nvfp4_gemm_smallm_ws(
         xq.data_ptr(), xs.data_ptr(), xg.data_ptr(), wq.data_ptr(), ws.data_ptr(),
@@ -350,10 +366,46 @@ def nvfp4_linear(x: torch.Tensor, xg: torch.Tensor, wq, ws, wg, out=None, x_out=
 linear = nvfp4_linear
 
 
+# ---- tile-major weights of the tensor-core kernel ------------------------------
+
+class TiledWeight:
+    """Packed weights in the tensor-core kernel's tile-major layout
+    (``nvfp4_tile_weight``): ``t_q`` / ``t_s`` flat uint8 device tensors, the
+    tensor scale ``w_g`` and the logical shape (n, k).  Accepted wherever a
+    ``(w_q, w_s, w_g)`` triple is, on the tensor-core kernel."""
+
+    def __init__(self, t_q, t_s, w_g, n: int, k: int):
+        self.t_q, self.t_s, self.w_g, self.n, self.k = t_q, t_s, w_g, int(n), int(k)
+
+
+def nvfp4_tile_weight(wq: torch.Tensor, ws: torch.Tensor, wg: torch.Tensor) -> TiledWeight:
+    """Repack row-major packed weights (w_q [n, k/2], w_s [n, k/16]) into the
+    tile-major layout; k a multiple of 256."""
+    _dev(wq, torch.uint8, "wq")
+    _dev(ws, torch.uint8, "ws")
+    _dev(wg, torch.float32, "wg")
+    n, kh = wq.shape
+    k = kh * 2
+    if ws.shape != (n, k // 16):
+        raise ValueError("operand shapes disagree")
+    sb = _i64(0)
+    qb = int(library().nvfp4_tiled_weight_bytes(n, k, ctypes.byref(sb)))
+    if qb < 0:
+        raise Nvfp4Error("nvfp4_tiled_weight_bytes", -qb)
+    tq = torch.empty(max(qb, 16), dtype=torch.uint8, device=wq.device)
+    ts = torch.empty(max(sb.value, 16), dtype=torch.uint8, device=wq.device)
+    _check("nvfp4_tile_weight", library().nvfp4_tile_weight(
+        wq.data_ptr(), ws.data_ptr(), n, k, tq.data_ptr(), ts.data_ptr(), _stream(wq)))
+    return TiledWeight(tq, ts, wg, n, k)
+
+
+tile_weight = nvfp4_tile_weight
+
+
 # ---- many independent linears in one persistent launch ----------------------
 
 CHAIN_MAX_LINEARS = 256
-TC_MAX_LINEARS = 160
+TC_MAX_LINEARS = 150
 
 
 class ChainLinear(ctypes.Structure):
@@ -387,7 +439,17 @@ class Chain:
         self._keep = []
         xdt = ydt = None
         m = None
-        for x, xg, (xq, xs), (wq, ws, wg), y in linears:
+        tiled = None
+        for x, xg, (xq, xs), wts, y in linears:
+            is_tiled = isinstance(wts, TiledWeight)
+            if tiled is None:
+                tiled = is_tiled
+            elif tiled != is_tiled:
+                raise ValueError("every linear of a chain has the same weight layout")
+            if is_tiled:
+                wq, ws, wg = wts.t_q, wts.t_s, wts.w_g
+            else:
+                wq, ws, wg = wts
             if x.dtype not in (torch.float32, torch.bfloat16):
                 raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
             _dev(x, x.dtype, "x")
@@ -399,9 +461,13 @@ class Chain:
                 raise ValueError(f"y must be float32 or bfloat16, got {y.dtype}")
             _dev(y, y.dtype, "y")
             mm, k = x.shape
-            n = wq.shape[0]
-            if (xq.shape != (mm, k // 2) or xs.shape != (mm, k // 16) or wq.shape != (n, k // 2)
-                    or ws.shape != (n, k // 16) or y.shape != (mm, n)):
+            n = wts.n if is_tiled else wq.shape[0]
+            if is_tiled:
+                wshape_ok = wts.k == k
+            else:
+                wshape_ok = wq.shape == (n, k // 2) and ws.shape == (n, k // 16)
+            if (xq.shape != (mm, k // 2) or xs.shape != (mm, k // 16) or not wshape_ok
+                    or y.shape != (mm, n)):
                 raise ValueError("operand shapes disagree")
             if m is None:
                 m, xdt, ydt = mm, x.dtype, y.dtype
@@ -414,8 +480,10 @@ class Chain:
         self.m = m
         self.count = len(descs)
         self._arr = (ChainLinear * self.count)(*descs)
+        self.tiled = bool(tiled)
         self._flags = (FLAG_X_BF16 if xdt == torch.bfloat16 else 0) | \
-                      (FLAG_Y_BF16 if ydt == torch.bfloat16 else 0)
+                      (FLAG_Y_BF16 if ydt == torch.bfloat16 else 0) | \
+                      (FLAG_W_TILED if self.tiled else 0)
         self.device = linears[0][0].device
         self.kernel = int(kernel)
         if self.kernel == KERNEL_AUTO:
@@ -456,7 +524,8 @@ class Chain:
         wp, wn = self._ws()
         _check("nvfp4_gemm_chain", library().nvfp4_gemm_chain_ws(
             ctypes.cast(self._arr, ctypes.c_void_p), self.count, self.m,
-            self.kernel | (self._flags & FLAG_Y_BF16) | (FLAG_PDL if pdl else 0), wp, wn,
+            self.kernel | (self._flags & (FLAG_Y_BF16 | FLAG_W_TILED)) | (FLAG_PDL if pdl else 0),
+            wp, wn,
             torch.cuda.current_stream(self.device).cuda_stream))
 
 

@@ -151,9 +151,12 @@ int check_gemm_args(int64_t m, int64_t n, int64_t k, uint32_t options)
     if (m < 0 || n < 0 || k < 0 || (k % 16) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if ((options & ~(uint32_t)(NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 |
-                               NVFP4_FLAG_TEST_WAIT_TIMEOUT)) != 0)
+                               NVFP4_FLAG_TEST_WAIT_TIMEOUT | NVFP4_FLAG_W_TILED)) != 0)
         return NVFP4_ERR_INVALID_ARG;
     if ((options & NVFP4_FLAG_TEST_WAIT_TIMEOUT) && (options & NVFP4_KERNEL_MASK) != NVFP4_KERNEL_TMA)
+        return NVFP4_ERR_INVALID_ARG;
+    // the tile-major weight layout is read by the tensor-core kernel only
+    if ((options & NVFP4_FLAG_W_TILED) && (options & NVFP4_KERNEL_MASK) != NVFP4_KERNEL_TC)
         return NVFP4_ERR_INVALID_ARG;
     // M above 8 only on the tensor-core kernel, by request
     if (m > ((options & NVFP4_KERNEL_MASK) == NVFP4_KERNEL_TC ? 32 : 8))
@@ -184,11 +187,16 @@ int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x_q, 8) || !aligned(w_q, 8) || !aligned(x_g, 4) || !aligned(w_g, 4))
         return NVFP4_ERR_INVALID_ARG;
+    const bool tiled = (options & NVFP4_FLAG_W_TILED) != 0;
+    if (tiled && (!aligned(w_q, 16) || !aligned(w_s, 16)))
+        return NVFP4_ERR_INVALID_ARG;
     const bool fast_ptrs = aligned(x_q, 32) && aligned(w_q, 32) && aligned(x_s, 4) &&
                            aligned(w_s, 4);
     const bool tma_ptrs = fast_ptrs && aligned(x_s, 32) && aligned(w_s, 32);
     const int64_t ws_bytes = workspace ? (int64_t)workspace_bytes : 0;
-    const int kern = select_kernel(m, n, k, options, fast_ptrs, tma_ptrs, ws_bytes);
+    const int kern = select_kernel(m, n, k, options, tiled ? aligned(x_q, 32) : fast_ptrs,
+                                   tiled ? aligned(x_q, 32) && aligned(x_s, 32) : tma_ptrs,
+                                   ws_bytes);
     if (kern < 0)
         return -kern;
     const bool pdl = (options & NVFP4_FLAG_PDL) != 0;
@@ -203,7 +211,7 @@ int gemm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g, const uint8_t
     case NVFP4_KERNEL_SPLITK:
         return from_cuda(nvfp4::launch_gemm_splitk(a, pdl, workspace, ws_bytes));
     case NVFP4_KERNEL_TC:
-        return from_cuda(nvfp4::launch_gemm_tc(a, pdl, workspace, ws_bytes));
+        return from_cuda(nvfp4::launch_gemm_tc(a, pdl, workspace, ws_bytes, tiled));
     default:
         return from_cuda(nvfp4::launch_gemm_generic(a));
     }
@@ -374,6 +382,7 @@ int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uin
     const bool x_bf16 = (options & NVFP4_FLAG_X_BF16) != 0;
     const bool y_bf16 = (options & NVFP4_FLAG_Y_BF16) != 0;
     const bool tc = engine == (int)NVFP4_KERNEL_TC;
+    const bool tiled = (options & NVFP4_FLAG_W_TILED) != 0;
     *kept = 0;
     for (int64_t i = 0; i < count; ++i) {
         const nvfp4_chain_linear& L = linears[i];
@@ -388,7 +397,7 @@ int check_chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uin
             (quantize && L.x == nullptr))
             return NVFP4_ERR_INVALID_ARG;
         const uintptr_t sal = tc ? 16 : 4;  // the tensor-core kernel loads scales 16 bytes at a time
-        if (!aligned(L.x_q, 32) || !aligned(L.w_q, 32) || !aligned(L.x_s, sal) ||
+        if (!aligned(L.x_q, 32) || !aligned(L.w_q, tiled ? 16 : 32) || !aligned(L.x_s, sal) ||
             !aligned(L.w_s, sal) || !aligned(L.x_g, 4) || !aligned(L.w_g, 4) ||
             !aligned(L.y, y_bf16 ? 2 : 4) || (quantize && !aligned(L.x, x_bf16 ? 8 : 16)))
             return NVFP4_ERR_INVALID_ARG;
@@ -404,12 +413,14 @@ int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t 
     if (workspace == nullptr ? workspace_bytes != 0 : !aligned(workspace, 16))
         return NVFP4_ERR_INVALID_ARG;
     const uint32_t allowed = NVFP4_KERNEL_MASK | NVFP4_FLAG_PDL | NVFP4_FLAG_Y_BF16 |
-                             (quantize ? NVFP4_FLAG_X_BF16 : 0u);
+                             NVFP4_FLAG_W_TILED | (quantize ? NVFP4_FLAG_X_BF16 : 0u);
     if (count < 0 || m < 0 || (count > 0 && linears == nullptr) || (options & ~allowed) != 0)
         return NVFP4_ERR_INVALID_ARG;
     const int engine = chain_engine(m, options);
     if (engine < 0)
         return NVFP4_ERR_UNSUPPORTED;
+    if ((options & NVFP4_FLAG_W_TILED) && engine != (int)NVFP4_KERNEL_TC)
+        return NVFP4_ERR_INVALID_ARG;  // the tile-major layout is the tensor-core kernel's
     if (m > (engine == (int)NVFP4_KERNEL_TC ? 32 : 2))
         return NVFP4_ERR_UNSUPPORTED;
     if (count == 0 || m == 0)
@@ -436,7 +447,8 @@ int chain(const nvfp4_chain_linear* linears, int64_t count, int64_t m, uint32_t 
         const cudaError_t e =
             engine == (int)NVFP4_KERNEL_TC
                 ? nvfp4::launch_tc_chain(part, (int)kept, (int)m, quantize, xb, yb, s, pdl || i0 > 0,
-                                         workspace, (int64_t)workspace_bytes)
+                                         workspace, (int64_t)workspace_bytes,
+                                         (options & NVFP4_FLAG_W_TILED) != 0)
                 : nvfp4::launch_linear_chain(part, (int)kept, (int)m, quantize, xb, yb, s,
                                              pdl || i0 > 0);
         if (e != cudaSuccess)
@@ -480,6 +492,29 @@ int64_t nvfp4_chain_workspace_size(int64_t m, uint32_t options)
     if (engine < 0 || m > (engine == (int)NVFP4_KERNEL_TC ? 32 : 2))
         return -NVFP4_ERR_UNSUPPORTED;
     return engine == (int)NVFP4_KERNEL_TC ? nvfp4::tc_workspace_bytes() : 0;
+}
+
+int64_t nvfp4_tiled_weight_bytes(int64_t n, int64_t k, int64_t* scale_bytes)
+{
+    if (n < 0 || k < 0 || k % 256 != 0)
+        return -NVFP4_ERR_INVALID_ARG;
+    if (scale_bytes != nullptr)
+        *scale_bytes = nvfp4::tiled_scale_bytes(n, k);
+    return nvfp4::tiled_code_bytes(n, k);
+}
+
+int nvfp4_tile_weight(const uint8_t* w_q, const uint8_t* w_s, int64_t n, int64_t k, uint8_t* t_q,
+                      uint8_t* t_s, void* stream)
+{
+    if (n < 0 || k < 0 || k % 256 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (n == 0 || k == 0)
+        return NVFP4_OK;
+    if (w_q == nullptr || w_s == nullptr || t_q == nullptr || t_s == nullptr ||
+        !aligned(w_q, 16) || !aligned(w_s, 16) || !aligned(t_q, 16) || !aligned(t_s, 16))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(nvfp4::launch_tile_weight(w_q, w_s, n, k, t_q, t_s,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4_chain_supported(int64_t m, int64_t n, int64_t k)

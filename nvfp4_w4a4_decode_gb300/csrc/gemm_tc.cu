@@ -69,20 +69,26 @@ constexpr uint32_t kColSfa = 64;                       // 16 columns per ring sl
 constexpr uint32_t kColSfb = kColSfa + 16 * kStages;   // 16 columns per ring slot
 static_assert(kColSfb + 16 * kStages <= kTmemCols, "scale slots fit the tensor memory");
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
-constexpr size_t kSmem = (size_t)kStages * (kABytes + kBBytes) + 1024;  // + alignment slack
+constexpr int kSBytes = kRows * 16;        // weight block scales of a stage (tile-major layout)
+// ring: weight codes, activation codes, and (tile-major weights) weight scales
+constexpr size_t smem_bytes(bool tiled)
+{
+    return (size_t)kStages * (kABytes + kBBytes + (tiled ? kSBytes : 0)) + 1024;  // + alignment
+}
 
 struct TcItem {
     const uint8_t* xq;
     const uint8_t* xs;
     const float* xg;
-    const uint8_t* ws;
+    const uint8_t* wq;  // tile-major weight codes (the row-major ones go through wmap)
+    const uint8_t* ws;  // weight block scales: row-major, or tile-major
     const float* wg;
     void* y;
     int32_t n, k;
     int32_t s0;  // first stage of this linear in the launch's stage list
     int32_t pad;
 };
-static_assert(sizeof(TcItem) == 64, "TcItem is one 64-byte line");
+static_assert(sizeof(TcItem) == 72, "TcItem layout");
 
 struct TcParams {
     CUtensorMap wmap[kTcMaxItems];  // weight codes [n][k/2]: boxes of 128 bytes x 128 rows,
@@ -267,7 +273,7 @@ struct AuxLoad {
     uint4 b1;  // activation codes, chunk u + 128 (M > 16)
 };
 
-template <int NMMA>
+template <int NMMA, bool TILED>
 __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cursor& c, int r,
                                          int lane, int u)
 {
@@ -275,7 +281,8 @@ __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cu
     const int32_t kb = it.k / 16, kh = it.k / 2;
     const int64_t row = (int64_t)c.tile * kRows + r;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    a.sa = row < it.n ? ld_nc_u4(it.ws + row * kb + c.st * 16) : z;
+    if constexpr (!TILED)  // tile-major scales arrive with the stage's bulk copy
+        a.sa = row < it.n ? ld_nc_u4(it.ws + row * kb + c.st * 16) : z;
     a.sb = lane < p.m ? __ldg(reinterpret_cast<const uint4*>(it.xs + lane * kb + c.st * 16)) : z;
     a.b0 = u < p.m * 8
                ? __ldg(reinterpret_cast<const uint4*>(it.xq + (u >> 3) * kh + c.st * 128 +
@@ -288,7 +295,7 @@ __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cu
                    : z;
 }
 
-template <int NMMA>
+template <int NMMA, bool TILED>
 __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -305,8 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     const int32_t total = hi - lo;  // this CTA's stages
     // tile-aligned (1024-byte) ring: weight slots, then activation slots
     const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes;
+    const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes, sS0 = sB0 + kStages * kBBytes;
     uint8_t* sB_gen = smem_raw + (sB0 - smem_u32(smem_raw));
+    const uint8_t* sS_gen = smem_raw + (sS0 - smem_u32(smem_raw));
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -347,12 +355,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                                p.status))
                     break;
                 const uint32_t fb = smem_u32(&full_bar[slot]);
-                mbar_expect_tx(fb, kABytes);
-                asm volatile(
-                    "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-                    "[%0], [%1, {%2, %3}], [%4];" ::"r"(sA0 + slot * kABytes),
-                    "l"(&p.wmap[c.item]), "r"(c.st * 128), "r"(c.tile * kRows), "r"(fb)
-                    : "memory");
+                if constexpr (TILED) {
+                    // tile-major layout: the stage's codes (already in the swizzled
+                    // shared-memory image) and its scales are two contiguous blocks
+                    const size_t blk = (size_t)c.tile * c.nst + c.st;
+                    mbar_expect_tx(fb, kABytes + kSBytes);
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                        "[%0], [%1], %2, [%3];" ::"r"(sA0 + slot * kABytes),
+                        "l"(p.item[c.item].wq + blk * kABytes), "r"(kABytes), "r"(fb)
+                        : "memory");
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                        "[%0], [%1], %2, [%3];" ::"r"(sS0 + slot * kSBytes),
+                        "l"(p.item[c.item].ws + blk * kSBytes), "r"(kSBytes), "r"(fb)
+                        : "memory");
+                } else {
+                    mbar_expect_tx(fb, kABytes);
+                    asm volatile(
+                        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::"
+                        "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(sA0 + slot * kABytes),
+                        "l"(&p.wmap[c.item]), "r"(c.st * 128), "r"(c.tile * kRows), "r"(fb)
+                        : "memory");
+                }
                 issued = i + 1;
                 cursor_next_stage(c, p);
             }
@@ -439,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
 #pragma unroll
             for (int d = 0; d < kPrefetch; ++d) {
                 if (d < total) {
-                    aux_load<NMMA>(ring[d], p, pf, r, lane, u);
+                    aux_load<NMMA, TILED>(ring[d], p, pf, r, lane, u);
                     cursor_next_stage(pf, p);
                 }
             }
@@ -459,8 +484,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
+                    uint4 sa4 = ring[d].sa;
+                    if constexpr (TILED) {
+                        // the weight scales come with the stage's bulk copy
+                        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full_bar[slot]),
+                                                               (i / kStages) & 1, abort_flag,
+                                                               p.status))) {
+                            ok = false;
+                            break;
+                        }
+                        sa4 = *reinterpret_cast<const uint4*>(sS_gen + slot * kSBytes + r * 16);
+                    }
                     asm volatile("tcgen05.fence::after_thread_sync;");
-                    const uint32_t sa[4] = {ring[d].sa.x, ring[d].sa.y, ring[d].sa.z, ring[d].sa.w};
+                    const uint32_t sa[4] = {sa4.x, sa4.y, sa4.z, sa4.w};
                     const uint32_t sb[4] = {ring[d].sb.x, ring[d].sb.y, ring[d].sb.z, ring[d].sb.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -487,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     if (lane == 0)
                         mbar_arrive(smem_u32(&aux_bar[slot]));
                     if (i + kPrefetch < total) {
-                        aux_load<NMMA>(ring[d], p, pf, r, lane, u);
+                        aux_load<NMMA, TILED>(ring[d], p, pf, r, lane, u);
                         cursor_next_stage(pf, p);
                     }
                 }
@@ -651,18 +687,19 @@ bool weight_map(CUtensorMap* m, const uint8_t* wq, int64_t n, int64_t k)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMMA>
+template <int NMMA, bool TILED>
 cudaError_t launch_tc_t(TcParams& prm, int grid, cudaStream_t stream, bool pdl)
 {
-    auto kern = tc_chain_kernel<NMMA>;
+    auto kern = tc_chain_kernel<NMMA, TILED>;
     const int dev = current_device();
-    cudaError_t e = ensure_smem_limit(kern, kSmem, dev);
+    const size_t smem = smem_bytes(TILED);
+    cudaError_t e = ensure_smem_limit(kern, smem, dev);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -690,7 +727,7 @@ int64_t tc_workspace_bytes()
 
 cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool quantize, bool x_bf16,
                             bool y_bf16, cudaStream_t stream, bool pdl, void* workspace,
-                            int64_t workspace_bytes)
+                            int64_t workspace_bytes, bool tiled)
 {
     if (count < 1 || count > kTcMaxItems || m < 1 || m > 32)
         return cudaErrorInvalidValue;
@@ -705,8 +742,9 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
     for (int i = 0; i < count; ++i) {
         const ChainLinear& L = items[i];
         TcItem& it = prm.item[i];
-        if (!weight_map(&prm.wmap[i], L.wq, L.n, L.k))
+        if (!tiled && !weight_map(&prm.wmap[i], L.wq, L.n, L.k))
             return cudaErrorInvalidValue;
+        it.wq = L.wq;
         it.xq = L.xq;
         it.xs = L.xs;
         it.xg = L.xg;
@@ -773,16 +811,93 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
             return e;
         tc_pdl = true;  // the weight loads do not depend on the quantiser
     }
-    return m <= 16 ? launch_tc_t<16>(prm, grid, stream, tc_pdl)
-                   : launch_tc_t<32>(prm, grid, stream, tc_pdl);
+    if (tiled)
+        return m <= 16 ? launch_tc_t<16, true>(prm, grid, stream, tc_pdl)
+                       : launch_tc_t<32, true>(prm, grid, stream, tc_pdl);
+    return m <= 16 ? launch_tc_t<16, false>(prm, grid, stream, tc_pdl)
+                   : launch_tc_t<32, false>(prm, grid, stream, tc_pdl);
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl, void* workspace, int64_t workspace_bytes)
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl, void* workspace, int64_t workspace_bytes,
+                           bool tiled)
 {
     const ChainLinear one = {nullptr, a.xg, const_cast<uint8_t*>(a.xq), const_cast<uint8_t*>(a.xs),
                              a.wq, a.ws, a.wg, a.y.p, a.n, a.k};
     return launch_tc_chain(&one, 1, a.m, false, false, a.y.bf16 != 0, a.stream, pdl, workspace,
-                           workspace_bytes);
+                           workspace_bytes, tiled);
+}
+
+// ---- tile-major weight layout ---------------------------------------------------
+
+namespace {
+
+// One 16-byte chunk of codes per thread: padded row p (tile p / 128, row
+// r = p % 128), chunk h of the row (stage h / 8, chunk c = h % 8 of the
+// stage's 128 bytes) goes to block (tile, stage), row r, swizzled chunk
+// c ^ (r % 8) -- the image TMA with 128-byte swizzle writes to shared memory.
+// Rows past n are zero.
+__global__ void tile_codes_kernel(const uint8_t* __restrict__ wq, int64_t n, int64_t k,
+                                  int64_t rows_padded, uint8_t* __restrict__ tq)
+{
+    const int64_t chunks = k / 32;  // 16-byte chunks per row
+    const int64_t total = rows_padded * chunks;
+    const int64_t nst = k / kStageK;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / chunks, h = i - row * chunks;
+        const int64_t t = row / kRows, r = row - t * kRows, st = h / 8, c = h - st * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < n)
+            v = __ldg(reinterpret_cast<const uint4*>(wq + row * (k / 2)) + h);
+        *reinterpret_cast<uint4*>(tq + ((t * nst + st) * kRows + r) * 128 + ((c ^ (r & 7)) << 4)) = v;
+    }
+}
+
+// One stage's 16 scale bytes of one padded row per thread: block (tile, stage),
+// row r at 16 r.  Rows past n are zero.
+__global__ void tile_scales_kernel(const uint8_t* __restrict__ ws, int64_t n, int64_t k,
+                                   int64_t rows_padded, uint8_t* __restrict__ ts)
+{
+    const int64_t nst = k / kStageK;
+    const int64_t total = rows_padded * nst;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / nst, st = i - row * nst;
+        const int64_t t = row / kRows, r = row - t * kRows;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < n)
+            v = __ldg(reinterpret_cast<const uint4*>(ws + row * (k / 16)) + st);
+        *reinterpret_cast<uint4*>(ts + ((t * nst + st) * kRows + r) * 16) = v;
+    }
+}
+
+}  // namespace
+
+int64_t tiled_code_bytes(int64_t n, int64_t k)
+{
+    return (n + kRows - 1) / kRows * kRows * (k / 2);
+}
+
+int64_t tiled_scale_bytes(int64_t n, int64_t k)
+{
+    return (n + kRows - 1) / kRows * kRows * (k / 16);
+}
+
+cudaError_t launch_tile_weight(const uint8_t* wq, const uint8_t* ws, int64_t n, int64_t k,
+                               uint8_t* tq, uint8_t* ts, cudaStream_t stream)
+{
+    const int64_t rows = (n + kRows - 1) / kRows * kRows;
+    const int sms = device_sm_count(current_device());
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+    int64_t g1 = (rows * (k / 32) + 255) / 256, g2 = (rows * (k / kStageK) + 255) / 256;
+    g1 = g1 < 1 ? 1 : (g1 > cap ? cap : g1);
+    g2 = g2 < 1 ? 1 : (g2 > cap ? cap : g2);
+    tile_codes_kernel<<<(unsigned)g1, 256, 0, stream>>>(wq, n, k, rows, tq);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    tile_scales_kernel<<<(unsigned)g2, 256, 0, stream>>>(ws, n, k, rows, ts);
+    return cudaGetLastError();
 }
 
 }  // namespace nvfp4

@@ -139,7 +139,7 @@ cudaError_t launch_chain_quant(const ChainLinear* items, int count, int m, bool 
 // 2^30; w_q 16-byte, x_q / x_s / w_s 16-byte aligned.  With quantize, one
 // launch of launch_chain_quant comes first.
 #ifndef NVFP4_TC_MAX_ITEMS
-#define NVFP4_TC_MAX_ITEMS 160
+#define NVFP4_TC_MAX_ITEMS 150
 #endif
 constexpr int kTcMaxItems = NVFP4_TC_MAX_ITEMS;
 constexpr int kTcMaxCtas = 256;
@@ -149,11 +149,24 @@ constexpr int kTcMaxCtas = 256;
 // it in a fixed order; without one the shares end on tile boundaries.
 bool tc_shape_ok(int64_t m, int64_t n, int64_t k);
 int64_t tc_workspace_bytes();
+// With tiled, every linear's wq / ws are in the tile-major layout of
+// launch_tile_weight (16-byte aligned).
 cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool quantize, bool x_bf16,
                             bool y_bf16, cudaStream_t stream, bool pdl, void* workspace = nullptr,
-                            int64_t workspace_bytes = 0);
+                            int64_t workspace_bytes = 0, bool tiled = false);
 // One linear through the tensor-core kernel (m up to 32).
-cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl, void* workspace, int64_t workspace_bytes);
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool pdl, void* workspace, int64_t workspace_bytes,
+                           bool tiled);
+
+// Tile-major weight layout of the tensor-core kernel: rows padded to a
+// multiple of 128; codes as 16 KB blocks (tile, stage of 256 K) holding the
+// 128-byte-swizzled shared-memory image, scales as 2 KB blocks (tile, stage)
+// of 16 bytes per row.  Sizes in bytes, and the repack from the row-major
+// layout (two kernels).
+int64_t tiled_code_bytes(int64_t n, int64_t k);
+int64_t tiled_scale_bytes(int64_t n, int64_t k);
+cudaError_t launch_tile_weight(const uint8_t* wq, const uint8_t* ws, int64_t n, int64_t k,
+                               uint8_t* tq, uint8_t* ts, cudaStream_t stream);
 
 cudaError_t read_device_status(cudaStream_t stream, unsigned* out, bool clear);
 // Device address of the status word on the current device (for kernels of

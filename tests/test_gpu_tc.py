@@ -293,3 +293,89 @@ def test_tc_chain_without_workspace(nv, m):
     nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC, workspace=False).run(pdl=True)
     torch.cuda.synchronize()
     check_chain(lins)
+
+
+# ---- tile-major weights (nvfp4_tile_weight, NVFP4_FLAG_W_TILED) ----------------
+
+def tile_reference(wq, ws, n, k):
+    """The tile-major layout written out from its definition (include/nvfp4.h):
+    blocks (tile, stage) of 128 rows; row r's chunk c of the stage at chunk
+    c XOR (r mod 8); scales 16 bytes a row; rows past n zero."""
+    tiles, nst = (n + 127) // 128, k // 256
+    rows = tiles * 128
+    q = np.zeros((rows, k // 2), np.uint8)
+    q[:n] = wq
+    s = np.zeros((rows, k // 16), np.uint8)
+    s[:n] = ws
+    q5 = q.reshape(tiles, 128, nst, 8, 16).transpose(0, 2, 1, 3, 4)   # [t][st][r][c][16]
+    tq = np.empty_like(q5)
+    for r in range(128):
+        for c in range(8):
+            tq[:, :, r, c ^ (r & 7)] = q5[:, :, r, c]
+    ts = s.reshape(tiles, 128, nst, 16).transpose(0, 2, 1, 3)           # [t][st][r][16]
+    return tq.reshape(-1), np.ascontiguousarray(ts).reshape(-1)
+
+
+@pytest.mark.parametrize("n,k", [(300, 4096), (128, 256), (1, 12288), (129, 512)])
+def test_tile_weight_layout(nv, n, k):
+    w = synthetic.weights(n, k, 0.02, seed=n + k)
+    owq, ows, _ = oracle.pack_weight(w)
+    wq, ws, wg = nv.pack_weight(dev(w))
+    tw = nv.tile_weight(wq, ws, wg)
+    torch.cuda.synchronize()
+    rq, rs = tile_reference(owq, ows, n, k)
+    np.testing.assert_array_equal(tw.t_q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(tw.t_s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 300, 4096), (8, 129, 12288), (32, 640, 5120), (3, 1, 256)])
+def test_tc_tiled_weights_same_bits(nv, m, n, k):
+    """Tile-major weights give the same bits as the row-major ones (the same
+    operands reach the tensor core) and stay within the oracle's bound."""
+    x = synthetic.activations(m, k, seed=2 * m + k)
+    w = synthetic.weights(n, k, 0.02, seed=3 * n + k)
+    ref, _ = oracle_y(x, w)
+    xq, xs, xg, wq, ws, wg = gpu_operands(nv, x, w)
+    y_row = nv.gemm_smallm(xq, xs, xg, wq, ws, wg, kernel=nv.KERNEL_TC)
+    tw = nv.tile_weight(wq, ws, wg)
+    y_tile = nv.gemm_smallm(xq, xs, xg, tw, None, None)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y_tile.cpu().numpy(), y_row.cpu().numpy())
+    assert gemm_error(y_tile.cpu().numpy(), ref) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("m", [1, 8])
+def test_tc_chain_tiled_weights(nv, m):
+    lins = make_chain(nv, m, CHAIN_SHAPES, seed=70 + m)
+    nv.Chain([L["entry"] for L in lins], kernel=nv.KERNEL_TC).run()
+    torch.cuda.synchronize()
+    rows = [L["entry"][4].cpu().numpy().copy() for L in lins]
+    tiled = []
+    for L in lins:
+        xd, xg, codes, (wq, ws, wg), y = L["entry"]
+        y.fill_(float("nan"))
+        tiled.append((xd, xg, codes, nv.tile_weight(wq, ws, wg), y))
+    ch = nv.Chain(tiled)
+    assert ch.tiled
+    ch.run(pdl=True)
+    torch.cuda.synchronize()
+    for L, r in zip(lins, rows):
+        np.testing.assert_array_equal(L["entry"][4].cpu().numpy(), r)
+    check_chain(lins)
+
+
+def test_tiled_flag_refusals(nv):
+    lib = nv.library()
+    g = torch.ones(1, device="cuda")
+    z = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    y = torch.full((2, 4), 7.0, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    args = (z.data_ptr(), z.data_ptr(), g.data_ptr(), z.data_ptr(), z.data_ptr(), g.data_ptr(),
+            y.data_ptr(), 2, 4, 256)
+    assert lib.nvfp4_gemm_smallm_ex(*args, nv.KERNEL_SPLITK | nv.FLAG_W_TILED, st) == 1
+    assert lib.nvfp4_gemm_smallm_ex(*args, nv.KERNEL_AUTO | nv.FLAG_W_TILED, st) == 1
+    assert lib.nvfp4_tile_weight(z.data_ptr(), z.data_ptr(), 4, 272, z.data_ptr(),
+                                 z.data_ptr(), st) == 1
+    assert lib.nvfp4_tiled_weight_bytes(300, 4096, None) == 384 * 2048
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy() == 7.0).all()
