@@ -57,6 +57,14 @@ constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
 constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
+// Stages ahead of the copy being issued whose weights the producer asks L2
+// to fetch (0: none): DRAM reads in flight beyond what the shared-memory ring
+// holds.
+#ifndef NVFP4_TC_L2_AHEAD
+#define NVFP4_TC_L2_AHEAD 16
+#endif
+constexpr int kL2Ahead = NVFP4_TC_L2_AHEAD;
+
 // Stages the scale / activation warps load ahead (measured on the decode
 // step: 6 against 4, 0.691 against 0.703-0.746 ms at M = 8).
 #ifndef NVFP4_TC_PREFETCH
@@ -347,6 +355,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         if (lane == 0 && total > 0) {
             Cursor c;
             cursor_at(c, p, lo);
+            // L2 prefetch cursor: kL2Ahead stages ahead of the copies issued
+            Cursor pc;
+            cursor_at(pc, p, lo);
+            auto l2_prefetch = [&](const Cursor& q) {
+                if constexpr (TILED) {
+                    const size_t blk = (size_t)q.tile * q.nst + q.st;
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                                 ::"l"(p.item[q.item].wq + blk * kABytes), "r"(kABytes)
+                                 : "memory");
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                                 ::"l"(p.item[q.item].ws + blk * kSBytes), "r"(kSBytes)
+                                 : "memory");
+                } else {
+                    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];"
+                                 ::"l"(&p.wmap[q.item]), "r"(q.st * 128), "r"(q.tile * kRows)
+                                 : "memory");
+                }
+            };
+            int32_t pfd = 0;  // stages prefetched so far
+            if constexpr (kL2Ahead > 0) {
+                // the ring's first kStages stages are copied at once; prefetch the
+                // ones after them up to the distance
+                for (int32_t j = 0; j < kStages && j < total; ++j)
+                    cursor_next_stage(pc, p);
+                pfd = kStages < total ? kStages : total;
+                for (; pfd < kL2Ahead && pfd < total; ++pfd) {
+                    l2_prefetch(pc);
+                    cursor_next_stage(pc, p);
+                }
+            }
             int32_t issued = 0;
             for (int32_t i = 0; i < total; ++i) {
                 const int slot = i % kStages;
@@ -380,6 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 }
                 issued = i + 1;
                 cursor_next_stage(c, p);
+                if constexpr (kL2Ahead > 0) {
+                    if (pfd < total && pfd <= i + kL2Ahead) {
+                        l2_prefetch(pc);
+                        cursor_next_stage(pc, p);
+                        ++pfd;
+                    }
+                }
             }
             // drain: every copy issued has landed before the CTA can exit
             for (int32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
