@@ -58,10 +58,12 @@ constexpr int kStageK = 256;               // K elements per stage (128 code byt
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
 constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
 // Stages ahead of the copy being issued whose weights the producer asks L2
-// to fetch (0: none): DRAM reads in flight beyond what the shared-memory ring
-// holds.
+// to fetch (0: none), to keep DRAM reads in flight beyond what the
+// shared-memory ring holds.  Measured on the 8B decode step it only adds
+// contention (M = 1: 0.665 ms without, 0.674 / 0.685 / 1.05 ms at 8 / 16 /
+// 32 stages ahead), so it is off.
 #ifndef NVFP4_TC_L2_AHEAD
-#define NVFP4_TC_L2_AHEAD 16
+#define NVFP4_TC_L2_AHEAD 0
 #endif
 constexpr int kL2Ahead = NVFP4_TC_L2_AHEAD;
 
