@@ -665,13 +665,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
 #pragma unroll
                         for (int n = 0; n < NMMA; ++n)
                             acc[n] = 0.0f;
-                        for (int cc = bf; cc <= bl; ++cc) {
-                            const float* src =
+                        // partials in stage order, two contributors' loads in flight
+                        // at a time (the additions keep that order)
+                        for (int cc = bf; cc <= bl; cc += 2) {
+                            const bool two = cc + 1 <= bl;
+                            const float* s0 =
                                 p.part + ((size_t)(2 * cc + (p.start[cc] >= T0 ? 0 : 1)) * 32) * kRows;
+                            const float* s1 =
+                                two ? p.part + ((size_t)(2 * (cc + 1) +
+                                                         (p.start[cc + 1] >= T0 ? 0 : 1)) * 32) * kRows
+                                    : s0;
+                            float a0[NMMA], a1[NMMA];
 #pragma unroll
-                            for (int n = 0; n < NMMA; ++n)
-                                if (n < p.m)
-                                    acc[n] += __ldcg(src + n * kRows + r);
+                            for (int n = 0; n < NMMA; ++n) {
+                                if (n < p.m) {
+                                    a0[n] = __ldcg(s0 + n * kRows + r);
+                                    a1[n] = two ? __ldcg(s1 + n * kRows + r) : 0.0f;
+                                }
+                            }
+#pragma unroll
+                            for (int n = 0; n < NMMA; ++n) {
+                                if (n < p.m) {
+                                    acc[n] += a0[n];
+                                    if (two)
+                                        acc[n] += a1[n];
+                                }
+                            }
                         }
                         if (row < it.n) {
 #pragma unroll
