@@ -516,10 +516,9 @@ def time_chain_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
     xd = torch.from_numpy(xa).cuda()
     xg = nv.global_scale(xd)
     entries = []
-    for wq, ws, wg in weights:
+    for wts in weights:                 # (w_q, w_s, w_g) triples or TiledWeight
         codes = nv.quantize_act(xd, xg)
-        entries.append((xd, xg, codes, (wq, ws, wg),
-                        torch.empty((m, lin.n), device="cuda")))
+        entries.append((xd, xg, codes, wts, torch.empty((m, lin.n), device="cuda")))
     ch = nv.Chain(entries, kernel=kernel)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -546,7 +545,7 @@ def sweep(nv, torch, stack, peaks, args) -> dict:
     out = {"8B": {}, "32B": {}, "C1": tiny_latency(nv, torch, kernels, stack.pdl)}
     reps = 5
 
-    def entry(m, lin, ws):
+    def entry(m, lin, ws, wt=None):
         auto = auto_choice(nv, m, lin) if m <= 8 else nv.KERNEL_TC
         ent = {"kernel": nv.KERNEL_NAMES.get(auto)}
         for name, kid in kernels.items():
@@ -558,21 +557,26 @@ def sweep(nv, torch, stack, peaks, args) -> dict:
                 continue
             ent[name] = time_linear(nv, torch, ws, lin, m, kid, stack.pdl, reps)
         ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
-        ent["tc_chain"] = time_chain_linear(nv, torch, ws, lin, m, nv.KERNEL_TC, stack.pdl, reps)
+        # inside a chain: the tile-major weights the decode step uses
+        ent["tc_chain"] = time_chain_linear(nv, torch, wt if wt is not None else ws, lin, m,
+                                            nv.KERNEL_TC, stack.pdl, reps)
         ent["tc_chain"]["frac_of_peak"] = round(ent["tc_chain"]["GBps"] / peaks["hbm_gbs"], 4)
         return ent
 
     w8 = {j: [stack.w[l][j] for l in range(stack.layers)] for j in range(4)}
+    w8t = {j: ([stack.wt[l][j] for l in range(stack.layers)] if stack.tiled else None)
+           for j in range(4)}
     for m in tuple(synthetic.M_SWEEP_8B) + tuple(synthetic.M_SWEEP_WIDE):
-        out["8B"][f"M={m}"] = {lin.name: entry(m, lin, w8[j])
+        out["8B"][f"M={m}"] = {lin.name: entry(m, lin, w8[j], w8t[j])
                                for j, lin in enumerate(synthetic.LINEARS_8B)}
     for j, lin in enumerate(synthetic.LINEARS_32B):
         per_copy = lin.n * lin.k * 9 // 16
         copies = max(3, -(-400_000_000 // per_copy))
         ws = make_weights(nv, torch, lin, synthetic.WEIGHT_STD_32B, copies, seed=4000 + 100 * j)
+        wt = [nv.tile_weight(*w) for w in ws] if stack.tiled else None
         for m in synthetic.M_SWEEP_32B:
-            out["32B"].setdefault(f"M={m}", {})[lin.name] = entry(m, lin, ws)
-        del ws
+            out["32B"].setdefault(f"M={m}", {})[lin.name] = entry(m, lin, ws, wt)
+        del ws, wt
         torch.cuda.empty_cache()
     return out
 
