@@ -8,8 +8,8 @@ programmatic dependent launch, in both of its forms --
   next linear's quantiser overwrites the codes the previous layer's GEMM of
   that shape read, which is safe only through the launches' ordering);
 * ``chain``: all linears as one nvfp4_linear_chain call (the tensor-core
-  kernel, the library's choice, at M up to 32, with the weights repacked
-  tile-major or as packed row-major; the CUDA-core stream by request at
+  kernel, the library's choice, at M up to 32, on the row-major packed
+  weights or on a tile-major repack; the CUDA-core stream by request at
   M <= 2).
 The step is replayed twice after its outputs are poisoned; then every
 layer's tensor scales and codes are compared bit for bit with the oracle's
@@ -52,7 +52,7 @@ CASES = [("launches", 1, False, "auto"), ("launches", 8, False, "auto"),
          ("launches", 1, True, "auto"), ("launches", 8, True, "auto"),
          ("chain", 1, False, "auto"), ("chain", 2, False, "auto"), ("chain", 1, True, "auto"),
          ("chain", 8, False, "auto"), ("chain", 8, True, "auto"), ("chain", 32, False, "auto"),
-         ("chain", 1, False, "rowmajor"), ("chain", 8, False, "rowmajor"),
+         ("chain", 1, False, "tiled"), ("chain", 8, True, "tiled"),
          ("chain", 1, False, "gemv"), ("chain", 2, True, "gemv")]
 
 
@@ -62,7 +62,7 @@ def test_decode_step_graph_matches_oracle(nv, mode, m, bf16, engine):
     stack = bench.DecodeStack(nv, torch, m=m, layers=LAYERS, pdl=True, fused=False, bf16=bf16,
                               mode=mode,
                               chain_kernel=nv.KERNEL_GEMV if engine == "gemv" else nv.KERNEL_AUTO,
-                              tiled=engine != "rowmajor")
+                              tiled=engine == "tiled")
     g = stack.capture(stack.step)
     stack.y_flat.fill_(float("nan"))
     for l in range(LAYERS):
