@@ -185,16 +185,24 @@ __host__ __device__ constexpr uint32_t instr_desc(int nmma)
     return (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 }
 
-// 16 bytes of a weight row's block scales (one stage).  Asking L2 for the
-// surrounding 256 bytes (NVFP4_TC_SCALE_L2_256=1) measured slower on the
-// decode step (M = 8: 0.725 against 0.691 ms), so it is off.
-#ifndef NVFP4_TC_SCALE_L2_256
-#define NVFP4_TC_SCALE_L2_256 0
+// 16 bytes of a weight row's block scales (one stage); the next stage's 16
+// share its 32-byte sector.  NVFP4_TC_SCALE_L2 asks L2 to fetch the
+// surrounding 64, 128 or 256 bytes with the same access (0: no hint).
+#ifndef NVFP4_TC_SCALE_L2
+#define NVFP4_TC_SCALE_L2 0
 #endif
 __device__ __forceinline__ uint4 ld_nc_u4(const void* p)
 {
     uint4 v;
-#if NVFP4_TC_SCALE_L2_256
+#if NVFP4_TC_SCALE_L2 == 64
+    asm volatile("ld.global.nc.L1::no_allocate.L2::64B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#elif NVFP4_TC_SCALE_L2 == 128
+    asm volatile("ld.global.nc.L1::no_allocate.L2::128B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#elif NVFP4_TC_SCALE_L2 == 256
     asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
