@@ -188,8 +188,11 @@ __host__ __device__ constexpr uint32_t instr_desc(int nmma)
 // 16 bytes of a weight row's block scales (one stage); the next stage's 16
 // share its 32-byte sector.  NVFP4_TC_SCALE_L2 asks L2 to fetch the
 // surrounding 64, 128 or 256 bytes with the same access (0: no hint).
+// Measured on the 8B decode step (GEMM launch, two runs each): no hint
+// 662 / 695 us at M = 1 / 8, 64 bytes 661 / 662 us, 128 bytes no change,
+// 256 bytes slower at M = 8; 64 it is.
 #ifndef NVFP4_TC_SCALE_L2
-#define NVFP4_TC_SCALE_L2 0
+#define NVFP4_TC_SCALE_L2 64
 #endif
 __device__ __forceinline__ uint4 ld_nc_u4(const void* p)
 {
