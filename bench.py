@@ -427,15 +427,17 @@ def make_weights(nv, torch, lin, std, copies, seed):
     return out
 
 
-def time_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5):
+def time_linear(nv, torch, weights, lin, m, kernel, pdl, reps, seed=5, workspace=True):
     """µs per call of one linear shape at this M: a graph of len(weights) GEMMs
-    over distinct weight copies (larger than L2 together), replayed."""
+    over distinct weight copies (larger than L2 together), replayed; with the
+    workspace the kernel asks for, or (``workspace=False``) none, as the plain
+    boundary call offers."""
     xa = synthetic.activations(m, lin.k, seed=seed)
     xd = torch.from_numpy(xa).cuda()
     xg = nv.global_scale(xd)
     xq, xs = nv.quantize_act(xd, xg)
     y = torch.empty((m, lin.n), device="cuda")
-    wsp = nv.workspace(m, lin.n, lin.k, kernel)
+    wsp = nv.workspace(m, lin.n, lin.k, kernel) if workspace else False
 
     def calls():
         for wq, ws, wg in weights:
@@ -539,8 +541,9 @@ def sweep(nv, torch, stack, peaks, args) -> dict:
     """µs/call and GB/s of every linear shape for every M of the sweep: each
     kernel that takes the shape as a lone call (graph of calls over rotating
     weight copies, L2-cold), the library's choice marked, and the shape
-    inside a multi-linear call on the tensor cores (``tc_chain``).  Beyond
-    M = 8 (tensor-core kernel only) the 8B shapes at M = 12..32."""
+    inside a multi-linear call on the tensor cores (``tc_chain``); at
+    M = 2..8 also the plain boundary call without a workspace (``plain``).
+    Beyond M = 8 (tensor-core kernel only) the 8B shapes at M = 12..32."""
     kernels = {"gemv": nv.KERNEL_GEMV, "mma": nv.KERNEL_MMA, "tma": nv.KERNEL_TMA,
                "splitk": nv.KERNEL_SPLITK, "tc": nv.KERNEL_TC, "generic": nv.KERNEL_GENERIC}
     out = {"8B": {}, "32B": {}, "C1": tiny_latency(nv, torch, kernels, stack.pdl)}
@@ -558,6 +561,13 @@ def sweep(nv, torch, stack, peaks, args) -> dict:
                 continue
             ent[name] = time_linear(nv, torch, ws, lin, m, kid, stack.pdl, reps)
         ent["frac_of_peak"] = round(ent[ent["kernel"]]["GBps"] / peaks["hbm_gbs"], 4)
+        if 2 <= m <= 8:
+            # the plain boundary call: the library's choice with no workspace
+            # (the split-K kernel's cluster form where K takes several chunks)
+            plain = nv.gemm_select(m, lin.n, lin.k)
+            ent["plain"] = time_linear(nv, torch, ws, lin, m, nv.KERNEL_AUTO, stack.pdl, reps,
+                                       workspace=False)
+            ent["plain"]["kernel"] = nv.KERNEL_NAMES.get(plain)
         # inside a chain: the tile-major weights the decode step uses
         ent["tc_chain"] = time_chain_linear(nv, torch, wt if wt is not None else ws, lin, m,
                                             nv.KERNEL_TC, stack.pdl, reps)

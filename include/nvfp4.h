@@ -114,14 +114,12 @@ int nvfp4_quantize_act(const float* x, int64_t m, int64_t k, const float* x_g,
  *   y               device float[m][n], overwritten
  * m must be 0..8 (NVFP4_ERR_UNSUPPORTED otherwise).  One kernel launch:
  * the CUDA-core stream at M = 1, the split-K tensor-core kernel at M >= 2
- * when its plan needs no workspace, else a TMA-fed or cluster tensor-core
- * kernel.  The result does not depend on the launch order of CTAs: every
- * reduction has a fixed order.  Without a workspace the split-K kernel only
- * takes K <= 4096 at M >= 3, and the fallbacks measured 1.6-3.6x slower on
- * the longer-K decode layers (8B down, 32B o / down): callers that want the
- * fast path offer a workspace (nvfp4_gemm_smallm_ws), use the allocation-free
- * nvfp4_gemm_smallm_static, or batch independent linears into one
- * nvfp4_linear_chain call.
+ * (with no workspace, its cluster form sums the K chunks of a tile through
+ * distributed shared memory), and, for shapes it cannot take (K not a
+ * multiple of 256, or no plan of at most 8 chunks), a TMA-fed or cluster
+ * tensor-core kernel.  The result does not depend on the launch order of
+ * CTAs: every reduction has a fixed order.  Independent linears run faster
+ * as one nvfp4_linear_chain call.
  */
 int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
                       const uint8_t* w_q, const uint8_t* w_s, const float* w_g,
@@ -147,11 +145,15 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       FP32 accumulation) in which every warp streams its own
  *                       (16 rows x K-chunk) work items with no CTA barrier:
  *                       M <= 8, K a multiple of 256.  K is cut into chunks of
- *                       at most 4096 elements; when there is more than one,
- *                       the partial tiles are combined in a workspace (the
- *                       _ws entry points), so without one it takes only
- *                       K <= 4096.  The last partial of a tile to arrive sums
- *                       them in chunk order: results do not depend on timing.
+ *                       at most 32768 / M elements; when there is more than
+ *                       one, the partial tiles are combined in a workspace
+ *                       (the _ws entry points; the last partial of a tile to
+ *                       arrive sums them) or, when the call offers less
+ *                       workspace than the plan wants, the chunks of a tile
+ *                       set run as one thread-block cluster of at most 8 CTAs
+ *                       that sums the partials through distributed shared
+ *                       memory.  Either way the sum is in chunk order:
+ *                       results do not depend on timing.
  * NVFP4_KERNEL_TC      the fifth-generation tensor-core kernel: tcgen05.mma
  *                       kind::mxf4nvf4 (the FP4 codes and UE4M3 block scales
  *                       go to the tensor core as they are; FP32 accumulation
@@ -265,8 +267,9 @@ int nvfp4_gemm_select_ws(int64_t m, int64_t n, int64_t k, uint32_t options,
  * size (the counter region's extent depends on the size only).  Calls that
  * can run at the same time (on other streams) must use separate workspaces:
  * two overlapping calls on one workspace race.  A smaller workspace than this
- * size restricts the kernel's plan to one that fits (NVFP4_ERR_UNSUPPORTED
- * when none does; 0 bytes: plans that need none).
+ * size restricts the kernel's plan to one that fits it or needs none (for
+ * the split-K kernel: one chunk, or the cluster form; NVFP4_ERR_UNSUPPORTED
+ * when none does).
  */
 int64_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, uint32_t options);
 

@@ -225,7 +225,10 @@ def nvfp4_workspace(m: int, n: int, k: int, kernel: int = KERNEL_AUTO,
 
 def _ws_args(workspace, m, n, k, kernel, device):
     """(pointer, bytes, keep-alive) of the workspace for one call; a zeroed
-    one is made for this call when none is given and the GEMM wants one."""
+    one is made for this call when none is given and the GEMM wants one;
+    ``False`` offers none (as the plain boundary call does)."""
+    if workspace is False:
+        return None, 0, None
     if workspace is None:
         workspace = nvfp4_workspace(m, n, k, kernel, device) if m and n and k else None
     if workspace is None:
@@ -245,7 +248,9 @@ def nvfp4_gemm_smallm(xq, xs, xg, wq, ws, wg, out: torch.Tensor | None = None,
     KERNEL_TMA, KERNEL_SPLITK); ``pdl`` lets the launch overlap the previous
     kernel (weights must not be written by it); ``workspace`` (from
     ``nvfp4_workspace``) is made per call when the kernel needs one and none
-    is given.  The output is float32, or bfloat16 (``out_dtype`` or the dtype
+    is given (``False``: none is offered, so the split-K kernel takes one
+    chunk or its cluster form).  The output is float32, or bfloat16
+    (``out_dtype`` or the dtype
     of ``out``): the float32 result rounded to nearest even."""
     tiled = isinstance(wq, TiledWeight)
     if tiled:                        # gemm_smallm(xq, xs, xg, TiledWeight, ...)

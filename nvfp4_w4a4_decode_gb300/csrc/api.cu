@@ -117,12 +117,13 @@ int select_kernel(int64_t m, int64_t n, int64_t k, uint32_t options, bool ptrs_o
     switch (req) {
     case NVFP4_KERNEL_AUTO:
         // measured on GB300 over the 8B / 32B decode shapes: at M >= 2 the
-        // split-K tensor-core kernel when the call offers the workspace its
-        // plan wants; the CUDA-core stream at M = 1 (and at M = 2 without a
-        // workspace); otherwise the TMA-fed tensor-core kernel when K fits
-        // one CTA, else the register-streaming one
+        // split-K tensor-core kernel (through the workspace its plan wants
+        // when the call offers it, else in its cluster form); the CUDA-core
+        // stream at M = 1; for shapes no split-K plan takes, the TMA-fed
+        // tensor-core kernel when K fits one CTA, else the register-streaming
+        // one
         if (m >= 2 && nvfp4::splitk_shape_ok(m, k) && ptrs_ok_fast &&
-            ws_bytes >= nvfp4::splitk_workspace_bytes(m, n, k))
+            nvfp4::splitk_plan_ok(m, n, k, ws_bytes))
             return (int)NVFP4_KERNEL_SPLITK;
         if (gemv_ok)
             return (int)NVFP4_KERNEL_GEMV;

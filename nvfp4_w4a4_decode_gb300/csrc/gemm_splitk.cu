@@ -14,9 +14,10 @@
 // inside an MMA is free: each lane takes the bytes that make its loads whole
 // 32-byte sectors.
 //
-// Work layout.  K is cut into chunks of kc elements (a multiple of 256, at
-// most 32768 / M).  CTA (c, y) of the (nchunks, Cy) grid -- one 16-warp CTA
-// per SM -- owns chunk c.  Its warps form groups of grp warps (1, 2, 4, 8 or
+// Work layout.  K is cut into nch chunks of whole 256-element sub-items, as
+// equal as they can be: the first r = (K / 256) % nch chunks one sub-item
+// longer than the others (at most kc elements, kc <= 32768 / M).  CTA (c, y)
+// of the (nch, Cy) grid -- one 16-warp CTA per SM -- owns chunk c.  Its warps form groups of grp warps (1, 2, 4, 8 or
 // 16); group gi owns the tiles (16 weight rows) y * ngrp + gi + j * Cy * ngrp,
 // and warp r of the group takes the sub-items (256 elements of K) r, r + grp,
 // ... of each tile's chunk.  After the prologue a warp streams its sub-items
@@ -30,8 +31,15 @@
 //   * stores the partial in the workspace and counts it in; the warp that
 //     stores a tile's last partial sums all of them in chunk order (so the
 //     result does not depend on which warp finishes last), writes Y and
-//     resets the tile's counter to zero for the next call.
-// There is no CTA-wide barrier after the prologue and no wait on another CTA.
+//     resets the tile's counter to zero for the next call; or
+//   * (cluster form: where the planner finds it cheaper, and for calls
+//     without the workspace a split needs) keeps the partial in its own
+//     shared memory: the nch CTAs of one tile set form a thread-block
+//     cluster (chunk = rank), and after the stream every warp of the cluster
+//     sums some of the set's tiles, reading the nch partials through
+//     distributed shared memory in chunk order, and writes Y.
+// There is no CTA-wide barrier after the prologue and no wait on another CTA
+// (the cluster form's two cluster barriers at the end aside).
 // Per sub-item, lane (g, t) = (lane / 4, lane % 4) copies of rows g and g + 8
 // the code bytes [16t, 16t + 16) and [64 + 16t, 64 + 16t + 16) of the row's
 // 128 (so one copy instruction covers two whole sectors per row) and uses the
@@ -39,6 +47,8 @@
 // The activations of the chunk are decoded once per CTA, scaled, into shared
 // memory in fragment order (one conflict-free 16-byte read per two MMAs), for
 // the M real columns only.
+#include <cooperative_groups.h>
+
 #include <mutex>
 #include <unordered_map>
 
@@ -51,9 +61,15 @@ namespace nvfp4 {
 
 namespace {
 
+namespace cg = cooperative_groups;
+
 // Planner allowances, in sub-items of streaming: a shared-memory reduction
 // per tile when warps share it, a workspace round trip per tile (fence and
-// counter) and the last partial's extra round trips at the end of a launch.
+// counter) and the last partial's extra round trips at the end of a launch;
+// the cluster form's end (two cluster barriers, which wait for the slowest of
+// the cluster's CTAs, and nch partial reads per tile) as a base plus a part
+// per chunk (fitted to lone-call times of the 8B / 32B decode shapes at
+// M = 2, 4, 8 over every chunk count in both forms).
 #ifndef NVFP4_SPLITK_COST_GROUP
 #define NVFP4_SPLITK_COST_GROUP 0.5
 #endif
@@ -62,6 +78,12 @@ namespace {
 #endif
 #ifndef NVFP4_SPLITK_COST_TAIL
 #define NVFP4_SPLITK_COST_TAIL 3.0
+#endif
+#ifndef NVFP4_SPLITK_COST_CLUSTER
+#define NVFP4_SPLITK_COST_CLUSTER 1.0
+#endif
+#ifndef NVFP4_SPLITK_COST_CLUSTER_CHUNK
+#define NVFP4_SPLITK_COST_CLUSTER_CHUNK 0.5
 #endif
 #ifndef NVFP4_SPLITK_STAGES
 #define NVFP4_SPLITK_STAGES 3
@@ -74,6 +96,7 @@ constexpr size_t kRingSmem = (size_t)kWarps * kStages * kSlotBytes;
 constexpr size_t kFragSmem = 64 * 1024;  // activation fragments: 2 M bytes per K element
 constexpr size_t kGroupSmem = 2 * kWarps * 32 * 16;  // partial tiles of the warp groups
 constexpr size_t kMaxSmem = kRingSmem + kFragSmem + kGroupSmem;
+constexpr int kMaxClusterChunks = 8;  // portable cluster size
 
 // Longest chunk whose fragments (M rows, 2 bytes per element) fit.
 __host__ __device__ constexpr int64_t max_chunk(int64_t m)
@@ -94,8 +117,11 @@ struct SplitkParams {
     int m;
     int64_t n;
     int64_t k;
-    int kc;   // chunk length
-    int grp;  // warps that share a tile (1, 2, 4 or 8), splitting its chunk
+    int kc;     // longest chunk, elements (sizes the fragment area)
+    int sub_q;  // sub-items of a short chunk
+    int sub_r;  // chunks (the first ones) one sub-item longer
+    int grp;    // warps that share a tile (1, 2, 4 or 8), splitting its chunk
+    int maxj;  // cluster form: partial slots per warp group (its most tiles)
 };
 
 // One sub-item of a lane, read from its ring slot: 16 + 16 code bytes of rows
@@ -134,12 +160,13 @@ __device__ __forceinline__ void cp_async_wait_oldest()
     asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
 }
 
-template <bool PDL>
+template <bool PDL, bool CLUSTER>
 __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkParams prm)
 {
     // [kWarps][kStages] sub-item slots of the warps' copy rings, then
     // [kc / 256][8 words][4 M lanes] activation fragments, then (grp > 1)
-    // [2][kWarps][32 lanes] float4 partial tiles of the warp groups
+    // [2][kWarps][32 lanes] float4 partial tiles of the warp groups, then
+    // (cluster form) [kWarps / grp][maxj][32 lanes] float4 chunk partials
     extern __shared__ __align__(16) unsigned char smem[];
     if constexpr (PDL)
         asm volatile("griddepcontrol.launch_dependents;");
@@ -148,8 +175,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
     const int g = lane >> 2, t = lane & 3;
     const int chunk = blockIdx.x, nch = gridDim.x;
     const int64_t n = prm.n, kh = prm.k / 2, kb = prm.k / 16;
-    const int nsub = prm.kc / kSub;
-    const int64_t k0 = (int64_t)chunk * prm.kc;
+    const int nsub = prm.sub_q + (chunk < prm.sub_r ? 1 : 0);
+    const int64_t k0 = ((int64_t)chunk * prm.sub_q + (chunk < prm.sub_r ? chunk : prm.sub_r)) * kSub;
     const int64_t ntiles = (n + 15) / 16;
     // warp group gi (grp warps) owns tiles; warp rank r of the group takes
     // sub-items r, r + grp, ... of each tile's chunk
@@ -319,9 +346,36 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
         }
     };
 
-    // End of a tile's chunk (one warp per tile): Y directly, or the workspace
+    // Y of a tile's 16 rows x M columns from this lane's four sums.
+    auto store_tile = [&](int64_t tile, float v0, float v1, float v2, float v3) {
+        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+        const int c0 = 2 * t, c1 = c0 + 1;
+        if (c0 < M) {
+            if (r0 < n)
+                store_y(prm.y, c0 * n + r0, v0 * gxw);
+            if (r1 < n)
+                store_y(prm.y, c0 * n + r1, v2 * gxw);
+        }
+        if (c1 < M) {
+            if (r0 < n)
+                store_y(prm.y, c1 * n + r0, v1 * gxw);
+            if (r1 < n)
+                store_y(prm.y, c1 * n + r1, v3 * gxw);
+        }
+    };
+
+    // cluster form: the chunk partial of the group's jt-th tile
+    float4* pstore = reinterpret_cast<float4*>(
+        smem + kRingSmem + (size_t)prm.kc * 2 * M + (G > 1 ? kGroupSmem : 0));
+
+    // End of a tile's chunk (one warp per tile, the group's jt-th): Y
+    // directly, or the cluster form's shared-memory slot, or the workspace
     // and, for the last partial of the tile, the fixed-order sum.
-    auto flush = [&](int64_t tile, float v0, float v1, float v2, float v3) {
+    auto flush = [&](int64_t tile, int jt, float v0, float v1, float v2, float v3) {
+        if (CLUSTER && nch > 1) {
+            pstore[(gi * prm.maxj + jt) * 32 + lane] = make_float4(v0, v1, v2, v3);
+            return;
+        }
         if (nch > 1) {
             float4* slot = prm.part + tile * nch * 32 + lane;
             __stcg(slot + chunk * 32, make_float4(v0, v1, v2, v3));
@@ -361,20 +415,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
             if (lane == 0)
                 atomicExch(prm.count + tile, 0u);
         }
-        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-        const int c0 = 2 * t, c1 = c0 + 1;
-        if (c0 < M) {
-            if (r0 < n)
-                store_y(prm.y, c0 * n + r0, v0 * gxw);
-            if (r1 < n)
-                store_y(prm.y, c0 * n + r1, v2 * gxw);
-        }
-        if (c1 < M) {
-            if (r0 < n)
-                store_y(prm.y, c1 * n + r0, v1 * gxw);
-            if (r1 < n)
-                store_y(prm.y, c1 * n + r1, v3 * gxw);
-        }
+        store_tile(tile, v0, v1, v2, v3);
     };
 
     // End of a warp's share of a tile: with warp groups, the group's warps
@@ -382,7 +423,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
     // per tile suffices) and rank 0 adds them in rank order and flushes.
     float4* red = reinterpret_cast<float4*>(xfrag + nsub * 8 * LW);  // after the fragments
     int rbuf = 0;
-    auto tile_end = [&](int64_t tile) {
+    auto tile_end = [&](int64_t tile, int jt) {
         float v0 = acc[0] + acc2[0], v1 = acc[1] + acc2[1], v2 = acc[2] + acc2[2],
               v3 = acc[3] + acc2[3];
         if (G > 1) {
@@ -405,12 +446,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
             v2 = s4.z;
             v3 = s4.w;
         }
-        flush(tile, v0, v1, v2, v3);
+        flush(tile, jt, v0, v1, v2, v3);
     };
 
     int64_t c_tile = tile0;
     const int b_first = r * 8 * LW, b_step = G * 8 * LW;  // fragment offsets of this warp's sub-items
-    int c_b = b_first, c_left = per_tile;
+    int c_b = b_first, c_left = per_tile, c_j = 0;
     const uint4* xb = xfrag + lane_b;
     for (int e = 0; e < nitems; e += kStages) {
 #pragma unroll
@@ -426,7 +467,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
                 issue(s);
                 c_b += b_step;
                 if (--c_left == 0) {
-                    tile_end(c_tile);
+                    tile_end(c_tile, c_j++);
                     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
                     acc2[0] = acc2[1] = acc2[2] = acc2[3] = 0.f;
                     c_b = b_first;
@@ -438,11 +479,48 @@ __global__ void __launch_bounds__(kWarps * 32, 1) splitk_kernel(const SplitkPara
     }
     // no copy is left in flight: every group issued past the last sub-item
     // was empty
+
+    if constexpr (CLUSTER) {
+        if (nch > 1) {
+            // Every partial of the cluster's tile set is in its CTA's shared
+            // memory once all CTAs pass the barrier.  Slot e = (group, j) of
+            // every rank holds that rank's chunk of the same tile; the
+            // cluster's warps take the slots in turn and sum the nch partials
+            // from zero in chunk order, as the workspace form does.
+            cg::cluster_group cl = cg::this_cluster();
+            cl.sync();
+            const int nent = ngrp * prm.maxj;
+            for (int e = chunk * kWarps + warp; e < nent; e += nch * kWarps) {
+                const int egi = e / prm.maxj, ej = e - egi * prm.maxj;
+                const int64_t tile = (int64_t)blockIdx.y * ngrp + egi + (int64_t)ej * tstride;
+                if (tile >= ntiles)
+                    continue;
+                float4 p[kMaxClusterChunks];
+#pragma unroll
+                for (int c = 0; c < kMaxClusterChunks; ++c)
+                    if (c < nch)
+                        p[c] = *cl.map_shared_rank(pstore + e * 32 + lane, (unsigned)c);
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < kMaxClusterChunks; ++c)
+                    if (c < nch) {
+                        s4.x += p[c].x;
+                        s4.y += p[c].y;
+                        s4.z += p[c].z;
+                        s4.w += p[c].w;
+                    }
+                store_tile(tile, s4.x, s4.y, s4.z, s4.w);
+            }
+            cl.sync();  // no CTA leaves while another may still read its partials
+        }
+    }
 }
 
 struct SplitkPlan {
-    int kc, nch, grp;
+    int kc, nch, grp;  // longest chunk (elements), chunks, warps per tile
     int64_t cy;
+    bool cluster;  // partials summed through distributed shared memory
+    int maxj;      // cluster form: partial slots per warp group
 };
 
 // Workspace layout: the per-tile counters in the first counter_region(size)
@@ -484,80 +562,186 @@ int64_t resident_ctas()
     const int dev = current_device();
     const size_t smem = kMaxSmem;
     int per_sm = 0;
-    if (ensure_smem_limit(splitk_kernel<false>, smem, dev) != cudaSuccess ||
-        ensure_smem_limit(splitk_kernel<true>, smem, dev) != cudaSuccess ||
-        cached_occupancy(splitk_kernel<true>, kWarps * 32, smem, 0, dev, &per_sm) != cudaSuccess ||
+    if (ensure_smem_limit(splitk_kernel<false, false>, smem, dev) != cudaSuccess ||
+        ensure_smem_limit(splitk_kernel<true, false>, smem, dev) != cudaSuccess ||
+        cached_occupancy(splitk_kernel<true, false>, kWarps * 32, smem, 0, dev, &per_sm) !=
+            cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     return (int64_t)device_sm_count(dev) * per_sm;
 }
 
-// Chunk length kc: multiples of 256 that divide K, at most 4096; warps per
-// tile grp: 1, 2, 4 or 8, dividing kc / 256.  The cost of a candidate, in
-// units of one sub-item of streaming, is the busiest warp's sub-items plus
-// allowances for what adds latency: a shared-memory reduction per tile when
-// warps share it, and, when partials go through the workspace, one per tile
-// and the last partial's round trips at the end.  The cheapest wins; ties go
-// to the earlier candidate (longer chunk, fewer warps per tile).  Candidates
-// whose workspace exceeds `ws_limit` are skipped (0: single-chunk plans only).
-bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* out)
+// Largest dynamic shared memory a CTA may opt into on the current device.
+size_t smem_optin()
+{
+    const int dev = current_device();
+    static std::mutex mu;
+    static std::unordered_map<int, size_t> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end())
+        return it->second;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        v = 0;
+    cache[dev] = (size_t)v;
+    return (size_t)v;
+}
+
+// Clusters of `nch` CTAs of the cluster form that run at once on the current
+// device (0 if the query fails).  Every CTA needs more than half an SM's
+// shared memory, so one per SM whatever its exact size: the query is made at
+// the opt-in maximum.
+int64_t resident_clusters(int nch)
+{
+    const int dev = current_device();
+    const size_t smem = smem_optin();
+    int v = 0;
+    if (smem < kMaxSmem ||
+        ensure_smem_limit(splitk_kernel<false, true>, smem, dev) != cudaSuccess ||
+        ensure_smem_limit(splitk_kernel<true, true>, smem, dev) != cudaSuccess ||
+        cached_occupancy(splitk_kernel<true, true>, kWarps * 32, smem, nch, dev, &v) !=
+            cudaSuccess)
+        return 0;
+    return v;
+}
+
+size_t plan_smem(const SplitkPlan& p, int64_t m)
+{
+    return kRingSmem + (size_t)p.kc * 2 * m + (p.grp > 1 ? kGroupSmem : 0) +
+           (p.cluster ? (size_t)(kWarps / p.grp) * p.maxj * 32 * sizeof(float4) : 0);
+}
+
+// Candidates: nch chunks (the longest at most max_chunk(m)); warps per tile
+// grp 1, 2, 4, 8 or 16 dividing every chunk's sub-items (so grp = 1 when the
+// chunks are unequal); each split candidate in its workspace form (when its
+// partials fit `ws_limit`) and in its cluster form (nch <= 8, the partials
+// within the shared memory).  The cost of a candidate, in units of one
+// sub-item of streaming, is the busiest warp's sub-items plus allowances for
+// what adds latency: a shared-memory reduction per tile when warps share it;
+// in the workspace form one round trip per tile and the last partial's at the
+// end; in the cluster form its end-of-launch reduction.  The cheapest wins;
+// ties go to the earlier candidate (fewer chunks, fewer warps per tile, the
+// workspace form).
+bool search_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* out)
 {
     if (m < 1 || m > 8 || n < 1 || n >= (int64_t(1) << 27) || k < kSub || k % kSub != 0)
         return false;
     const int64_t slots = resident_ctas();
     const int64_t ntiles = (n + 15) / 16;
+    const int64_t subs = k / kSub, len_max = max_chunk(m) / kSub;
     bool found = false;
     double best = 0.0;
-    const int64_t kc_max = max_chunk(m);
-    for (int64_t kc = (k < kc_max ? k : kc_max) / kSub * kSub; kc >= kSub; kc -= kSub) {
-        if (k % kc)
-            continue;
-        const int64_t nch = k / kc, nsub = kc / kSub;
-        if (nch > 65535 || !plan_fits(ntiles, (int)nch, ws_limit))
-            continue;
-        for (int grp = 1; grp <= kWarps; grp *= 2) {
-            if (nsub % grp)
+    for (int64_t nch = (subs + len_max - 1) / len_max; nch <= subs && nch <= 65535; ++nch) {
+        const int64_t q = subs / nch, r = subs % nch, len = q + (r ? 1 : 0);
+        for (int form = 0; form < 2; ++form) {
+            const bool cluster = form == 1;
+            if (nch == 1 && cluster)
                 continue;
-            const int64_t ngrp = kWarps / grp;
-            int64_t cy = slots / nch;
-            const int64_t cy_max = (ntiles + ngrp - 1) / ngrp;
-            if (cy > cy_max)
-                cy = cy_max;
-            if (cy < 1)
-                cy = 1;
-            const int64_t per_group = (ntiles + cy * ngrp - 1) / (cy * ngrp);
-            const double per_tile = (double)(nsub / grp) +
-                                    (grp > 1 ? NVFP4_SPLITK_COST_GROUP : 0.0) +
-                                    (nch > 1 ? NVFP4_SPLITK_COST_FLUSH : 0.0);
-            const double cost =
-                (double)per_group * per_tile + (nch > 1 ? NVFP4_SPLITK_COST_TAIL : 0.0);
-            if (!found || cost < best) {
-                found = true;
-                best = cost;
-                out->kc = (int)kc;
-                out->nch = (int)nch;
-                out->grp = grp;
-                out->cy = cy;
+            if (!cluster && !plan_fits(ntiles, (int)nch, ws_limit))
+                continue;
+            if (cluster && nch > kMaxClusterChunks)
+                continue;
+            const int64_t clusters = cluster ? resident_clusters((int)nch) : 0;
+            if (cluster && clusters < 1)
+                continue;
+            for (int grp = 1; grp <= kWarps; grp *= 2) {
+                if (q % grp || (r && grp > 1))
+                    continue;
+                const int64_t ngrp = kWarps / grp;
+                int64_t cy = cluster ? clusters : slots / nch;
+                const int64_t cy_max = (ntiles + ngrp - 1) / ngrp;
+                if (cy > cy_max)
+                    cy = cy_max;
+                if (cy < 1)
+                    cy = 1;
+                const int64_t per_group = (ntiles + cy * ngrp - 1) / (cy * ngrp);
+                const SplitkPlan cand = {(int)(len * kSub), (int)nch, grp, cy, cluster,
+                                         (int)per_group};
+                if (cluster && plan_smem(cand, m) > smem_optin())
+                    continue;
+                const double per_tile = (double)(len / grp) +
+                                        (grp > 1 ? NVFP4_SPLITK_COST_GROUP : 0.0) +
+                                        (nch > 1 && !cluster ? NVFP4_SPLITK_COST_FLUSH : 0.0);
+                const double tail =
+                    nch <= 1  ? 0.0
+                    : cluster ? NVFP4_SPLITK_COST_CLUSTER + NVFP4_SPLITK_COST_CLUSTER_CHUNK * nch
+                              : NVFP4_SPLITK_COST_TAIL;
+                const double cost = (double)per_group * per_tile + tail;
+                if (!found || cost < best) {
+                    found = true;
+                    best = cost;
+                    *out = cand;
+                }
             }
         }
     }
     return found;
 }
 
-template <bool PDL>
+// The plan of a call offering `ws_limit` bytes of workspace: the best of the
+// candidates it can run (with any workspace at least the size that
+// splitk_workspace_bytes reports, the best of all).  Cached per device,
+// shape and offer, so that a launch plans once.
+struct PlanKey {
+    int dev;
+    int64_t m, n, k, ws;
+    bool operator==(const PlanKey& o) const
+    {
+        return dev == o.dev && m == o.m && n == o.n && k == o.k && ws == o.ws;
+    }
+};
+struct PlanKeyHash {
+    size_t operator()(const PlanKey& p) const
+    {
+        size_t h = (size_t)p.dev;
+        h = h * 1000003u ^ (size_t)p.m;
+        h = h * 1000003u ^ (size_t)p.n;
+        h = h * 1000003u ^ (size_t)p.k;
+        h = h * 1000003u ^ (size_t)p.ws;
+        return h;
+    }
+};
+
+bool plan_splitk(int64_t m, int64_t n, int64_t k, int64_t ws_limit, SplitkPlan* out)
+{
+    static std::mutex mu;
+    static std::unordered_map<PlanKey, std::pair<bool, SplitkPlan>, PlanKeyHash> cache;
+    const PlanKey key{current_device(), m, n, k, ws_limit};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *out = it->second.second;
+            return it->second.first;
+        }
+    }
+    SplitkPlan p = {};
+    const bool ok = search_splitk(m, n, k, ws_limit, &p);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() > 4096)
+        cache.clear();
+    cache[key] = {ok, p};
+    *out = p;
+    return ok;
+}
+
+template <bool PDL, bool CLUSTER>
 cudaError_t launch_t(const GemmArgs& a, const SplitkPlan& p, void* workspace, int64_t ws_bytes)
 {
-    const size_t smem = kRingSmem + (size_t)p.kc * 2 * a.m + (p.grp > 1 ? kGroupSmem : 0);
-    auto kern = splitk_kernel<PDL>;
+    const size_t smem = plan_smem(p, a.m);
+    auto kern = splitk_kernel<PDL, CLUSTER>;
     const int dev = current_device();
     if (smem > 48 * 1024) {
-        const cudaError_t e = ensure_smem_limit(kern, kMaxSmem, dev);
+        const cudaError_t e = ensure_smem_limit(kern, CLUSTER ? smem_optin() : kMaxSmem, dev);
         if (e != cudaSuccess)
             return e;
     }
-    SplitkParams prm = {a.xq, a.xs, a.xg, a.wq, a.ws, a.wg, a.y, nullptr, nullptr,
-                        a.m,  a.n,  a.k,  p.kc, p.grp};
-    if (p.nch > 1) {
+    const int subs = (int)(a.k / kSub);
+    SplitkParams prm = {a.xq, a.xs, a.xg, a.wq, a.ws, a.wg, a.y, nullptr,
+                        nullptr, a.m, a.n, a.k, p.kc, subs / p.nch, subs % p.nch,
+                        p.grp, p.maxj};
+    if (p.nch > 1 && !CLUSTER) {
         unsigned char* base = static_cast<unsigned char*>(workspace);
         prm.count = reinterpret_cast<unsigned*>(base);
         prm.part = reinterpret_cast<float4*>(base + counter_region(ws_bytes));
@@ -567,11 +751,22 @@ cudaError_t launch_t(const GemmArgs& a, const SplitkPlan& p, void* workspace, in
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = PDL ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (CLUSTER) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.nch;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (PDL) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
@@ -624,7 +819,8 @@ int64_t splitk_static_scratch_bytes()
 bool splitk_static_fits(int64_t m, int64_t n, int64_t k)
 {
     SplitkPlan p;
-    return plan_splitk(m, n, k, INT64_MAX, &p) && plan_fits((n + 15) / 16, p.nch, kStaticScratchBytes);
+    return plan_splitk(m, n, k, INT64_MAX, &p) &&
+           (p.cluster || plan_fits((n + 15) / 16, p.nch, kStaticScratchBytes));
 }
 
 cudaError_t launch_gemm_splitk_static(const GemmArgs& a, bool pdl)
@@ -653,7 +849,7 @@ bool splitk_plan_ok(int64_t m, int64_t n, int64_t k, int64_t workspace_bytes)
 int64_t splitk_workspace_bytes(int64_t m, int64_t n, int64_t k)
 {
     SplitkPlan p;
-    if (!plan_splitk(m, n, k, INT64_MAX, &p))
+    if (!plan_splitk(m, n, k, INT64_MAX, &p) || p.cluster)
         return 0;
     return workspace_bytes_for((n + 15) / 16, p.nch);
 }
@@ -664,8 +860,10 @@ cudaError_t launch_gemm_splitk(const GemmArgs& a, bool pdl, void* workspace,
     SplitkPlan p;
     if (!plan_splitk(a.m, a.n, a.k, workspace ? workspace_bytes : 0, &p))
         return cudaErrorInvalidValue;
-    return pdl ? launch_t<true>(a, p, workspace, workspace_bytes)
-               : launch_t<false>(a, p, workspace, workspace_bytes);
+    if (p.cluster)
+        return pdl ? launch_t<true, true>(a, p, nullptr, 0) : launch_t<false, true>(a, p, nullptr, 0);
+    return pdl ? launch_t<true, false>(a, p, workspace, workspace_bytes)
+               : launch_t<false, false>(a, p, workspace, workspace_bytes);
 }
 
 }  // namespace nvfp4

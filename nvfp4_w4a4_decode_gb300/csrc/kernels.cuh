@@ -79,7 +79,9 @@ cudaError_t launch_gemm_tma(const GemmArgs& a, bool pdl, bool test_timeout);
 // splitk_workspace_bytes() bytes (the plan with an unlimited workspace); it
 // must be zero before its first use and every completed launch leaves it
 // zero.  With a smaller workspace (or none) the plan is restricted to what
-// fits; splitk_plan_ok() says whether one does.
+// fits or needs none (one chunk, or the cluster form: at most 8 chunks as one
+// thread-block cluster, partials summed through distributed shared memory);
+// splitk_plan_ok() says whether one exists.
 bool splitk_shape_ok(int64_t m, int64_t k);
 bool splitk_plan_ok(int64_t m, int64_t n, int64_t k, int64_t workspace_bytes);
 int64_t splitk_workspace_bytes(int64_t m, int64_t n, int64_t k);

@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from conftest import ROOT
 
@@ -106,11 +107,17 @@ def test_gemm_select_host_only(lib):
     for m in range(1, 9):
         for k in (1024, 2048, 4096, 5120, 8192, 12288, 25600):
             assert nv.gemm_select(m, 100, k, MMA) == MMA, (m, k)
-        assert nv.gemm_select(m, 100, 4096) == (GEMV if m <= 2 else nv.KERNEL_TMA)
-        assert nv.gemm_select(m, 100, 12288) in ((GEMV,) if m <= 2 else (MMA, nv.KERNEL_TMA))
+        # M >= 2: split-K in one chunk (K <= 32768 / M) or, where a device
+        # allows it, in its cluster form; else the TMA-fed or register kernel
+        assert nv.gemm_select(m, 100, 4096) == (GEMV if m == 1 else nv.KERNEL_SPLITK)
+        assert nv.gemm_select(m, 100, 12288) in ((GEMV,) if m == 1 else (nv.KERNEL_SPLITK,) if m == 2
+                                                 else (nv.KERNEL_SPLITK, MMA, nv.KERNEL_TMA))
     assert nv.gemm_select(1, 10, 384, MMA) == -2          # too few 128-ranges
     assert nv.gemm_select(4, 10, 256 * 37, MMA) == -2     # 74 ranges: no split fits
-    assert nv.gemm_select(4, 10, 256 * 37) == GENERIC
+    # 37 sub-items of 256 at M = 4: two unequal chunks, so split-K where a
+    # device runs its cluster form, else the generic kernel
+    assert nv.gemm_select(4, 10, 256 * 37) == (nv.KERNEL_SPLITK if torch.cuda.is_available()
+                                                else GENERIC)
 
 
 def test_ex_options_validated(lib):
@@ -143,7 +150,8 @@ def test_workspace_entry_points_host_only(lib):
     SPLITK = nv.KERNEL_SPLITK
     assert lib.nvfp4_gemm_workspace_size(1, 100, 4096, nv.KERNEL_GEMV) == 0
     assert lib.nvfp4_gemm_workspace_size(8, 6144, 4096, SPLITK) >= 0
-    assert lib.nvfp4_gemm_workspace_size(8, 6144, 12288, SPLITK) > 0    # K > one chunk
+    assert lib.nvfp4_gemm_workspace_size(8, 6144, 12288, SPLITK) >= 0   # workspace or cluster
+    assert lib.nvfp4_gemm_workspace_size(8, 512, 40960, SPLITK) > 0     # > 8 chunks: workspace
     assert lib.nvfp4_gemm_workspace_size(9, 100, 4096, SPLITK) == -2
     assert lib.nvfp4_gemm_workspace_size(1, 100, 40, SPLITK) == -1
     assert lib.nvfp4_gemm_workspace_size(1, 100, 4000, SPLITK) == -2   # K % 256 != 0
@@ -152,11 +160,10 @@ def test_workspace_entry_points_host_only(lib):
         need = lib.nvfp4_gemm_workspace_size(m, n, k, nv.KERNEL_AUTO)
         assert need == lib.nvfp4_gemm_workspace_size(m, n, k, SPLITK)
         assert nv.gemm_select(m, n, k, nv.KERNEL_AUTO, need) == SPLITK     # offered: taken
-        if need:
-            assert nv.gemm_select(m, n, k, nv.KERNEL_AUTO, need - 256) != SPLITK
     assert lib.nvfp4_gemm_workspace_size(1, 6144, 4096, nv.KERNEL_AUTO) == 0   # gemv
     assert nv.gemm_select(1, 6144, 4096, nv.KERNEL_AUTO, 1 << 30) == nv.KERNEL_GEMV
-    assert nv.gemm_select(8, 100, 8192, SPLITK) == -2        # M = 8: K > 4096 needs a workspace
+    if not torch.cuda.is_available():   # M = 8, K > 4096: a workspace or a device's clusters
+        assert nv.gemm_select(8, 100, 8192, SPLITK) == -2
     assert nv.gemm_select(2, 100, 12288, SPLITK) == SPLITK   # M = 2: K up to 16384 in one chunk
     ok = [FAKE] * 7
     g = lib.nvfp4_gemm_smallm_ws
@@ -181,9 +188,10 @@ def test_read_probe_rejects_bad_arguments(lib):
 
 def test_splitk_planner_properties_host_only(lib):
     """For many shapes: the workspace the split-K plan asks for is accepted
-    for that plan; one chunk (no workspace) is possible exactly when K fits
-    one CTA's activation fragments (2 M bytes per element, 64 KB); K not a
-    multiple of 256 and M outside 1..8 are refused."""
+    for that plan; without a workspace and without a device (so without the
+    cluster form) a plan exists exactly when K fits one CTA's activation
+    fragments (2 M bytes per element, 64 KB); K not a multiple of 256 and M
+    outside 1..8 are refused."""
     import random
     rnd = random.Random(5)
     SPLITK = nv.KERNEL_SPLITK
@@ -195,7 +203,8 @@ def test_splitk_planner_properties_host_only(lib):
         assert need >= 0
         assert lib.nvfp4_gemm_select_ws(m, n, k, SPLITK, need) == SPLITK
         one_chunk = k <= (65536 // (2 * m)) // 256 * 256
-        assert (lib.nvfp4_gemm_select_ws(m, n, k, SPLITK, 0) == SPLITK) == one_chunk, (m, n, k)
+        nows = lib.nvfp4_gemm_select_ws(m, n, k, SPLITK, 0) == SPLITK
+        assert nows == one_chunk or (nows and torch.cuda.is_available()), (m, n, k)
         if one_chunk:
             assert need == 0 or need >= 1024 * ((n + 15) // 16)   # 2+ partials of 512 B per tile
     for m, k in ((1, 4000), (9, 4096), (0, 4096)):

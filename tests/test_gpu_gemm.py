@@ -413,34 +413,105 @@ def test_splitk_kernel(nv, m, n, k):
     y2 = nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK, pdl=True, workspace=wsp)
     np.testing.assert_array_equal(host(y2), y)
     if nv.gemm_select(m, n, k, nv.KERNEL_SPLITK) == nv.KERNEL_SPLITK:
-        # without a workspace: K in one chunk, another plan
-        y3 = host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK))
+        # without a workspace: K in one chunk, or the cluster form
+        y3 = host(nv.gemm_smallm(*ops, kernel=nv.KERNEL_SPLITK, workspace=False))
         assert check_rows(y3, oops, n) <= GEMM_TOL
 
 
-def test_splitk_needs_workspace_beyond_one_chunk(nv):
-    m, n, k = 8, 64, 8192
-    assert nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) > 0
-    assert nv.gemm_select(m, n, k, nv.KERNEL_SPLITK) == -2   # no workspace on offer
-    ops, _ = splitk_case(nv, m, n, k, seed=5)
+# Shapes whose K takes several chunks at that M, so that a call without a
+# workspace runs the cluster form (partials summed through distributed shared
+# memory): the 8B down at M = 8, the 32B down at M = 4 and M = 8 (100
+# sub-items of 256: unequal chunks), a ragged N at M = 3, a 4-tile N, a
+# 2500-tile N, M = 2 with K = 32768, M = 7, and 37 sub-items (a prime) at M = 8.
+CLUSTER_SHAPES = [(8, 4096, 12288), (4, 5120, 25600), (8, 5120, 25600), (3, 16 * 37 + 5, 16384),
+                  (8, 64, 8192), (6, 40000, 8192), (2, 2048, 32768), (7, 1000, 10240),
+                  (8, 1000, 256 * 37)]
+
+
+def gemm_raw(nv, ops, m, n, k, options, ws=None, entry="ws"):
+    """One call through the C ABI: nvfp4_gemm_smallm_ws with the given
+    workspace tensor (None: no workspace), or the plain nvfp4_gemm_smallm."""
     lib = nv.library()
-    y = torch.empty((m, n), device="cuda")
-    st = lib.nvfp4_gemm_smallm_ws(*[t.data_ptr() for t in ops[:6]], y.data_ptr(), m, n, k,
-                                  nv.KERNEL_SPLITK, None, 0,
-                                  torch.cuda.current_stream().cuda_stream)
-    assert st == 2
-    small = torch.zeros(64, dtype=torch.uint8, device="cuda")    # too small for any split
-    st = lib.nvfp4_gemm_smallm_ws(*[t.data_ptr() for t in ops[:6]], y.data_ptr(), m, n, k,
-                                  nv.KERNEL_SPLITK, small.data_ptr(), small.numel(),
-                                  torch.cuda.current_stream().cuda_stream)
-    assert st == 2
+    y = torch.full((m, n), float("nan"), device="cuda")
+    ptrs = [t.data_ptr() for t in ops[:6]]
+    st = torch.cuda.current_stream().cuda_stream
+    if entry == "plain":
+        status = lib.nvfp4_gemm_smallm(*ptrs, y.data_ptr(), m, n, k, st)
+    else:
+        status = lib.nvfp4_gemm_smallm_ws(*ptrs, y.data_ptr(), m, n, k, options,
+                                          ws.data_ptr() if ws is not None else None,
+                                          ws.numel() if ws is not None else 0, st)
+    return status, y
+
+
+@pytest.mark.parametrize("m,n,k", CLUSTER_SHAPES)
+def test_splitk_cluster_form_without_workspace(nv, m, n, k):
+    """Without a workspace (or with one too small for any split) the split-K
+    kernel still takes a K of several chunks, in its cluster form: results
+    within the tolerance of the oracle's FP64 sum, the same bits on every
+    call (fixed chunk order), with PDL, with a too-small workspace, and
+    through the plain boundary call, which selects it."""
+    assert m * k * 2 > 65536                      # more than one chunk
+    assert nv.gemm_select(m, n, k, nv.KERNEL_SPLITK) == nv.KERNEL_SPLITK
+    assert nv.gemm_select(m, n, k) == nv.KERNEL_SPLITK
+    ops, oops = splitk_case(nv, m, n, k, seed=3 * m + n + k)
+    SPLITK = nv.KERNEL_SPLITK
+    st, y = gemm_raw(nv, ops, m, n, k, SPLITK)
+    assert st == 0
+    yh = host(y).copy()
+    assert check_rows(yh, oops, n) <= GEMM_TOL
+    st, y2 = gemm_raw(nv, ops, m, n, k, SPLITK | nv.FLAG_PDL)
+    assert st == 0
+    np.testing.assert_array_equal(host(y2), yh)
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")   # too small for any split
+    st, y3 = gemm_raw(nv, ops, m, n, k, SPLITK, ws=small)
+    assert st == 0
+    np.testing.assert_array_equal(host(y3), yh)
+    st, y4 = gemm_raw(nv, ops, m, n, k, 0, entry="plain")
+    assert st == 0
+    np.testing.assert_array_equal(host(y4), yh)
+    # with the workspace the plan asks for (if any): the same plan when that
+    # is a cluster plan, else the workspace form, within the tolerance
+    yw = host(nv.gemm_smallm(*ops, kernel=SPLITK))
+    if nv.gemm_workspace_size(m, n, k, SPLITK) == 0:
+        np.testing.assert_array_equal(yw, yh)
+    assert check_rows(yw, oops, n) <= GEMM_TOL
+    assert nv.device_status() == 0
+
+
+def test_splitk_cluster_form_in_a_graph(nv):
+    """The cluster form replayed from a CUDA graph, twice: same bits as the
+    eager call."""
+    m, n, k = 8, 4096, 12288
+    ops, oops = splitk_case(nv, m, n, k, seed=17)
+    st, y = gemm_raw(nv, ops, m, n, k, nv.KERNEL_SPLITK)
+    assert st == 0
+    ref = host(y).copy()
+    assert check_rows(ref, oops, n) <= GEMM_TOL
+    yg = torch.empty((m, n), device="cuda")
+    lib = nv.library()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            assert lib.nvfp4_gemm_smallm_ws(*[t.data_ptr() for t in ops[:6]], yg.data_ptr(), m,
+                                            n, k, nv.KERNEL_SPLITK | nv.FLAG_PDL, None, 0,
+                                            s.cuda_stream) == 0
+    for _ in range(2):
+        yg.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host(yg), ref)
 
 
 def test_splitk_workspace_shared_across_shapes(nv):
     """One workspace, sized for the largest, serves a sequence of shapes and
     orders (every call leaves its counters at zero); results equal those of
-    fresh workspaces."""
-    shapes = [(8, 6144, 4096), (1, 4096, 12288), (4, 5120, 25600), (8, 6144, 4096)]
+    fresh workspaces.  K = 40960 at M = 8 needs more chunks than one cluster
+    holds, so its partials go through the workspace."""
+    shapes = [(8, 6144, 4096), (8, 512, 40960), (1, 4096, 12288), (4, 5120, 25600),
+              (8, 512, 40960), (8, 6144, 4096)]
+    assert nv.gemm_workspace_size(8, 512, 40960, nv.KERNEL_SPLITK) > 0
     cases = [splitk_case(nv, m, n, k, seed=40 + i)[0] for i, (m, n, k) in enumerate(shapes)]
     size = max(nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) for m, n, k in shapes)
     shared = torch.zeros(size, dtype=torch.uint8, device="cuda")

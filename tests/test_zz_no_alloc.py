@@ -37,9 +37,12 @@ def operands(nv, m, n, k, seed):
 
 
 # a few tiles, the 8B qkv at M = 8, the 8B down at M = 1, the 32B down at
-# M = 4 (K of 1 to 25600 / 256 chunks, whatever the plan picks), and a shape
-# whose plan keeps K in one chunk (the scratch is not touched)
-SHAPES = [(3, 300, 4096), (8, 6144, 4096), (1, 4096, 12288), (4, 5120, 25600), (2, 40000, 1024)]
+# M = 4 (K of 1 to 25600 / 256 chunks, whatever the plan picks), a shape whose
+# plan keeps K in one chunk (the scratch is not touched), and K = 40960 at
+# M = 8 (more chunks than one cluster holds: the partials go through the
+# scratch)
+SHAPES = [(3, 300, 4096), (8, 6144, 4096), (1, 4096, 12288), (4, 5120, 25600), (2, 40000, 1024),
+          (8, 512, 40960)]
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
@@ -80,8 +83,8 @@ def test_static_allocates_no_device_memory(nv):
     """Free device memory (cudaMemGetInfo, which sees every allocation on the
     device, not only torch's) is unchanged by repeated calls once the first
     call has looked up the scratch address; the shape here needs the scratch
-    (its split-K plan cuts K into several chunks)."""
-    m, n, k = 4, 5120, 25600
+    (its split-K plan cuts K into more chunks than one cluster holds)."""
+    m, n, k = 8, 512, 40960
     assert nv.gemm_workspace_size(m, n, k, nv.KERNEL_SPLITK) > 0
     ops, _, _ = operands(nv, m, n, k, seed=11)
     y = torch.empty((m, n), device="cuda")
