@@ -249,9 +249,9 @@ class DecodeStack:
         self.xq = [(torch.empty((m, lin.k // 2), dtype=torch.uint8, device=dev),
                     torch.empty((m, lin.k // 16), dtype=torch.uint8, device=dev)) for lin in self.lins]
         self.chain = None
-        # on request the tensor-core chain streams tile-major weights (an
-        # offline repack of the same bytes; measured 1-2 % slower than the
-        # row-major ones, which are the default)
+        # the tensor-core chain streams tile-major weights (an offline repack
+        # of the same bytes: contiguous 16 KB stages, and at M <= 2 the CUDA-core
+        # stream warps take the last tiles of every linear); row-major on request
         self.tiled = bool(tiled) and self.has_chain and chain_kernel in (0, nv.KERNEL_TC)
         self.wt = None
         if self.tiled:
@@ -615,7 +615,7 @@ def run_ours(args) -> dict:
                         fused=args.fused, kernel=KERNELS[args.kernel](nv), bf16=args.bf16,
                         mode=mode, chain_kernel=KERNELS[args.chain_kernel](nv),
                         chain_workspace=not args.no_chain_workspace,
-                        tiled=args.tile_major_weights)
+                        tiled=not args.row_major_weights)
     step_graph = stack.capture(stack.step)
     if args.profile_step:
         # only the step graph, replayed: a clean launch list for the profiler
@@ -819,8 +819,10 @@ TRAFFIC_SOURCES = {
                     "quantize.cu", "stream_core.cuh"),
     "gemm_chain": ("api.cu", "formats.cuh", "gemm_chain.cu", "kernels.cuh", "launch_cache.cuh",
                    "stream_core.cuh"),
-    "gemm_tc": ("api.cu", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh"),
-    "gemm_tc_tiled": ("api.cu", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh"),
+    "gemm_tc": ("api.cu", "formats.cuh", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh",
+                "stream_core.cuh"),
+    "gemm_tc_tiled": ("api.cu", "formats.cuh", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh",
+                      "stream_core.cuh"),
 }
 
 
@@ -1198,10 +1200,10 @@ def main():
     ap.add_argument("--chain-kernel", default="auto", choices=["auto", "gemv", "tc"],
                     help="engine of the chain step (auto: CUDA-core stream at M <= 2, "
                          "tensor cores above)")
-    ap.add_argument("--tile-major-weights", action="store_true",
-                    help="the tensor-core chain reads the weights repacked tile-major "
-                         "(nvfp4_tile_weight, two bulk copies a stage) instead of the row-major "
-                         "packed ones (TMA with a tensor map)")
+    ap.add_argument("--row-major-weights", action="store_true",
+                    help="the tensor-core chain reads the row-major packed weights (TMA with a "
+                         "tensor map, no stream warps) instead of the tile-major repack "
+                         "(nvfp4_tile_weight: one bulk copy a stage)")
     ap.add_argument("--no-chain-workspace", action="store_true",
                     help="run the tensor-core chain without its workspace (CTA shares end on "
                          "tile boundaries)")

@@ -44,6 +44,7 @@
 #include "../../include/nvfp4.h"
 #include "kernels.cuh"
 #include "launch_cache.cuh"
+#include "stream_core.cuh"
 
 namespace nvfp4 {
 
@@ -73,17 +74,48 @@ constexpr int kL2Ahead = NVFP4_TC_L2_AHEAD;
 #define NVFP4_TC_PREFETCH 6
 #endif
 constexpr int kPrefetch = NVFP4_TC_PREFETCH;
-constexpr int kThreads = 320;              // 10 warps
+constexpr int kThreads = 320;              // 10 warps of the tensor-core roles
+// Stream warps (N = 16 kernel, tile-major weights): CUDA-core warps beside the
+// tensor-core roles that take the last tiles of every linear (a share of them,
+// in per mille of each linear's tiles) when M <= 2, so that the SM's CUDA
+// cores add their stream to the tensor pipe's.  kStreamWarps compute warps
+// (32 rows of a tile each) and one copy warp.
+#ifndef NVFP4_TC_STREAM_WARPS
+#define NVFP4_TC_STREAM_WARPS 4
+#endif
+#ifndef NVFP4_TC_STREAM_PERMILLE
+#define NVFP4_TC_STREAM_PERMILLE 250  // at M = 1
+#endif
+#ifndef NVFP4_TC_STREAM_PERMILLE_M2
+#define NVFP4_TC_STREAM_PERMILLE_M2 0  // at M = 2 (twice the MAC work per byte: measured no gain)
+#endif
+constexpr int kStreamWarps = NVFP4_TC_STREAM_WARPS;
+static_assert(kStreamWarps * 32 == kRows, "a stream warp per 32 rows of a tile");
+template <int NMMA, bool TILED>
+__host__ __device__ constexpr bool has_stream()
+{
+    return NMMA == 16 && TILED;
+}
+template <int NMMA, bool TILED>
+__host__ __device__ constexpr int tc_threads()
+{
+    return has_stream<NMMA, TILED>() ? kThreads + 32 * (kStreamWarps + 1) : kThreads;
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSfa = 64;                       // 16 columns per ring slot
 constexpr uint32_t kColSfb = kColSfa + 16 * kStages;   // 16 columns per ring slot
 static_assert(kColSfb + 16 * kStages <= kTmemCols, "scale slots fit the tensor memory");
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
 constexpr int kSBytes = kRows * 16;        // weight block scales of a stage (tile-major layout)
-// ring: weight codes, activation codes, and (tile-major weights) weight scales
-constexpr size_t smem_bytes(bool tiled)
+constexpr int kCcSlots = 3;                  // the stream warps' ring
+constexpr int kCcBytes = kABytes + kSBytes;  // a slot: a stage's codes, then its scales
+// ring: weight codes and activation codes (the weight scales go through
+// registers), then the stream warps' slots
+template <int NMMA, bool TILED>
+constexpr size_t smem_bytes()
 {
-    return (size_t)kStages * (kABytes + kBBytes + (tiled ? kSBytes : 0)) + 1024;  // + alignment
+    return (size_t)kStages * (kABytes + kBBytes) +
+           (has_stream<NMMA, TILED>() ? (size_t)kCcSlots * kCcBytes : 0) + 1024;  // + alignment
 }
 
 struct TcItem {
@@ -96,7 +128,7 @@ struct TcItem {
     void* y;
     int32_t n, k;
     int32_t s0;  // first stage of this linear in the launch's stage list
-    int32_t pad;
+    int32_t ttiles;  // leading tiles on the tensor cores (the rows past them: stream warps)
 };
 static_assert(sizeof(TcItem) == 72, "TcItem layout");
 
@@ -249,7 +281,7 @@ __device__ __forceinline__ void cursor_at(Cursor& c, const TcParams& p, int32_t 
     c.item = item_of_stage(p, g);
     const TcItem& it = p.item[c.item];
     c.nst = it.k / kStageK;
-    c.tiles = (it.n + kRows - 1) / kRows;
+    c.tiles = it.ttiles;
     const int32_t local = g - it.s0;
     c.tile = local / c.nst;
     c.st = local - c.tile * c.nst;
@@ -262,7 +294,7 @@ __device__ __forceinline__ void cursor_next_tile(Cursor& c, const TcParams& p)
         ++c.item;
         c.tile = 0;
         c.nst = p.item[c.item].k / kStageK;
-        c.tiles = (p.item[c.item].n + kRows - 1) / kRows;
+        c.tiles = p.item[c.item].ttiles;
     }
 }
 
@@ -302,7 +334,9 @@ __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cu
     const int32_t kb = it.k / 16, kh = it.k / 2;
     const int64_t row = (int64_t)c.tile * kRows + r;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (!TILED)  // tile-major scales arrive with the stage's bulk copy
+    if constexpr (TILED)  // the stage's 2 KB block, row r at 16 r (rows past n are zero)
+        a.sa = ld_nc_u4(it.ws + ((size_t)c.tile * c.nst + c.st) * kSBytes + r * 16);
+    else
         a.sa = row < it.n ? ld_nc_u4(it.ws + row * kb + c.st * 16) : z;
     a.sb = lane < p.m ? __ldg(reinterpret_cast<const uint4*>(it.xs + lane * kb + c.st * 16)) : z;
     a.b0 = u < p.m * 8
@@ -316,12 +350,181 @@ __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cu
                    : z;
 }
 
+// ---- stream warps: whole tiles on the CUDA cores --------------------------------
+// The last tiles of every linear (tile-major weights, M <= 2) go to the stream
+// warps: CTA b takes whole tiles, a contiguous range of them cut near an equal
+// share of their stages.  One lane copies each stage's 16 KB of codes and
+// 2 KB of scales (two contiguous blocks) into a ring of kCcSlots shared-memory
+// slots; stream warp w owns rows 32 w .. 32 w + 31 of the tile, a row per
+// lane, and per stage runs the CUDA-core MAC of the single-linear stream (exact
+// E2M1 block sums in packed FP16, one FP32 FMA per 16-block with the scale
+// product) over the row's 256 elements against the activation chunks (the
+// same for every lane: broadcast loads).  The lane sums its row in stage
+// order and writes Y at the tile's end: no partial leaves the CTA.
+// Stages of the stream warps' tiles before `g`'s tile boundary: the first
+// boundary at or after stage `target` of their list (items in order, tiles
+// ttiles.. of each).
+__device__ int64_t cc_boundary(const TcParams& p, int64_t target)
+{
+    int64_t s = 0;
+    for (int i = 0; i < p.count_items; ++i) {
+        const TcItem& it = p.item[i];
+        const int32_t nst = it.k / kStageK;
+        const int64_t len = ((int64_t)(it.n + kRows - 1) / kRows - it.ttiles) * nst;
+        if (target <= s)
+            return s;
+        if (target < s + len)
+            return s + (target - s + nst - 1) / nst * nst;
+        s += len;
+    }
+    return s;
+}
+
+struct CcCursor {
+    int item;
+    int32_t tile, st, nst, tiles;  // tile index within the linear; tiles of the linear
+};
+
+__device__ void cc_cursor_at(CcCursor& c, const TcParams& p, int64_t g)
+{
+    int64_t s = 0;
+    for (int i = 0; i < p.count_items; ++i) {
+        const TcItem& it = p.item[i];
+        const int32_t nst = it.k / kStageK, tiles = (it.n + kRows - 1) / kRows;
+        const int64_t len = (int64_t)(tiles - it.ttiles) * nst;
+        if (g < s + len) {
+            c.item = i;
+            c.nst = nst;
+            c.tiles = tiles;
+            c.tile = it.ttiles + (int32_t)((g - s) / nst);
+            c.st = (int32_t)((g - s) % nst);
+            return;
+        }
+        s += len;
+    }
+    c.item = p.count_items;  // past the end
+}
+
+__device__ __forceinline__ void cc_next(CcCursor& c, const TcParams& p)
+{
+    if (++c.st < c.nst)
+        return;
+    c.st = 0;
+    if (++c.tile < c.tiles)
+        return;
+    // the next linear that has stream tiles
+    for (++c.item; c.item < p.count_items; ++c.item) {
+        const TcItem& it = p.item[c.item];
+        c.nst = it.k / kStageK;
+        c.tiles = (it.n + kRows - 1) / kRows;
+        c.tile = it.ttiles;
+        if (c.tile < c.tiles)
+            return;
+    }
+}
+
+// The copy lane: stage i of the CTA's stream range into slot i % kCcSlots,
+// once the compute warps have freed it; then every copy in flight lands.
+__device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t sC0,
+                           uint64_t* full, uint64_t* empty, volatile int* abort_flag)
+{
+    CcCursor c;
+    cc_cursor_at(c, p, lo);
+    int64_t issued = 0;
+    for (int64_t i = 0; i < cnt; ++i) {
+        const int slot = (int)(i % kCcSlots);
+        if (i >= kCcSlots &&
+            !mbar_wait(smem_u32(&empty[slot]), (uint32_t)(((i / kCcSlots) - 1) & 1), abort_flag,
+                       p.status))
+            break;
+        const TcItem& it = p.item[c.item];
+        const size_t blk = (size_t)c.tile * c.nst + c.st;
+        const uint32_t fb = smem_u32(&full[slot]), dst = sC0 + (uint32_t)(slot * kCcBytes);
+        mbar_expect_tx(fb, kCcBytes);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(dst), "l"(it.wq + blk * kABytes), "r"(kABytes), "r"(fb)
+            : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(dst + kABytes), "l"(it.ws + blk * kSBytes), "r"(kSBytes), "r"(fb)
+            : "memory");
+        issued = i + 1;
+        cc_next(c, p);
+    }
+    for (int64_t i = issued > kCcSlots ? issued - kCcSlots : 0; i < issued; ++i) {
+        const long long t0 = clock64();
+        while (!mbar_test(smem_u32(&full[i % kCcSlots]), (uint32_t)((i / kCcSlots) & 1)) &&
+               clock64() - t0 < kWaitBudget) {
+        }
+    }
+}
+
+// A compute warp: row 32 w + lane of every tile of the CTA's stream range.
+template <int M>
+__device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uint8_t* sC,
+                           uint64_t* full, uint64_t* empty, volatile int* abort_flag, int w,
+                           int lane)
+{
+    const int rr = 32 * w + lane;  // row within the tile
+    CcCursor c;
+    cc_cursor_at(c, p, lo);
+    float acc[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+        acc[m] = 0.f;
+    for (int64_t i = 0; i < cnt; ++i) {
+        const int slot = (int)(i % kCcSlots);
+        // warp-uniform: every lane leaves together
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[slot]), (uint32_t)((i / kCcSlots) & 1),
+                                               abort_flag, p.status)))
+            break;
+        const TcItem& it = p.item[c.item];
+        const int64_t kh = it.k / 2, kb = it.k / 16;
+        const uint8_t* sl = sC + slot * kCcBytes;
+        // the row's 16 scale bytes of this stage: bytes 2c, 2c + 1 for chunk c
+        const uint4 sc4 = *reinterpret_cast<const uint4*>(sl + kABytes + rr * 16);
+        const uint32_t scw[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            // chunk ch of the row in the swizzled image: 16 bytes at rr * 128 + ((ch ^ (rr & 7)) << 4)
+            const uint4 cw = *reinterpret_cast<const uint4*>(sl + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            uint32_t wh[16];
+            decode_w_chunk(cw, wh);
+            const float2 sw = e4m3x2_to_float2((ch & 1) ? scw[ch >> 1] >> 16 : scw[ch >> 1] & 0xFFFFu);
+            XChunk<M> x;
+            load_x_chunk<M>(x, it.xq, it.xs, kh, kb, c.st * 8 + ch);
+            float t[M];
+            mac_chunk<M>(wh, sw, x, t);
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+                acc[m] += t[m];
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&empty[slot]));
+        if (c.st == c.nst - 1) {
+            const int64_t row = (int64_t)c.tile * kRows + rr;
+            const float gxw = __fmul_rn(__ldg(it.xg), __ldg(it.wg));
+            const OutY y = {it.y, p.y_bf16};
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                if (row < it.n)
+                    store_y(y, (int64_t)m * it.n + row, acc[m] * gxw);
+                acc[m] = 0.f;
+            }
+        }
+        cc_next(c, p);
+    }
+}
+
 template <int NMMA, bool TILED>
-__global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_constant__ TcParams p)
+__global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages], aux_bar[kStages], empty_bar[kStages];
     __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar;
+    __shared__ __align__(8) uint64_t cfull_bar[kCcSlots], cempty_bar[kCcSlots];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ int epi_fail_s;  // an epilogue warp gave up: every epilogue warp stops
@@ -333,9 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     const int32_t total = hi - lo;  // this CTA's stages
     // tile-aligned (1024-byte) ring: weight slots, then activation slots
     const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes, sS0 = sB0 + kStages * kBBytes;
+    const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes, sC0 = sB0 + kStages * kBBytes;
     uint8_t* sB_gen = smem_raw + (sB0 - smem_u32(smem_raw));
-    const uint8_t* sS_gen = smem_raw + (sS0 - smem_u32(smem_raw));
+    const uint8_t* sC_gen = smem_raw + (sC0 - smem_u32(smem_raw));
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -353,6 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
             mbar_init(smem_u32(&acce_bar[b]), 4);
         }
         mbar_init(smem_u32(&drain_bar), 1);
+        for (int s = 0; s < kCcSlots; ++s) {
+            mbar_init(smem_u32(&cfull_bar[s]), 1);
+            mbar_init(smem_u32(&cempty_bar[s]), kStreamWarps);
+        }
         abort_s = 0;
         epi_fail_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -407,19 +614,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     break;
                 const uint32_t fb = smem_u32(&full_bar[slot]);
                 if constexpr (TILED) {
-                    // tile-major layout: the stage's codes (already in the swizzled
-                    // shared-memory image) and its scales are two contiguous blocks
+                    // tile-major layout: the stage's codes, already in the swizzled
+                    // shared-memory image, are one contiguous 16 KB block (its
+                    // scales go through the scale warps' registers)
                     const size_t blk = (size_t)c.tile * c.nst + c.st;
-                    mbar_expect_tx(fb, kABytes + kSBytes);
+                    mbar_expect_tx(fb, kABytes);
                     asm volatile(
                         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
                         "[%0], [%1], %2, [%3];" ::"r"(sA0 + slot * kABytes),
                         "l"(p.item[c.item].wq + blk * kABytes), "r"(kABytes), "r"(fb)
-                        : "memory");
-                    asm volatile(
-                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-                        "[%0], [%1], %2, [%3];" ::"r"(sS0 + slot * kSBytes),
-                        "l"(p.item[c.item].ws + blk * kSBytes), "r"(kSBytes), "r"(fb)
                         : "memory");
                 } else {
                     mbar_expect_tx(fb, kABytes);
@@ -542,17 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    uint4 sa4 = ring[d].sa;
-                    if constexpr (TILED) {
-                        // the weight scales come with the stage's bulk copy
-                        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full_bar[slot]),
-                                                               (i / kStages) & 1, abort_flag,
-                                                               p.status))) {
-                            ok = false;
-                            break;
-                        }
-                        sa4 = *reinterpret_cast<const uint4*>(sS_gen + slot * kSBytes + r * 16);
-                    }
+                    const uint4 sa4 = ring[d].sa;
                     asm volatile("tcgen05.fence::after_thread_sync;");
                     const uint32_t sa[4] = {sa4.x, sa4.y, sa4.z, sa4.w};
                     const uint32_t sb[4] = {ring[d].sb.x, ring[d].sb.y, ring[d].sb.z, ring[d].sb.w};
@@ -587,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 }
             }
         }
-    } else {
+    } else if (warp < kThreads / 32) {
         // ---- epilogue ----------------------------------------------------------------------
         asm volatile("griddepcontrol.wait;" ::: "memory");  // Y may still be read before
         const int q = warp & 3;
@@ -718,6 +911,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 cursor_next_tile(c, p);
             }
         }
+    } else if constexpr (has_stream<NMMA, TILED>()) {
+        // ---- stream warps: the last tiles of every linear on the CUDA cores -------------
+        const int w = warp - kThreads / 32;  // compute warps 0 .. kStreamWarps - 1, then the copy warp
+        const int64_t all = cc_boundary(p, INT64_MAX);
+        const int64_t lo = cc_boundary(p, all * blockIdx.x / gridDim.x);
+        const int64_t cnt = cc_boundary(p, all * (blockIdx.x + 1) / gridDim.x) - lo;
+        if (cnt > 0 && p.m <= 2) {
+            if (w == kStreamWarps) {
+                if (lane == 0)
+                    cc_produce(p, lo, cnt, sC0, cfull_bar, cempty_bar, abort_flag);
+            } else {
+                asm volatile("griddepcontrol.wait;" ::: "memory");  // x_q / x_s come from the producer
+                if (p.m == 1)
+                    cc_consume<1>(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
+                else
+                    cc_consume<2>(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
+            }
+        }
     }
 
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -769,13 +980,13 @@ cudaError_t launch_tc_t(TcParams& prm, int grid, cudaStream_t stream, bool pdl)
 {
     auto kern = tc_chain_kernel<NMMA, TILED>;
     const int dev = current_device();
-    const size_t smem = smem_bytes(TILED);
+    const size_t smem = smem_bytes<NMMA, TILED>();
     cudaError_t e = ensure_smem_limit(kern, smem, dev);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(tc_threads<NMMA, TILED>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -815,6 +1026,10 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
     cudaError_t e = device_status_address(&prm.status);
     if (e != cudaSuccess)
         return e;
+    // at M <= 2, with tile-major weights, the stream warps take the last tiles
+    // of every linear (a share of its tiles, at least one left to the tensor
+    // cores)
+    const bool rows_to_stream = m <= 2 && tiled;
     int64_t stages = 0;
     for (int i = 0; i < count; ++i) {
         const ChainLinear& L = items[i];
@@ -831,8 +1046,16 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
         it.n = (int32_t)L.n;
         it.k = (int32_t)L.k;
         it.s0 = (int32_t)stages;
-        it.pad = 0;
-        stages += ((L.n + kRows - 1) / kRows) * (L.k / kStageK);
+        const int64_t tiles = (L.n + kRows - 1) / kRows;
+        int64_t cc = 0;
+        if (rows_to_stream) {
+            cc = (tiles * (m == 1 ? NVFP4_TC_STREAM_PERMILLE : NVFP4_TC_STREAM_PERMILLE_M2) + 500) /
+                 1000;
+            if (cc > tiles - 1)
+                cc = tiles - 1;
+        }
+        it.ttiles = (int32_t)(tiles - cc);
+        stages += (tiles - cc) * (L.k / kStageK);
     }
     if (stages >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;
@@ -855,7 +1078,7 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
         // ranges on tile boundaries, each near an equal share of the stages
         int64_t tiles = 0;
         for (int i = 0; i < count; ++i)
-            tiles += (items[i].n + kRows - 1) / kRows;
+            tiles += prm.item[i].ttiles;
         if (grid > tiles)
             grid = (int)tiles;
         int i = 0;
