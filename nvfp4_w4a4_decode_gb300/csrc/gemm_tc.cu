@@ -84,10 +84,10 @@ constexpr int kThreads = 320;              // 10 warps of the tensor-core roles
 #define NVFP4_TC_STREAM_WARPS 4
 #endif
 #ifndef NVFP4_TC_STREAM_PERMILLE
-#define NVFP4_TC_STREAM_PERMILLE 250  // at M = 1
+#define NVFP4_TC_STREAM_PERMILLE 310  // at M = 1
 #endif
 #ifndef NVFP4_TC_STREAM_PERMILLE_M2
-#define NVFP4_TC_STREAM_PERMILLE_M2 0  // at M = 2 (twice the MAC work per byte: measured no gain)
+#define NVFP4_TC_STREAM_PERMILLE_M2 175  // at M = 2 (twice the MAC work per weight byte)
 #endif
 constexpr int kStreamWarps = NVFP4_TC_STREAM_WARPS;
 static_assert(kStreamWarps * 32 == kRows, "a stream warp per 32 rows of a tile");
@@ -108,7 +108,11 @@ static_assert(kColSfb + 16 * kStages <= kTmemCols, "scale slots fit the tensor m
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
 constexpr int kSBytes = kRows * 16;        // weight block scales of a stage (tile-major layout)
 constexpr int kCcSlots = 3;                  // the stream warps' ring
-constexpr int kCcBytes = kABytes + kSBytes;  // a slot: a stage's codes, then its scales
+// a slot: a stage's codes, its scales, then the stage's activation chunks
+// decoded once (M <= 2 rows x 8 chunks of 16 f16x2 words and 2 scales, 80 bytes each)
+constexpr int kCcXOff = kABytes + kSBytes;
+constexpr int kCcXChunk = 80;
+constexpr int kCcBytes = kCcXOff + 2 * 8 * kCcXChunk;
 // ring: weight codes and activation codes (the weight scales go through
 // registers), then the stream warps' slots
 template <int NMMA, bool TILED>
@@ -423,39 +427,71 @@ __device__ __forceinline__ void cc_next(CcCursor& c, const TcParams& p)
     }
 }
 
-// The copy lane: stage i of the CTA's stream range into slot i % kCcSlots,
-// once the compute warps have freed it; then every copy in flight lands.
-__device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t sC0,
-                           uint64_t* full, uint64_t* empty, volatile int* abort_flag)
+// The copy warp: stage i of the CTA's stream range into slot i % kCcSlots,
+// once the compute warps have freed it (one lane issues the two bulk copies,
+// 8 M lanes decode the stage's activation chunks into the slot); then every
+// copy in flight lands.
+__device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t sC0, uint8_t* sC,
+                           uint64_t* full, uint64_t* empty, volatile int* abort_flag, int lane)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // x_q / x_s come from the producer
     CcCursor c;
     cc_cursor_at(c, p, lo);
     int64_t issued = 0;
     for (int64_t i = 0; i < cnt; ++i) {
         const int slot = (int)(i % kCcSlots);
         if (i >= kCcSlots &&
-            !mbar_wait(smem_u32(&empty[slot]), (uint32_t)(((i / kCcSlots) - 1) & 1), abort_flag,
-                       p.status))
+            !__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&empty[slot]),
+                                               (uint32_t)(((i / kCcSlots) - 1) & 1), abort_flag,
+                                               p.status)))
             break;
         const TcItem& it = p.item[c.item];
-        const size_t blk = (size_t)c.tile * c.nst + c.st;
         const uint32_t fb = smem_u32(&full[slot]), dst = sC0 + (uint32_t)(slot * kCcBytes);
-        mbar_expect_tx(fb, kCcBytes);
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-            ::"r"(dst), "l"(it.wq + blk * kABytes), "r"(kABytes), "r"(fb)
-            : "memory");
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-            ::"r"(dst + kABytes), "l"(it.ws + blk * kSBytes), "r"(kSBytes), "r"(fb)
-            : "memory");
+        if (lane == 0) {
+            const size_t blk = (size_t)c.tile * c.nst + c.st;
+            mbar_expect_tx(fb, kABytes + kSBytes);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(dst), "l"(it.wq + blk * kABytes), "r"(kABytes), "r"(fb)
+                : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(dst + kABytes), "l"(it.ws + blk * kSBytes), "r"(kSBytes), "r"(fb)
+                : "memory");
+        }
+        if (lane < 8 * p.m) {
+            // chunk ch of activation row m: the K elements 256 st + 32 ch ..
+            const int m = lane >> 3, ch = lane & 7;
+            const int64_t cidx = (int64_t)c.st * 8 + ch;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(it.xq + m * (int64_t)(it.k / 2) + 16 * cidx));
+            const uint32_t sc2 = __ldg(reinterpret_cast<const unsigned short*>(
+                it.xs + m * (int64_t)(it.k / 16) + 2 * cidx));
+            uint32_t h[16];
+            e2m1x8_to_f16(v.x, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
+            e2m1x8_to_f16(v.y, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
+            e2m1x8_to_f16(v.z, *reinterpret_cast<uint32_t(*)[4]>(&h[8]));
+            e2m1x8_to_f16(v.w, *reinterpret_cast<uint32_t(*)[4]>(&h[12]));
+            const float2 f = e4m3x2_to_float2(sc2);
+            uint4* xo = reinterpret_cast<uint4*>(sC + slot * kCcBytes + kCcXOff + (m * 8 + ch) * kCcXChunk);
+            xo[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            xo[1] = make_uint4(h[4], h[5], h[6], h[7]);
+            xo[2] = make_uint4(h[8], h[9], h[10], h[11]);
+            xo[3] = make_uint4(h[12], h[13], h[14], h[15]);
+            xo[4] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), 0u, 0u);
+            __threadfence_block();
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(fb);  // the decoded activations are in the slot
         issued = i + 1;
         cc_next(c, p);
     }
-    for (int64_t i = issued > kCcSlots ? issued - kCcSlots : 0; i < issued; ++i) {
-        const long long t0 = clock64();
-        while (!mbar_test(smem_u32(&full[i % kCcSlots]), (uint32_t)((i / kCcSlots) & 1)) &&
-               clock64() - t0 < kWaitBudget) {
+    if (lane == 0) {
+        for (int64_t i = issued > kCcSlots ? issued - kCcSlots : 0; i < issued; ++i) {
+            const long long t0 = clock64();
+            while (!mbar_test(smem_u32(&full[i % kCcSlots]), (uint32_t)((i / kCcSlots) & 1)) &&
+                   clock64() - t0 < kWaitBudget) {
+            }
         }
     }
 }
@@ -480,7 +516,6 @@ __device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uin
                                                abort_flag, p.status)))
             break;
         const TcItem& it = p.item[c.item];
-        const int64_t kh = it.k / 2, kb = it.k / 16;
         const uint8_t* sl = sC + slot * kCcBytes;
         // the row's 16 scale bytes of this stage: bytes 2c, 2c + 1 for chunk c
         const uint4 sc4 = *reinterpret_cast<const uint4*>(sl + kABytes + rr * 16);
@@ -492,8 +527,22 @@ __device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uin
             uint32_t wh[16];
             decode_w_chunk(cw, wh);
             const float2 sw = e4m3x2_to_float2((ch & 1) ? scw[ch >> 1] >> 16 : scw[ch >> 1] & 0xFFFFu);
-            XChunk<M> x;
-            load_x_chunk<M>(x, it.xq, it.xs, kh, kb, c.st * 8 + ch);
+            XChunk<M> x;  // the copy warp's decode of the chunk (the same for every lane)
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const uint4* xi = reinterpret_cast<const uint4*>(sl + kCcXOff + (m * 8 + ch) * kCcXChunk);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = xi[q];
+                    x.h[m][4 * q] = v.x;
+                    x.h[m][4 * q + 1] = v.y;
+                    x.h[m][4 * q + 2] = v.z;
+                    x.h[m][4 * q + 3] = v.w;
+                }
+                const uint4 sv = xi[4];
+                x.s[m][0] = __uint_as_float(sv.x);
+                x.s[m][1] = __uint_as_float(sv.y);
+            }
             float t[M];
             mac_chunk<M>(wh, sw, x, t);
 #pragma unroll
@@ -557,7 +606,7 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
         }
         mbar_init(smem_u32(&drain_bar), 1);
         for (int s = 0; s < kCcSlots; ++s) {
-            mbar_init(smem_u32(&cfull_bar[s]), 1);
+            mbar_init(smem_u32(&cfull_bar[s]), 2);  // the copies, and the decoded activations
             mbar_init(smem_u32(&cempty_bar[s]), kStreamWarps);
         }
         abort_s = 0;
@@ -919,8 +968,8 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
         const int64_t cnt = cc_boundary(p, all * (blockIdx.x + 1) / gridDim.x) - lo;
         if (cnt > 0 && p.m <= 2) {
             if (w == kStreamWarps) {
-                if (lane == 0)
-                    cc_produce(p, lo, cnt, sC0, cfull_bar, cempty_bar, abort_flag);
+                cc_produce(p, lo, cnt, sC0, smem_raw + (sC0 - smem_u32(smem_raw)), cfull_bar,
+                           cempty_bar, abort_flag, lane);
             } else {
                 asm volatile("griddepcontrol.wait;" ::: "memory");  // x_q / x_s come from the producer
                 if (p.m == 1)
