@@ -820,9 +820,9 @@ TRAFFIC_SOURCES = {
     "gemm_chain": ("api.cu", "formats.cuh", "gemm_chain.cu", "kernels.cuh", "launch_cache.cuh",
                    "stream_core.cuh"),
     "gemm_tc": ("api.cu", "formats.cuh", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh",
-                "stream_core.cuh"),
+                "mma_frag.cuh"),
     "gemm_tc_tiled": ("api.cu", "formats.cuh", "gemm_tc.cu", "kernels.cuh", "launch_cache.cuh",
-                      "stream_core.cuh"),
+                      "mma_frag.cuh"),
 }
 
 

@@ -166,13 +166,13 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       128 rows x K per work unit, so a lone call occupies
  *                       ceil(N / 128) SMs.  Results are exact sums up to FP32
  *                       rounding in the tensor core's own order.  With
- *                       tile-major weights (NVFP4_FLAG_W_TILED) at M = 1 and
- *                       2 the last 31 % (M = 1) or 17.5 % (M = 2) of every
+ *                       tile-major weights (NVFP4_FLAG_W_TILED) at M <= 8
+ *                       the last 20 % (M = 8) to 32 % (M = 1) of every
  *                       linear's tiles (rounded, at least one tile left to the
- *                       tensor cores) run on the CUDA cores of the same SMs
- *                       instead (exact 16-element block sums, FP32
- *                       accumulation in row order), so that both stream at
- *                       once.
+ *                       tcgen05 MMAs) run on other warps of the same SMs
+ *                       through mma.sync instead (f16 operands with the block
+ *                       scales folded in exactly, FP32 accumulation), so that
+ *                       two weight streams run at once.
  *   The GEMV, MMA and SPLITK kernels need x_q/w_q 32-byte and x_s/w_s 4-byte
  *   aligned, the TMA and TC kernels all four 32-byte aligned; a request a
  *   kernel cannot take returns NVFP4_ERR_UNSUPPORTED.
@@ -194,8 +194,8 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       row-major: every pipeline stage of the tensor-core
  *                       kernel is then one contiguous 16 KB bulk copy of
  *                       codes instead of 128 strided pieces, its scales one
- *                       contiguous 2 KB block, and at M <= 2 part of the
- *                       tiles go to the CUDA cores (see NVFP4_KERNEL_TC).
+ *                       contiguous 2 KB block, and at M <= 8 part of the
+ *                       tiles go to a second stream (see NVFP4_KERNEL_TC).
  * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
  *                       while the previous kernel on the stream is still
  *                       running and waits for it before it touches anything

@@ -44,7 +44,8 @@
 #include "../../include/nvfp4.h"
 #include "kernels.cuh"
 #include "launch_cache.cuh"
-#include "stream_core.cuh"
+#include "formats.cuh"
+#include "mma_frag.cuh"
 
 namespace nvfp4 {
 
@@ -57,7 +58,12 @@ constexpr int kStages = NVFP4_TC_STAGES;   // shared-memory ring
 constexpr int kRows = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kStageK = 256;               // K elements per stage (128 code bytes a row)
 constexpr int kABytes = kRows * 128;       // weight codes of a stage
-constexpr int kBBytes = 32 * 128;          // activation codes of a stage (N <= 32)
+// activation codes of a stage: N rows of 128 bytes (two or four 1024-byte swizzle atoms)
+template <int NMMA>
+__host__ __device__ constexpr int b_bytes()
+{
+    return NMMA * 128;
+}
 // Stages ahead of the copy being issued whose weights the producer asks L2
 // to fetch (0: none), to keep DRAM reads in flight beyond what the
 // shared-memory ring holds.  Measured on the 8B decode step it only adds
@@ -75,20 +81,45 @@ constexpr int kL2Ahead = NVFP4_TC_L2_AHEAD;
 #endif
 constexpr int kPrefetch = NVFP4_TC_PREFETCH;
 constexpr int kThreads = 320;              // 10 warps of the tensor-core roles
-// Stream warps (N = 16 kernel, tile-major weights): CUDA-core warps beside the
+// Stream warps (N = 16 kernel, tile-major weights): warps beside the
 // tensor-core roles that take the last tiles of every linear (a share of them,
-// in per mille of each linear's tiles) when M <= 2, so that the SM's CUDA
-// cores add their stream to the tensor pipe's.  kStreamWarps compute warps
-// (32 rows of a tile each) and one copy warp.
+// in per mille of each linear's tiles, per M) when M <= 8, so that the SM adds
+// a second weight stream to the tcgen05 one.  kStreamWarps compute warps (32
+// rows of a tile each) and one copy warp.
 #ifndef NVFP4_TC_STREAM_WARPS
 #define NVFP4_TC_STREAM_WARPS 4
 #endif
-#ifndef NVFP4_TC_STREAM_PERMILLE
-#define NVFP4_TC_STREAM_PERMILLE 310  // at M = 1
+// share of every linear's tiles (per mille, rounded) the stream warps take, per M
+// (measured optima on the 8B decode step, set a little below where the
+// stream warps would become the slower part)
+#ifndef NVFP4_TC_STREAM_SHARE_1
+#define NVFP4_TC_STREAM_SHARE_1 320
 #endif
-#ifndef NVFP4_TC_STREAM_PERMILLE_M2
-#define NVFP4_TC_STREAM_PERMILLE_M2 175  // at M = 2 (twice the MAC work per weight byte)
+#ifndef NVFP4_TC_STREAM_SHARE_2
+#define NVFP4_TC_STREAM_SHARE_2 270
 #endif
+#ifndef NVFP4_TC_STREAM_SHARE_3
+#define NVFP4_TC_STREAM_SHARE_3 250
+#endif
+#ifndef NVFP4_TC_STREAM_SHARE_4
+#define NVFP4_TC_STREAM_SHARE_4 245
+#endif
+#ifndef NVFP4_TC_STREAM_SHARE_5
+#define NVFP4_TC_STREAM_SHARE_5 220
+#endif
+#ifndef NVFP4_TC_STREAM_SHARE_6
+#define NVFP4_TC_STREAM_SHARE_6 225
+#endif
+#ifndef NVFP4_TC_STREAM_SHARE_7
+#define NVFP4_TC_STREAM_SHARE_7 212
+#endif
+#ifndef NVFP4_TC_STREAM_SHARE_8
+#define NVFP4_TC_STREAM_SHARE_8 200
+#endif
+constexpr int kStreamShare[9] = {0, NVFP4_TC_STREAM_SHARE_1, NVFP4_TC_STREAM_SHARE_2,
+                                    NVFP4_TC_STREAM_SHARE_3, NVFP4_TC_STREAM_SHARE_4,
+                                    NVFP4_TC_STREAM_SHARE_5, NVFP4_TC_STREAM_SHARE_6,
+                                    NVFP4_TC_STREAM_SHARE_7, NVFP4_TC_STREAM_SHARE_8};
 constexpr int kStreamWarps = NVFP4_TC_STREAM_WARPS;
 static_assert(kStreamWarps * 32 == kRows, "a stream warp per 32 rows of a tile");
 template <int NMMA, bool TILED>
@@ -108,17 +139,18 @@ static_assert(kColSfb + 16 * kStages <= kTmemCols, "scale slots fit the tensor m
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
 constexpr int kSBytes = kRows * 16;        // weight block scales of a stage (tile-major layout)
 constexpr int kCcSlots = 3;                  // the stream warps' ring
-// a slot: a stage's codes, its scales, then the stage's activation chunks
-// decoded once (M <= 2 rows x 8 chunks of 16 f16x2 words and 2 scales, 80 bytes each)
+// a slot: a stage's codes, its scales, then the B fragments of the stage's 16
+// m16n8k16 MMAs per 16 rows (8 words x 32 lanes of 16 bytes, the activations'
+// block scales folded in), which the copy warp prepares
 constexpr int kCcXOff = kABytes + kSBytes;
-constexpr int kCcXChunk = 80;
-constexpr int kCcBytes = kCcXOff + 2 * 8 * kCcXChunk;
+constexpr int kCcFragBytes = 8 * 32 * 16;
+constexpr int kCcBytes = kCcXOff + kCcFragBytes;
 // ring: weight codes and activation codes (the weight scales go through
 // registers), then the stream warps' slots
 template <int NMMA, bool TILED>
 constexpr size_t smem_bytes()
 {
-    return (size_t)kStages * (kABytes + kBBytes) +
+    return (size_t)kStages * (kABytes + b_bytes<NMMA>()) +
            (has_stream<NMMA, TILED>() ? (size_t)kCcSlots * kCcBytes : 0) + 1024;  // + alignment
 }
 
@@ -354,17 +386,18 @@ __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cu
                    : z;
 }
 
-// ---- stream warps: whole tiles on the CUDA cores --------------------------------
-// The last tiles of every linear (tile-major weights, M <= 2) go to the stream
+// ---- stream warps: whole tiles beside the tensor pipe -----------------------------
+// The last tiles of every linear (tile-major weights, M <= 8) go to the stream
 // warps: CTA b takes whole tiles, a contiguous range of them cut near an equal
-// share of their stages.  One lane copies each stage's 16 KB of codes and
+// share of their stages.  The copy warp brings each stage's 16 KB of codes and
 // 2 KB of scales (two contiguous blocks) into a ring of kCcSlots shared-memory
-// slots; stream warp w owns rows 32 w .. 32 w + 31 of the tile, a row per
-// lane, and per stage runs the CUDA-core MAC of the single-linear stream (exact
-// E2M1 block sums in packed FP16, one FP32 FMA per 16-block with the scale
-// product) over the row's 256 elements against the activation chunks (the
-// same for every lane: broadcast loads).  The lane sums its row in stage
-// order and writes Y at the tile's end: no partial leaves the CTA.
+// slots and writes the stage's activation B fragments into the slot; compute
+// warp w owns rows 32 w .. 32 w + 31 of the tile and runs the single-linear
+// split-K kernel's MAC on them (E2M1 codes decoded to f16 with the 16-block
+// scale folded in exactly, mma.sync m16n8k16, FP32 accumulation) -- the legacy
+// MMA path, which the tcgen05 MMAs of the other warps leave free.  A tile's
+// sums stay in the warp in stage order and go to Y at the tile's end: no
+// partial leaves the CTA.
 // Stages of the stream warps' tiles before `g`'s tile boundary: the first
 // boundary at or after stage `target` of their list (items in order, tiles
 // ttiles.. of each).
@@ -459,25 +492,38 @@ __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t 
                 ::"r"(dst + kABytes), "l"(it.ws + blk * kSBytes), "r"(kSBytes), "r"(fb)
                 : "memory");
         }
-        if (lane < 8 * p.m) {
-            // chunk ch of activation row m: the K elements 256 st + 32 ch ..
-            const int m = lane >> 3, ch = lane & 7;
-            const int64_t cidx = (int64_t)c.st * 8 + ch;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(it.xq + m * (int64_t)(it.k / 2) + 16 * cidx));
-            const uint32_t sc2 = __ldg(reinterpret_cast<const unsigned short*>(
-                it.xs + m * (int64_t)(it.k / 16) + 2 * cidx));
-            uint32_t h[16];
-            e2m1x8_to_f16(v.x, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
-            e2m1x8_to_f16(v.y, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
-            e2m1x8_to_f16(v.z, *reinterpret_cast<uint32_t(*)[4]>(&h[8]));
-            e2m1x8_to_f16(v.w, *reinterpret_cast<uint32_t(*)[4]>(&h[12]));
-            const float2 f = e4m3x2_to_float2(sc2);
-            uint4* xo = reinterpret_cast<uint4*>(sC + slot * kCcBytes + kCcXOff + (m * 8 + ch) * kCcXChunk);
-            xo[0] = make_uint4(h[0], h[1], h[2], h[3]);
-            xo[1] = make_uint4(h[4], h[5], h[6], h[7]);
-            xo[2] = make_uint4(h[8], h[9], h[10], h[11]);
-            xo[3] = make_uint4(h[12], h[13], h[14], h[15]);
-            xo[4] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), 0u, 0u);
+        {
+            // B fragments of the stage for the mma.sync MAC: lane (g, t) of
+            // the compute warps takes, for code word w, the 8 elements at
+            // (w < 4 ? 0 : 128) + 32 t + 8 (w & 3) of the stage from its rows;
+            // its B fragment is activation row g at the same 8 elements, each
+            // times its block scale (exact in f16), and zero for rows g >= M
+            const int g = lane >> 2, t = lane & 3;
+            uint4* fo = reinterpret_cast<uint4*>(sC + slot * kCcBytes + kCcXOff);
+            if (g < p.m) {
+                const uint8_t* xr = it.xq + g * (int64_t)(it.k / 2) + (int64_t)c.st * 128;
+                const uint8_t* sr = it.xs + g * (int64_t)(it.k / 16) + (int64_t)c.st * 16;
+                const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * t));
+                const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(xr + 64 + 16 * t));
+                const uint32_t s01 = e4m3x2_to_f16x2_bits(
+                    __ldg(reinterpret_cast<const unsigned short*>(sr + 2 * t)));
+                const uint32_t s23 = e4m3x2_to_f16x2_bits(
+                    __ldg(reinterpret_cast<const unsigned short*>(sr + 8 + 2 * t)));
+                const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const uint32_t ps = w < 4 ? s01 : s23;
+                    const uint32_t sc = (w & 2) ? f16x2_dup_hi(ps) : f16x2_dup_lo(ps);
+                    uint32_t h[4];
+                    e2m1x8_to_f16(words[w], h);
+                    fo[w * 32 + lane] = make_uint4(f16x2_mul(h[0], sc), f16x2_mul(h[1], sc),
+                                                   f16x2_mul(h[2], sc), f16x2_mul(h[3], sc));
+                }
+            } else {
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    fo[w * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
+            }
             __threadfence_block();
         }
         __syncwarp();
@@ -496,71 +542,94 @@ __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t 
     }
 }
 
-// A compute warp: row 32 w + lane of every tile of the CTA's stream range.
-template <int M>
+// A compute warp (M <= 8): rows
+// 32 w + 16 b + g and + 8 (b = 0, 1) of every tile of the CTA's stream range.
+// Lane (g, t) reads 16-byte chunks t and 4 + t of its two rows in the
+// swizzled image (row r's chunk c at r * 128 + ((c ^ (r & 7)) << 4), and
+// r & 7 = g), folds each 16-block's scale into the decoded codes (exact in
+// f16) and runs two m16n8k16 MMAs per code word against the copy warp's B
+// fragments (the same element order), FP32 accumulation in stage order.
 __device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uint8_t* sC,
-                           uint64_t* full, uint64_t* empty, volatile int* abort_flag, int w,
-                           int lane)
+                               uint64_t* full, uint64_t* empty, volatile int* abort_flag, int w,
+                               int lane)
 {
-    const int rr = 32 * w + lane;  // row within the tile
+    const int g = lane >> 2, t = lane & 3;
     CcCursor c;
     cc_cursor_at(c, p, lo);
-    float acc[M];
+    float acc[2][4], acc2[2][4];
 #pragma unroll
-    for (int m = 0; m < M; ++m)
-        acc[m] = 0.f;
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            acc[b][q] = acc2[b][q] = 0.f;
     for (int64_t i = 0; i < cnt; ++i) {
         const int slot = (int)(i % kCcSlots);
-        // warp-uniform: every lane leaves together
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[slot]), (uint32_t)((i / kCcSlots) & 1),
                                                abort_flag, p.status)))
             break;
         const TcItem& it = p.item[c.item];
         const uint8_t* sl = sC + slot * kCcBytes;
-        // the row's 16 scale bytes of this stage: bytes 2c, 2c + 1 for chunk c
-        const uint4 sc4 = *reinterpret_cast<const uint4*>(sl + kABytes + rr * 16);
-        const uint32_t scw[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+        const uint4* xf = reinterpret_cast<const uint4*>(sl + kCcXOff) + lane;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            // chunk ch of the row in the swizzled image: 16 bytes at rr * 128 + ((ch ^ (rr & 7)) << 4)
-            const uint4 cw = *reinterpret_cast<const uint4*>(sl + rr * 128 + ((ch ^ (rr & 7)) << 4));
-            uint32_t wh[16];
-            decode_w_chunk(cw, wh);
-            const float2 sw = e4m3x2_to_float2((ch & 1) ? scw[ch >> 1] >> 16 : scw[ch >> 1] & 0xFFFFu);
-            XChunk<M> x;  // the copy warp's decode of the chunk (the same for every lane)
+        for (int b = 0; b < 2; ++b) {
+            const int ra = 32 * w + 16 * b + g, rb = ra + 8;
+            const uint4 a0 = *reinterpret_cast<const uint4*>(sl + ra * 128 + ((t ^ g) << 4));
+            const uint4 a1 = *reinterpret_cast<const uint4*>(sl + ra * 128 + (((4 + t) ^ g) << 4));
+            const uint4 b0 = *reinterpret_cast<const uint4*>(sl + rb * 128 + ((t ^ g) << 4));
+            const uint4 b1 = *reinterpret_cast<const uint4*>(sl + rb * 128 + (((4 + t) ^ g) << 4));
+            const uint8_t* sa = sl + kABytes + ra * 16;
+            const uint8_t* sb = sl + kABytes + rb * 16;
+            const uint32_t sa01 = e4m3x2_to_f16x2_bits(*reinterpret_cast<const unsigned short*>(sa + 2 * t));
+            const uint32_t sa23 = e4m3x2_to_f16x2_bits(*reinterpret_cast<const unsigned short*>(sa + 8 + 2 * t));
+            const uint32_t sb01 = e4m3x2_to_f16x2_bits(*reinterpret_cast<const unsigned short*>(sb + 2 * t));
+            const uint32_t sb23 = e4m3x2_to_f16x2_bits(*reinterpret_cast<const unsigned short*>(sb + 8 + 2 * t));
+            const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                const uint4* xi = reinterpret_cast<const uint4*>(sl + kCcXOff + (m * 8 + ch) * kCcXChunk);
+            for (int wd = 0; wd < 8; ++wd) {
+                const uint32_t pa = wd < 4 ? sa01 : sa23, pb = wd < 4 ? sb01 : sb23;
+                const uint32_t sA = (wd & 2) ? f16x2_dup_hi(pa) : f16x2_dup_lo(pa);
+                const uint32_t sB = (wd & 2) ? f16x2_dup_hi(pb) : f16x2_dup_lo(pb);
+                uint32_t ha[4], hb[4];
+                e2m1x8_to_f16(wa[wd], ha);
+                e2m1x8_to_f16(wb[wd], hb);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint4 v = xi[q];
-                    x.h[m][4 * q] = v.x;
-                    x.h[m][4 * q + 1] = v.y;
-                    x.h[m][4 * q + 2] = v.z;
-                    x.h[m][4 * q + 3] = v.w;
+                    ha[q] = f16x2_mul(ha[q], sA);
+                    hb[q] = f16x2_mul(hb[q], sB);
                 }
-                const uint4 sv = xi[4];
-                x.s[m][0] = __uint_as_float(sv.x);
-                x.s[m][1] = __uint_as_float(sv.y);
+                const uint4 xb = xf[wd * 32];
+                mma_m16n8k16(acc[b], ha[0], hb[0], ha[1], hb[1], xb.x, xb.y);
+                mma_m16n8k16(acc2[b], ha[2], hb[2], ha[3], hb[3], xb.z, xb.w);
             }
-            float t[M];
-            mac_chunk<M>(wh, sw, x, t);
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-                acc[m] += t[m];
         }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(&empty[slot]));
         if (c.st == c.nst - 1) {
-            const int64_t row = (int64_t)c.tile * kRows + rr;
             const float gxw = __fmul_rn(__ldg(it.xg), __ldg(it.wg));
             const OutY y = {it.y, p.y_bf16};
+            const int m0 = 2 * t, m1 = m0 + 1;
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                if (row < it.n)
-                    store_y(y, (int64_t)m * it.n + row, acc[m] * gxw);
-                acc[m] = 0.f;
+            for (int b = 0; b < 2; ++b) {
+                const int64_t ra = (int64_t)c.tile * kRows + 32 * w + 16 * b + g, rb = ra + 8;
+                const float d[4] = {acc[b][0] + acc2[b][0], acc[b][1] + acc2[b][1],
+                                    acc[b][2] + acc2[b][2], acc[b][3] + acc2[b][3]};
+                if (m0 < p.m) {
+                    if (ra < it.n)
+                        store_y(y, (int64_t)m0 * it.n + ra, d[0] * gxw);
+                    if (rb < it.n)
+                        store_y(y, (int64_t)m0 * it.n + rb, d[2] * gxw);
+                }
+                if (m1 < p.m) {
+                    if (ra < it.n)
+                        store_y(y, (int64_t)m1 * it.n + ra, d[1] * gxw);
+                    if (rb < it.n)
+                        store_y(y, (int64_t)m1 * it.n + rb, d[3] * gxw);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc[b][q] = acc2[b][q] = 0.f;
             }
         }
         cc_next(c, p);
@@ -585,6 +654,7 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
     const int32_t total = hi - lo;  // this CTA's stages
     // tile-aligned (1024-byte) ring: weight slots, then activation slots
     const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    constexpr int kBBytes = b_bytes<NMMA>();
     const uint32_t sA0 = ring, sB0 = ring + kStages * kABytes, sC0 = sB0 + kStages * kBBytes;
     uint8_t* sB_gen = smem_raw + (sB0 - smem_u32(smem_raw));
     const uint8_t* sC_gen = smem_raw + (sC0 - smem_u32(smem_raw));
@@ -966,16 +1036,13 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
         const int64_t all = cc_boundary(p, INT64_MAX);
         const int64_t lo = cc_boundary(p, all * blockIdx.x / gridDim.x);
         const int64_t cnt = cc_boundary(p, all * (blockIdx.x + 1) / gridDim.x) - lo;
-        if (cnt > 0 && p.m <= 2) {
+        if (cnt > 0 && p.m <= 8) {
             if (w == kStreamWarps) {
                 cc_produce(p, lo, cnt, sC0, smem_raw + (sC0 - smem_u32(smem_raw)), cfull_bar,
                            cempty_bar, abort_flag, lane);
             } else {
                 asm volatile("griddepcontrol.wait;" ::: "memory");  // x_q / x_s come from the producer
-                if (p.m == 1)
-                    cc_consume<1>(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
-                else
-                    cc_consume<2>(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
+                cc_consume(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
             }
         }
     }
@@ -1075,10 +1142,11 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
     cudaError_t e = device_status_address(&prm.status);
     if (e != cudaSuccess)
         return e;
-    // at M <= 2, with tile-major weights, the stream warps take the last tiles
+    // at M <= 8, with tile-major weights, the stream warps take the last tiles
     // of every linear (a share of its tiles, at least one left to the tensor
     // cores)
-    const bool rows_to_stream = m <= 2 && tiled;
+    const bool rows_to_stream = m <= 8 && tiled;
+    const int64_t share = rows_to_stream ? kStreamShare[m] : 0;
     int64_t stages = 0;
     for (int i = 0; i < count; ++i) {
         const ChainLinear& L = items[i];
@@ -1098,8 +1166,7 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
         const int64_t tiles = (L.n + kRows - 1) / kRows;
         int64_t cc = 0;
         if (rows_to_stream) {
-            cc = (tiles * (m == 1 ? NVFP4_TC_STREAM_PERMILLE : NVFP4_TC_STREAM_PERMILLE_M2) + 500) /
-                 1000;
+            cc = (tiles * share + 500) / 1000;
             if (cc > tiles - 1)
                 cc = tiles - 1;
         }
