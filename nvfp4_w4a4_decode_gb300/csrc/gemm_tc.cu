@@ -11,8 +11,10 @@
 // One persistent CTA per SM streams a contiguous range of the 128-row weight
 // tiles of a list of independent linears (one linear is a list of one), K
 // whole per tile, through an 8-stage shared-memory ring.  Warp roles:
-//   warp 0      one thread issues the TMA loads (cp.async.bulk.tensor, 128-byte
-//               swizzle) of each stage's 128 x 256 weight codes;
+//   warp 0      one thread issues each stage's 128 x 256 weight-code copy: one
+//               contiguous 16 KB cp.async.bulk with tile-major weights (laid
+//               out in the swizzled shared-memory image when packed), a TMA
+//               box (cp.async.bulk.tensor, 128-byte swizzle) with row-major ones;
 //   warp 1      allocates tensor memory; one thread issues the MMAs: four
 //               K = 64 MMAs per stage into the tile's accumulator (two
 //               accumulators alternate, so the epilogue of one tile overlaps
@@ -24,6 +26,9 @@
 //               writes), loaded from global memory kPrefetch stages ahead;
 //   warps 6..9  epilogue: the accumulator out of tensor memory (tcgen05.ld),
 //               Y[m][row] = acc * gX * gW (FP32 or BF16).
+//   warps 10..14 (N = 16 with tile-major weights) the stream warps: the last
+//               tiles of every linear at M <= 16 on the legacy mma.sync path,
+//               beside the tcgen05 stream (see below).
 // Every wait is on an mbarrier with a clock budget: running out records
 // NVFP4_DEVICE_WAIT_TIMEOUT in the library's status word, every role stops,
 // the copies and MMAs already issued are drained (again bounded) and tensor
@@ -1056,7 +1061,7 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
             }
         }
     } else if constexpr (has_stream<NMMA, TILED>()) {
-        // ---- stream warps: the last tiles of every linear on the CUDA cores -------------
+        // ---- stream warps: the last tiles of every linear on mma.sync -------------------
         const int w = warp - kThreads / 32;  // compute warps 0 .. kStreamWarps - 1, then the copy warp
         const int64_t all = cc_boundary(p, INT64_MAX);
         const int64_t lo = cc_boundary(p, all * blockIdx.x / gridDim.x);
