@@ -166,8 +166,8 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       128 rows x K per work unit, so a lone call occupies
  *                       ceil(N / 128) SMs.  Results are exact sums up to FP32
  *                       rounding in the tensor core's own order.  With
- *                       tile-major weights (NVFP4_FLAG_W_TILED) at M <= 16
- *                       the last 7.5 % (M = 16) to 32 % (M = 1) of every
+ *                       tile-major weights (NVFP4_FLAG_W_TILED) at M <= 8
+ *                       the last 20 % (M = 8) to 32 % (M = 1) of every
  *                       linear's tiles (rounded, at least one tile left to the
  *                       tcgen05 MMAs) run on other warps of the same SMs
  *                       through mma.sync instead (f16 operands with the block
@@ -194,7 +194,7 @@ int nvfp4_gemm_smallm(const uint8_t* x_q, const uint8_t* x_s, const float* x_g,
  *                       row-major: every pipeline stage of the tensor-core
  *                       kernel is then one contiguous 16 KB bulk copy of
  *                       codes instead of 128 strided pieces, its scales one
- *                       contiguous 2 KB block, and at M <= 16 part of the
+ *                       contiguous 2 KB block, and at M <= 8 part of the
  *                       tiles go to a second stream (see NVFP4_KERNEL_TC).
  * NVFP4_FLAG_PDL        programmatic dependent launch: the kernel may start
  *                       while the previous kernel on the stream is still

@@ -27,7 +27,7 @@
 //   warps 6..9  epilogue: the accumulator out of tensor memory (tcgen05.ld),
 //               Y[m][row] = acc * gX * gW (FP32 or BF16).
 //   warps 10..14 (N = 16 with tile-major weights) the stream warps: the last
-//               tiles of every linear at M <= 16 on the legacy mma.sync path,
+//               tiles of every linear at M <= 8 on the legacy mma.sync path,
 //               beside the tcgen05 stream (see below).
 // Every wait is on an mbarrier with a clock budget: running out records
 // NVFP4_DEVICE_WAIT_TIMEOUT in the library's status word, every role stops,
@@ -121,19 +121,10 @@ constexpr int kThreads = 320;              // 10 warps of the tensor-core roles
 #ifndef NVFP4_TC_STREAM_SHARE_8
 #define NVFP4_TC_STREAM_SHARE_8 200
 #endif
-#ifndef NVFP4_TC_STREAM_SHARE_12
-#define NVFP4_TC_STREAM_SHARE_12 150  // M = 9 .. 12 (two column tiles: ~1 % gained)
-#endif
-#ifndef NVFP4_TC_STREAM_SHARE_16
-#define NVFP4_TC_STREAM_SHARE_16 75  // M = 13 .. 16
-#endif
-constexpr int kStreamShare[17] = {
-    0, NVFP4_TC_STREAM_SHARE_1, NVFP4_TC_STREAM_SHARE_2, NVFP4_TC_STREAM_SHARE_3,
-    NVFP4_TC_STREAM_SHARE_4, NVFP4_TC_STREAM_SHARE_5, NVFP4_TC_STREAM_SHARE_6,
-    NVFP4_TC_STREAM_SHARE_7, NVFP4_TC_STREAM_SHARE_8, NVFP4_TC_STREAM_SHARE_12,
-    NVFP4_TC_STREAM_SHARE_12, NVFP4_TC_STREAM_SHARE_12, NVFP4_TC_STREAM_SHARE_12,
-    NVFP4_TC_STREAM_SHARE_16, NVFP4_TC_STREAM_SHARE_16, NVFP4_TC_STREAM_SHARE_16,
-    NVFP4_TC_STREAM_SHARE_16};
+constexpr int kStreamShare[9] = {0, NVFP4_TC_STREAM_SHARE_1, NVFP4_TC_STREAM_SHARE_2,
+                                    NVFP4_TC_STREAM_SHARE_3, NVFP4_TC_STREAM_SHARE_4,
+                                    NVFP4_TC_STREAM_SHARE_5, NVFP4_TC_STREAM_SHARE_6,
+                                    NVFP4_TC_STREAM_SHARE_7, NVFP4_TC_STREAM_SHARE_8};
 constexpr int kStreamWarps = NVFP4_TC_STREAM_WARPS;
 static_assert(kStreamWarps * 32 == kRows, "a stream warp per 32 rows of a tile");
 template <int NMMA, bool TILED>
@@ -153,13 +144,12 @@ static_assert(kColSfb + 16 * kStages <= kTmemCols, "scale slots fit the tensor m
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles a wait may take
 constexpr int kSBytes = kRows * 16;        // weight block scales of a stage (tile-major layout)
 constexpr int kCcSlots = 3;                  // the stream warps' ring
-// a slot: a stage's codes, its scales, then the B fragments of the stage's
-// m16n8k16 MMAs (per 8-column tile of activation rows: 8 words x 32 lanes of
-// 16 bytes, the activations' block scales folded in), which the copy warp
-// prepares; two column tiles for M = 9..16
+// a slot: a stage's codes, its scales, then the B fragments of the stage's 16
+// m16n8k16 MMAs per 16 rows (8 words x 32 lanes of 16 bytes, the activations'
+// block scales folded in), which the copy warp prepares
 constexpr int kCcXOff = kABytes + kSBytes;
 constexpr int kCcFragBytes = 8 * 32 * 16;
-constexpr int kCcBytes = kCcXOff + 2 * kCcFragBytes;
+constexpr int kCcBytes = kCcXOff + kCcFragBytes;
 // ring: weight codes and activation codes (the weight scales go through
 // registers), then the stream warps' slots
 template <int NMMA, bool TILED>
@@ -511,39 +501,33 @@ __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t 
             // B fragments of the stage for the mma.sync MAC: lane (g, t) of
             // the compute warps takes, for code word w, the 8 elements at
             // (w < 4 ? 0 : 128) + 32 t + 8 (w & 3) of the stage from its rows;
-            // its B fragment of column tile nt is activation row 8 nt + g at
-            // the same 8 elements, each times its block scale (exact in f16),
-            // and zero for rows past M
+            // its B fragment is activation row g at the same 8 elements, each
+            // times its block scale (exact in f16), and zero for rows g >= M
             const int g = lane >> 2, t = lane & 3;
-            const int ntiles = p.m > 8 ? 2 : 1;
-            for (int nt = 0; nt < ntiles; ++nt) {
-                const int row = 8 * nt + g;
-                uint4* fo = reinterpret_cast<uint4*>(sC + slot * kCcBytes + kCcXOff +
-                                                     nt * kCcFragBytes);
-                if (row < p.m) {
-                    const uint8_t* xr = it.xq + row * (int64_t)(it.k / 2) + (int64_t)c.st * 128;
-                    const uint8_t* sr = it.xs + row * (int64_t)(it.k / 16) + (int64_t)c.st * 16;
-                    const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * t));
-                    const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(xr + 64 + 16 * t));
-                    const uint32_t s01 = e4m3x2_to_f16x2_bits(
-                        __ldg(reinterpret_cast<const unsigned short*>(sr + 2 * t)));
-                    const uint32_t s23 = e4m3x2_to_f16x2_bits(
-                        __ldg(reinterpret_cast<const unsigned short*>(sr + 8 + 2 * t)));
-                    const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint4* fo = reinterpret_cast<uint4*>(sC + slot * kCcBytes + kCcXOff);
+            if (g < p.m) {
+                const uint8_t* xr = it.xq + g * (int64_t)(it.k / 2) + (int64_t)c.st * 128;
+                const uint8_t* sr = it.xs + g * (int64_t)(it.k / 16) + (int64_t)c.st * 16;
+                const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * t));
+                const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(xr + 64 + 16 * t));
+                const uint32_t s01 = e4m3x2_to_f16x2_bits(
+                    __ldg(reinterpret_cast<const unsigned short*>(sr + 2 * t)));
+                const uint32_t s23 = e4m3x2_to_f16x2_bits(
+                    __ldg(reinterpret_cast<const unsigned short*>(sr + 8 + 2 * t)));
+                const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const uint32_t ps = w < 4 ? s01 : s23;
-                        const uint32_t sc = (w & 2) ? f16x2_dup_hi(ps) : f16x2_dup_lo(ps);
-                        uint32_t h[4];
-                        e2m1x8_to_f16(words[w], h);
-                        fo[w * 32 + lane] = make_uint4(f16x2_mul(h[0], sc), f16x2_mul(h[1], sc),
-                                                       f16x2_mul(h[2], sc), f16x2_mul(h[3], sc));
-                    }
-                } else {
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        fo[w * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
+                for (int w = 0; w < 8; ++w) {
+                    const uint32_t ps = w < 4 ? s01 : s23;
+                    const uint32_t sc = (w & 2) ? f16x2_dup_hi(ps) : f16x2_dup_lo(ps);
+                    uint32_t h[4];
+                    e2m1x8_to_f16(words[w], h);
+                    fo[w * 32 + lane] = make_uint4(f16x2_mul(h[0], sc), f16x2_mul(h[1], sc),
+                                                   f16x2_mul(h[2], sc), f16x2_mul(h[3], sc));
                 }
+            } else {
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    fo[w * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
             }
             __threadfence_block();
         }
@@ -563,29 +547,26 @@ __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t 
     }
 }
 
-// A compute warp (NT 8-column tiles of activation rows: M <= 8 NT): rows
+// A compute warp (M <= 8): rows
 // 32 w + 16 b + g and + 8 (b = 0, 1) of every tile of the CTA's stream range.
 // Lane (g, t) reads 16-byte chunks t and 4 + t of its two rows in the
 // swizzled image (row r's chunk c at r * 128 + ((c ^ (r & 7)) << 4), and
 // r & 7 = g), folds each 16-block's scale into the decoded codes (exact in
 // f16) and runs two m16n8k16 MMAs per code word against the copy warp's B
 // fragments (the same element order), FP32 accumulation in stage order.
-template <int NT>
 __device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uint8_t* sC,
-                           uint64_t* full, uint64_t* empty, volatile int* abort_flag, int w,
-                           int lane)
+                               uint64_t* full, uint64_t* empty, volatile int* abort_flag, int w,
+                               int lane)
 {
     const int g = lane >> 2, t = lane & 3;
     CcCursor c;
     cc_cursor_at(c, p, lo);
-    float acc[2][NT][4], acc2[2][NT][4];
+    float acc[2][4], acc2[2][4];
 #pragma unroll
     for (int b = 0; b < 2; ++b)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                acc[b][nt][q] = acc2[b][nt][q] = 0.f;
+        for (int q = 0; q < 4; ++q)
+            acc[b][q] = acc2[b][q] = 0.f;
     for (int64_t i = 0; i < cnt; ++i) {
         const int slot = (int)(i % kCcSlots);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[slot]), (uint32_t)((i / kCcSlots) & 1),
@@ -622,12 +603,9 @@ __device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uin
                     ha[q] = f16x2_mul(ha[q], sA);
                     hb[q] = f16x2_mul(hb[q], sB);
                 }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const uint4 xb = xf[nt * (kCcFragBytes / 16) + wd * 32];
-                    mma_m16n8k16(acc[b][nt], ha[0], hb[0], ha[1], hb[1], xb.x, xb.y);
-                    mma_m16n8k16(acc2[b][nt], ha[2], hb[2], ha[3], hb[3], xb.z, xb.w);
-                }
+                const uint4 xb = xf[wd * 32];
+                mma_m16n8k16(acc[b], ha[0], hb[0], ha[1], hb[1], xb.x, xb.y);
+                mma_m16n8k16(acc2[b], ha[2], hb[2], ha[3], hb[3], xb.z, xb.w);
             }
         }
         __syncwarp();
@@ -636,30 +614,27 @@ __device__ void cc_consume(const TcParams& p, int64_t lo, int64_t cnt, const uin
         if (c.st == c.nst - 1) {
             const float gxw = __fmul_rn(__ldg(it.xg), __ldg(it.wg));
             const OutY y = {it.y, p.y_bf16};
+            const int m0 = 2 * t, m1 = m0 + 1;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const int64_t ra = (int64_t)c.tile * kRows + 32 * w + 16 * b + g, rb = ra + 8;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
-                    const float d[4] = {acc[b][nt][0] + acc2[b][nt][0], acc[b][nt][1] + acc2[b][nt][1],
-                                        acc[b][nt][2] + acc2[b][nt][2], acc[b][nt][3] + acc2[b][nt][3]};
-                    if (m0 < p.m) {
-                        if (ra < it.n)
-                            store_y(y, (int64_t)m0 * it.n + ra, d[0] * gxw);
-                        if (rb < it.n)
-                            store_y(y, (int64_t)m0 * it.n + rb, d[2] * gxw);
-                    }
-                    if (m1 < p.m) {
-                        if (ra < it.n)
-                            store_y(y, (int64_t)m1 * it.n + ra, d[1] * gxw);
-                        if (rb < it.n)
-                            store_y(y, (int64_t)m1 * it.n + rb, d[3] * gxw);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        acc[b][nt][q] = acc2[b][nt][q] = 0.f;
+                const float d[4] = {acc[b][0] + acc2[b][0], acc[b][1] + acc2[b][1],
+                                    acc[b][2] + acc2[b][2], acc[b][3] + acc2[b][3]};
+                if (m0 < p.m) {
+                    if (ra < it.n)
+                        store_y(y, (int64_t)m0 * it.n + ra, d[0] * gxw);
+                    if (rb < it.n)
+                        store_y(y, (int64_t)m0 * it.n + rb, d[2] * gxw);
                 }
+                if (m1 < p.m) {
+                    if (ra < it.n)
+                        store_y(y, (int64_t)m1 * it.n + ra, d[1] * gxw);
+                    if (rb < it.n)
+                        store_y(y, (int64_t)m1 * it.n + rb, d[3] * gxw);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc[b][q] = acc2[b][q] = 0.f;
             }
         }
         cc_next(c, p);
@@ -1066,16 +1041,13 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
         const int64_t all = cc_boundary(p, INT64_MAX);
         const int64_t lo = cc_boundary(p, all * blockIdx.x / gridDim.x);
         const int64_t cnt = cc_boundary(p, all * (blockIdx.x + 1) / gridDim.x) - lo;
-        if (cnt > 0 && p.m <= 16) {
+        if (cnt > 0 && p.m <= 8) {
             if (w == kStreamWarps) {
                 cc_produce(p, lo, cnt, sC0, smem_raw + (sC0 - smem_u32(smem_raw)), cfull_bar,
                            cempty_bar, abort_flag, lane);
             } else {
                 asm volatile("griddepcontrol.wait;" ::: "memory");  // x_q / x_s come from the producer
-                if (p.m > 8)
-                    cc_consume<2>(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
-                else
-                    cc_consume<1>(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
+                cc_consume(p, lo, cnt, sC_gen, cfull_bar, cempty_bar, abort_flag, w, lane);
             }
         }
     }
@@ -1175,10 +1147,10 @@ cudaError_t launch_tc_chain(const ChainLinear* items, int count, int m, bool qua
     cudaError_t e = device_status_address(&prm.status);
     if (e != cudaSuccess)
         return e;
-    // at M <= 16, with tile-major weights, the stream warps take the last tiles
+    // at M <= 8, with tile-major weights, the stream warps take the last tiles
     // of every linear (a share of its tiles, at least one left to the tensor
     // cores)
-    const bool rows_to_stream = m <= 16 && tiled;
+    const bool rows_to_stream = m <= 8 && tiled;
     const int64_t share = rows_to_stream ? kStreamShare[m] : 0;
     int64_t stages = 0;
     for (int i = 0; i < count; ++i) {

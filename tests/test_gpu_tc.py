@@ -375,17 +375,17 @@ def test_tc_chain_tiled_weights(nv, m):
     check_chain(lins)
 
 
-# linears whose last tiles go to the stream warps at every M <= 16 (three or
+# linears whose last tiles go to the stream warps at every M <= 8 (three or
 # more tiles), ragged N, one-tile linears that keep all rows on tcgen05, and K
 # from one stage (256) to 48 stages
 STREAM_SHAPES = [(300, 4096), (640, 256), (1000, 12288), (128, 512), (5 * 128 + 7, 1024),
                  (3 * 128, 2048)]
 
 
-@pytest.mark.parametrize("m", list(range(1, 9)) + [9, 12, 13, 16])
+@pytest.mark.parametrize("m", list(range(1, 9)) + [9, 16])
 def test_tc_stream_warps_match_oracle(nv, m):
-    """Tile-major chains at every M <= 8 and at M = 9..16 (two column tiles of
-    activation rows), where the last tiles of every linear
+    """Tile-major chains at every M <= 8 (and at M = 9, 16, where every tile
+    stays on the tcgen05 MMAs), where the last tiles of every linear
     run on the stream warps (mma.sync beside the tcgen05 MMAs): codes and
     outputs against the oracle, the same bits on a second run and from a CUDA
     graph, and the device status word clear."""
