@@ -184,7 +184,8 @@ class DecodeStack:
     * ``chain``: the step's 144 independent linears as one nvfp4_linear_chain
       call (one quantiser launch for all of them, one persistent GEMM launch),
       each linear with its own (x_q, x_s) -- the synthetic step's inputs are
-      all known when it starts.  M of 1 or 2."""
+      all known when it starts.  Any M up to 32 on the tensor cores (M <= 2 on
+      the CUDA-core stream)."""
 
     def __init__(self, nv, torch, m: int, layers: int, seed: int = 1234, pdl: bool = True,
                  fused: bool = True, kernel: int = 0, bf16: bool = False, mode: str = "launches",
@@ -1198,8 +1199,8 @@ def main():
                     help="the step as one multi-linear call (chain, M <= 2) or one call per "
                          "linear (launches); auto: chain where it applies")
     ap.add_argument("--chain-kernel", default="auto", choices=["auto", "gemv", "tc"],
-                    help="engine of the chain step (auto: CUDA-core stream at M <= 2, "
-                         "tensor cores above)")
+                    help="engine of the chain step (auto: the library's choice, the tensor "
+                         "cores at every M; gemv: the CUDA-core stream, M <= 2)")
     ap.add_argument("--row-major-weights", action="store_true",
                     help="the tensor-core chain reads the row-major packed weights (TMA with a "
                          "tensor map, no stream warps) instead of the tile-major repack "
