@@ -271,9 +271,33 @@ class DecodeStack:
                             for j in range(4)]
         torch.cuda.synchronize()
 
-    def _chain_entry(self, l: int, j: int):
+    def _chain_entry(self, l: int, j: int, x=None, y=None):
         wts = self.wt[l][j] if self.tiled else self.w[l][j]
-        return (self.x[l][j], self.xg[l][j], self.xq_item[l][j], wts, self.y[l][j])
+        return ((x or self.x)[l][j], self.xg[l][j], self.xq_item[l][j], wts, (y or self.y)[l][j])
+
+    def second_buffers(self):
+        """A second X / Y buffer set and the step over it as a chain on the same
+        weights and activation-code buffers (consecutive steps' kernels stay
+        ordered on the compute stream): (x_flat, y_flat, chain)."""
+        torch = self.torch
+        x2 = torch.empty_like(self.x_flat)
+        y2 = torch.empty_like(self.y_flat)
+        x2.copy_(self.x_flat)
+        xs, ys = [], []
+        xo = yo = 0
+        for l in range(self.layers):
+            xr, yr = [], []
+            for lin in self.lins:
+                xr.append(x2[xo:xo + self.m * lin.k].view(self.m, lin.k))
+                yr.append(y2[yo:yo + self.m * lin.n].view(self.m, lin.n))
+                xo += self.m * lin.k
+                yo += self.m * lin.n
+            xs.append(xr)
+            ys.append(yr)
+        ch = self.nv.Chain([self._chain_entry(l, j, xs, ys) for l in range(self.layers)
+                            for j in range(4)], kernel=self.chain_kernel,
+                           workspace=self.chain.workspace is not None)
+        return x2, y2, ch
 
     def weight_fp32(self, l: int, j: int):
         """FP32 weights of linear j of layer l, drawn on the device: N(0, 0.02^2),
@@ -766,7 +790,15 @@ def run_e2e(torch, stack, step_graph, args, world: int = 1) -> dict:
     activations from pinned host memory to the device, replays the step (the
     same graph of C-ABI calls) and reads all of its outputs back to pinned host
     memory -- both copies inside the timed region.  With several ranks: a
-    barrier on both sides, the slowest rank's time, all ranks' bytes."""
+    barrier on both sides, the slowest rank's time, all ranks' bytes.
+
+    In chain mode the steps alternate between two device buffer sets (two
+    graphs of the same chain call over the same weights), so that a step's
+    input copy (its own stream) runs while the previous step computes and its
+    output copy (another stream) while the next one does; every step still
+    copies all of its inputs in and all of its outputs out."""
+    if stack.mode == "chain":
+        return run_e2e_overlapped(torch, stack, step_graph, args, world)
     x_host = stack.x_flat.cpu().pin_memory()
     y_host = torch.empty(stack.y_flat.shape, dtype=stack.y_flat.dtype).pin_memory()
     h2d = x_host.numel() * x_host.element_size()
@@ -795,6 +827,60 @@ def run_e2e(torch, stack, step_graph, args, world: int = 1) -> dict:
             "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3),
             "path": "per step: pinned H2D of all activations, the step's CUDA graph of "
                     "nvfp4_linear calls, D2H of all outputs; wall clock"}
+
+
+def run_e2e_overlapped(torch, stack, step_graph, args, world: int = 1) -> dict:
+    x2, y2, chain2 = stack.second_buffers()
+    graph2 = stack.capture(lambda: chain2.run(pdl=stack.pdl))
+    xs, ys, graphs = (stack.x_flat, x2), (stack.y_flat, y2), (step_graph, graph2)
+    x_host = [stack.x_flat.cpu().pin_memory(), x2.cpu().pin_memory()]
+    y_host = [torch.empty(stack.y_flat.shape, dtype=stack.y_flat.dtype).pin_memory()
+              for _ in range(2)]
+    h2d = x_host[0].numel() * x_host[0].element_size()
+    d2h = y_host[0].numel() * y_host[0].element_size()
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {key: [torch.cuda.Event(), torch.cuda.Event()] for key in ("in", "comp", "out")}
+    used = [False, False]
+
+    def one_step(i):
+        b = i & 1
+        with torch.cuda.stream(cin):
+            if used[b]:
+                cin.wait_event(ev["comp"][b])     # the step that last read this X is done
+            xs[b].copy_(x_host[b], non_blocking=True)
+            ev["in"][b].record(cin)
+        comp.wait_event(ev["in"][b])
+        if used[b]:
+            comp.wait_event(ev["out"][b])         # this Y has been read back
+        graphs[b].replay()
+        ev["comp"][b].record(comp)
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev["comp"][b])
+            y_host[b].copy_(ys[b], non_blocking=True)
+            ev["out"][b].record(cout)
+        used[b] = True
+
+    for i in range(max(4, args.warmup)):
+        one_step(i)
+    torch.cuda.synchronize()
+    reps = max(10, args.steps // 3)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(reps):
+        one_step(i)
+    torch.cuda.synchronize()
+    sec = (time.perf_counter() - t0) / reps
+    barrier(world)
+    sec = reduce_max(sec, world)
+    b = stack.bytes_per_step()
+    v = world * (b["gemm"] + b["quant"]) / sec / 1e9
+    return {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3),
+            "path": "per step: pinned H2D of all activations (own stream), the step's CUDA "
+                    "graph of the nvfp4_linear_chain call, D2H of all outputs (own stream); "
+                    "two device buffer sets alternate so that the copies overlap the "
+                    "neighbouring steps' kernels; wall clock"}
 
 
 def profile_traffic(kernel: str):
