@@ -97,3 +97,30 @@ def test_decode_step_graph_matches_oracle(nv, mode, m, bf16, engine):
             assert err <= tol, (l, lin.name, err)
     del stack, g
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("m", [1, 8])
+def test_overlapped_end_to_end_buffers(nv, m):
+    """The benchmark's end-to-end loop in chain mode alternates two device
+    buffer sets (two graphs of the same chain call): the second set's step
+    gives the same bits as the first on the same inputs, and the loop itself
+    (host copies on their own streams, overlapping the neighbouring steps)
+    runs and leaves the first set's outputs unchanged."""
+    from types import SimpleNamespace
+    stack = bench.DecodeStack(nv, torch, m=m, layers=2, pdl=True, fused=False, mode="chain",
+                              tiled=True)
+    g = stack.capture(stack.step)
+    g.replay()
+    torch.cuda.synchronize()
+    ref = stack.y_flat.clone()
+    x2, y2, ch2 = stack.second_buffers()
+    assert torch.equal(x2, stack.x_flat)
+    y2.fill_(float("nan"))
+    ch2.run(pdl=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, ref)
+    res = bench.run_e2e(torch, stack, g, SimpleNamespace(warmup=3, steps=6), 1)
+    assert res["ms_per_step"] > 0 and res["h2d_bytes_per_step"] == stack.x_flat.numel() * 4
+    torch.cuda.synchronize()
+    assert torch.equal(stack.y_flat, ref)
+    assert nv.device_status() == 0
