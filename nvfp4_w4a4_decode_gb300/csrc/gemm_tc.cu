@@ -122,9 +122,9 @@ constexpr int kThreads = 320;              // 10 warps of the tensor-core roles
 #define NVFP4_TC_STREAM_SHARE_8 200
 #endif
 constexpr int kStreamShare[9] = {0, NVFP4_TC_STREAM_SHARE_1, NVFP4_TC_STREAM_SHARE_2,
-                                    NVFP4_TC_STREAM_SHARE_3, NVFP4_TC_STREAM_SHARE_4,
-                                    NVFP4_TC_STREAM_SHARE_5, NVFP4_TC_STREAM_SHARE_6,
-                                    NVFP4_TC_STREAM_SHARE_7, NVFP4_TC_STREAM_SHARE_8};
+                                 NVFP4_TC_STREAM_SHARE_3, NVFP4_TC_STREAM_SHARE_4,
+                                 NVFP4_TC_STREAM_SHARE_5, NVFP4_TC_STREAM_SHARE_6,
+                                 NVFP4_TC_STREAM_SHARE_7, NVFP4_TC_STREAM_SHARE_8};
 constexpr int kStreamWarps = NVFP4_TC_STREAM_WARPS;
 static_assert(kStreamWarps * 32 == kRows, "a stream warp per 32 rows of a tile");
 template <int NMMA, bool TILED>
@@ -403,9 +403,10 @@ __device__ __forceinline__ void aux_load(AuxLoad& a, const TcParams& p, const Cu
 // MMA path, which the tcgen05 MMAs of the other warps leave free.  A tile's
 // sums stay in the warp in stage order and go to Y at the tile's end: no
 // partial leaves the CTA.
-// Stages of the stream warps' tiles before `g`'s tile boundary: the first
-// boundary at or after stage `target` of their list (items in order, tiles
-// ttiles.. of each).
+// The stream warps' stage list: the linears in order, tiles ttiles .. of each,
+// K / 256 stages a tile.  The first tile boundary at or after stage `target`
+// of that list (its length when `target` is past the end), so that CTA ranges
+// cut there hold whole tiles.
 __device__ int64_t cc_boundary(const TcParams& p, int64_t target)
 {
     int64_t s = 0;
@@ -467,8 +468,8 @@ __device__ __forceinline__ void cc_next(CcCursor& c, const TcParams& p)
 
 // The copy warp: stage i of the CTA's stream range into slot i % kCcSlots,
 // once the compute warps have freed it (one lane issues the two bulk copies,
-// 8 M lanes decode the stage's activation chunks into the slot); then every
-// copy in flight lands.
+// every lane writes its B fragments of the stage into the slot and lane 0
+// arrives a second time when they are there); then every copy in flight lands.
 __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t sC0, uint8_t* sC,
                            uint64_t* full, uint64_t* empty, volatile int* abort_flag, int lane)
 {
@@ -533,7 +534,7 @@ __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t 
         }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(fb);  // the decoded activations are in the slot
+            mbar_arrive(fb);  // the B fragments are in the slot
         issued = i + 1;
         cc_next(c, p);
     }
@@ -547,8 +548,8 @@ __device__ void cc_produce(const TcParams& p, int64_t lo, int64_t cnt, uint32_t 
     }
 }
 
-// A compute warp (M <= 8): rows
-// 32 w + 16 b + g and + 8 (b = 0, 1) of every tile of the CTA's stream range.
+// A compute warp (M <= 8): rows 32 w + 16 b + g and + 8 (b = 0, 1) of every
+// tile of the CTA's stream range.
 // Lane (g, t) reads 16-byte chunks t and 4 + t of its two rows in the
 // swizzled image (row r's chunk c at r * 128 + ((c ^ (r & 7)) << 4), and
 // r & 7 = g), folds each 16-block's scale into the decoded codes (exact in
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(tc_threads<NMMA, TILED>(), 1) tc_chain_kernel(
         }
         mbar_init(smem_u32(&drain_bar), 1);
         for (int s = 0; s < kCcSlots; ++s) {
-            mbar_init(smem_u32(&cfull_bar[s]), 2);  // the copies, and the decoded activations
+            mbar_init(smem_u32(&cfull_bar[s]), 2);  // the copies, and the B fragments
             mbar_init(smem_u32(&cempty_bar[s]), kStreamWarps);
         }
         abort_s = 0;
